@@ -1,0 +1,497 @@
+#!/usr/bin/env python3
+"""Benchmark of the Q8_0 hot path (row quantizer + qdot_t) on GB300.
+
+A step is one pass of the path over one batch: quantize the activation rows
+(pq_quantize_q8_0), then contract them with the resident Q8_0 weights
+(pq_qdot_q8_0).  The headline workload is the decode projection
+M=1, K=4096, N=4096; its metric is weight GB/s (stored weight bytes,
+1.125 B per weight, per second).  The same line carries the prompt GEMM
+(M=512, K=4096, N=14336) as int8-equivalent TOPS (2*M*N*K per second) and the
+other workloads.
+
+Timing: W warm-up steps, then exactly K steps captured in one CUDA graph and
+replayed once, bracketed by a barrier and torch.cuda.synchronize(); the step
+time is taken with CUDA events on the launching stream, max over ranks.  Each
+step reads the next of B rotating copies of the weights, with B * bytes
+>= 2 x L2, so a step never finds its weights in L2.  External event nodes
+around every kernel in the graph give each kernel's average duration for the
+roofline.  SM clocks and throttle reasons are sampled through NVML during the
+timed region.
+
+``--impl reference`` times the CPU oracle (the plain C reference) on the same
+workload and metric on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gemm_q8_qdot_gb300 import workloads  # noqa: E402
+
+METRIC = "Q8_0 matvec weight GB/s (M=1) & int8 GEMM TOPS (M=512), % of roofline"
+HEADLINE = "decode_m1_k4096_n4096"
+PROMPT = "prompt_m512_k4096_n14336"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+KERNEL_SOURCES = {
+    "qdot_simt": ["gemm_q8_qdot_gb300/csrc/qdot_simt.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
+    "qdot_tc": ["gemm_q8_qdot_gb300/csrc/qdot_tc.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
+    "quantize": ["gemm_q8_qdot_gb300/csrc/quantize.cu"],
+}
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from profiles/dram_traffic.md, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    try:
+        digest = source_digest(KERNEL_SOURCES[kernel])
+        with open(path) as f:
+            for line in f:
+                cells = [c.strip() for c in line.strip().strip("|").split("|")]
+                if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload and cells[2] == digest:
+                    return float(cells[3])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML in a thread."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device_index: int = 0, period_s: float = 0.002):
+        self.samples: list[tuple[float, int, int]] = []
+        self.period = period_s
+        self.ok = False
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            import torch
+            props = torch.cuda.get_device_properties(torch_device_index)
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0".encode()
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(torch_device_index), ctypes.byref(h)) != 0:
+                    return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self.nv, self.h, self.ok = nv, h, True
+        except Exception:
+            self.ok = False
+
+    def _sample(self):
+        mhz = ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz))
+        fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        fn(self.h, ctypes.byref(reasons))
+        self.samples.append((time.perf_counter(), int(mhz.value), int(reasons.value)))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread:
+            self._stop.set()
+            self._thread.join()
+            self._sample()
+
+    def summary(self, t0: float, t1: float):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["nvml unavailable"]}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1] or self.samples[-2:]
+        reasons = set()
+        for _, _, r in inside:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def make_event():
+    """A timing event that becomes an event-record node when captured in a graph."""
+    import torch
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return _DriverEvent()
+
+
+class _DriverEvent:
+    """Driver-API event recorded with CU_EVENT_RECORD_EXTERNAL (for torch without `external`)."""
+    _cu = None
+
+    def __init__(self):
+        if _DriverEvent._cu is None:
+            _DriverEvent._cu = ctypes.CDLL("libcuda.so.1")
+        self.ev = ctypes.c_void_p()
+        assert self._cu.cuEventCreate(ctypes.byref(self.ev), 0) == 0
+
+    def record(self, stream=None):
+        import torch
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        assert self._cu.cuEventRecordWithFlags(self.ev, ctypes.c_void_p(s), 1) == 0
+
+    def elapsed_time(self, other) -> float:
+        ms = ctypes.c_float()
+        fn = getattr(self._cu, "cuEventElapsedTime_v2", None) or self._cu.cuEventElapsedTime
+        assert fn(ctypes.byref(ms), self.ev, other.ev) == 0
+        return float(ms.value)
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_units: float, per_rank_seconds: float, world: int, device=None):
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    t = max_over_ranks(per_rank_seconds, world, device)
+    return per_rank_units * world / t, t
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class Problem:
+    """Device buffers of one workload: f32 activations, rotating Q8_0 weight copies, outputs."""
+
+    def __init__(self, pq, wl: workloads.Workload, device):
+        import torch
+        self.wl = wl
+        self.pq = pq
+        x = workloads.activations(wl)
+        self.x_host = torch.from_numpy(x).pin_memory()
+        self.x = self.x_host.to(device)
+        w = torch.from_numpy(workloads.weights(wl)).to(device)
+        W, WS = pq.quantize_q8_0(w)
+        del w
+        wbytes = W.numel() + WS.numel() * 4
+        self.copies = max(2, -(-2 * L2_BYTES // wbytes))
+        self.W = [W] + [W.clone() for _ in range(self.copies - 1)]
+        self.WS = [WS] + [WS.clone() for _ in range(self.copies - 1)]
+        self.A = torch.empty((wl.M, wl.K), dtype=torch.int8, device=device)
+        self.AS = torch.empty((wl.M, wl.K // 32), dtype=torch.float32, device=device)
+        self.C = torch.empty((wl.M, wl.N), dtype=torch.float32, device=device)
+        self.C_host = torch.empty((wl.M, wl.N), dtype=torch.float32).pin_memory()
+        torch.cuda.synchronize()
+
+    def step(self, t: int, events=None):
+        if events is not None:
+            events[0].record()
+        self.pq.quantize_q8_0(self.x, self.A, self.AS)
+        if events is not None:
+            events[1].record()
+        self.pq.qdot_q8_0(self.A, self.AS, self.W[t % self.copies], self.WS[t % self.copies], self.C)
+        if events is not None:
+            events[2].record()
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """Bytes qdot_t must move per launch: W, WS, A, AS read once, C written once."""
+        wl = self.wl
+        return wl.weight_bytes + wl.M * wl.K + 4 * wl.M * (wl.K // 32) + 4 * wl.M * wl.N
+
+
+def time_graph(prob: Problem, steps: int, warmup: int, world: int, sampler=None):
+    import torch
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    # warm-up graph and timed graph (the timed one carries per-kernel event nodes)
+    with torch.cuda.stream(stream):
+        for t in range(2):
+            prob.step(t)  # eager warm-up of the launch path
+    stream.synchronize()
+    g_warm = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_warm, stream=stream):
+        for t in range(warmup):
+            prob.step(t)
+    evs = [[make_event() for _ in range(3)] for _ in range(steps)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for t in range(steps):
+            prob.step(warmup + t, evs[t])
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g_warm.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    barrier(world)
+    if sampler:
+        sampler.stop()
+    ms = start.elapsed_time(end)
+    quant_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in evs)
+    qdot_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in evs)
+    return ms, quant_ms, qdot_ms, (t0, t1)
+
+
+def time_e2e(prob: Problem, steps: int, warmup: int):
+    """Through the public API with host buffers: H2D of x, quantize, qdot, D2H of C, per step."""
+    import torch
+    torch.cuda.synchronize()
+    for t in range(warmup + steps):
+        if t == warmup:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        prob.x.copy_(prob.x_host, non_blocking=True)
+        prob.step(t)
+        prob.C_host.copy_(prob.C, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    dt = time.perf_counter() - t0
+    return dt, prob.x_host.numel() * 4, prob.C_host.numel() * 4
+
+
+def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str):
+    wl = prob.wl
+    if wl.M <= 64:
+        achieved = prob.algorithmic_bytes / (qdot_ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        kernel = "qdot_simt" if wl.M <= 8 else "qdot_tc"
+        traffic = recorded_traffic(kernel, wl.name)
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
+                "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes": prob.algorithmic_bytes}
+    achieved = wl.ops / (qdot_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = recorded_traffic("qdot_tc", wl.name)
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "qdot_tc",
+            "peak_source": f"{peak_src} bf16_tflops (f16 operands: same dense rate)",
+            "algorithmic_flops": wl.ops}
+
+
+def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sampler=None, e2e=False):
+    wl = workloads.WORKLOADS[name]
+    prob = Problem(pq, wl, device)
+    ms, quant_ms, qdot_ms, window = time_graph(prob, steps, warmup, world, sampler)
+    per_rank_s = ms * 1e-3
+    if wl.M == 1 or wl.M <= 64:
+        units, unit = wl.weight_bytes * steps, "GB/s"
+        scale = 1e9
+    else:
+        units, unit = wl.ops * steps, "TOPS"
+        scale = 1e12
+    value, t_max = aggregate(units, per_rank_s, world, device)
+    res = {"value": round(value / scale, 3), "unit": unit, "ms_per_step": round(t_max * 1e3 / steps, 5),
+           "kernel_ms": {"quantize": round(quant_ms, 5), "qdot": round(qdot_ms, 5)},
+           "roofline": roofline_for(prob, qdot_ms, peaks, peak_src), "weight_copies": prob.copies,
+           "window": window}
+    if e2e:
+        dt, h2d, d2h = time_e2e(prob, steps, warmup)
+        ev, _ = aggregate(units, dt, world, device)
+        res["e2e"] = {"value": round(ev / scale, 3), "unit": unit, "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h}
+    del prob
+    import torch
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline(name: str, budget_s: float = 10.0):
+    """The oracle, as it stands, on a bounded sample of the workload (rank 0, host cores)."""
+    import oracle
+    wl = workloads.WORKLOADS[name]
+    x = workloads.activations(wl)
+    qw, sw = oracle.quantize_q8_0(workloads.weights(wl))
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        qa, sa = oracle.quantize_q8_0(x)
+        oracle.qdot(qa, sa, qw, sw)
+        steps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s:
+            break
+    return {"value": round(wl.weight_bytes * steps / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "sample": f"{steps} full steps of {name} (quantize x + qdot_t, single thread) "
+                                        f"in {dt:.1f} s"}
+
+
+def reference_arm(args):
+    """--impl reference: the CPU oracle on the headline workload, on the host cores."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    wl = workloads.WORKLOADS[args.workload]
+    x = workloads.activations(wl)
+    qw, sw = oracle.quantize_q8_0(workloads.weights(wl))
+    # calibrate one full step; sample columns so that W + K steps stay near 60 s
+    t0 = time.perf_counter()
+    qa, sa = oracle.quantize_q8_0(x)
+    oracle.qdot(qa, sa, qw, sw)
+    full = time.perf_counter() - t0
+    budget = 60.0
+    frac = min(1.0, budget / max(1e-9, full * (args.steps + args.warmup)))
+    ncols = max(1, int(wl.N * frac))
+    qw_s, sw_s = qw[:ncols], sw[:ncols]
+    for _ in range(args.warmup):
+        qa, sa = oracle.quantize_q8_0(x)
+        oracle.qdot(qa, sa, qw_s, sw_s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        qa, sa = oracle.quantize_q8_0(x)
+        oracle.qdot(qa, sa, qw_s, sw_s)
+    dt = time.perf_counter() - t0
+    wbytes = ncols * wl.K + 4 * ncols * (wl.K // 32)
+    value = wbytes * args.steps / dt / 1e9
+    sample = f"{ncols} of {wl.N} weight rows per step ({args.steps} steps, single thread)"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64/f64",
+            "data": "synthetic", "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--no-others", action="store_true", help="time only the headline workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    import gemm_q8_qdot_gb300 as pq
+    pq.load()
+    peaks, peak_src = load_peaks()
+    sampler = ClockSampler(local)
+    head = run_workload(pq, args.workload, args.steps, args.warmup, world, device, peaks, peak_src,
+                        sampler=sampler, e2e=True)
+    clocks = sampler.summary(*head.pop("window"))
+    others = {}
+    if not args.no_others:
+        for name in (PROMPT, "ffn_up_m1_k4096_n14336", "ffn_down_m1_k14336_n4096",
+                     "smallm_m4_k4096_n11008", "smallm_m16_k4096_n11008", "smallm_m64_k4096_n11008"):
+            if name == args.workload:
+                continue
+            try:
+                r = run_workload(pq, name, args.steps, args.warmup, world, device, peaks, peak_src)
+                r.pop("window")
+                others[name] = r
+            except pq.PQError as e:
+                others[name] = {"error": str(e)}
+    launches_per_step = 2
+    line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "M": workloads.WORKLOADS[args.workload].M,
+                       "K": workloads.WORKLOADS[args.workload].K, "N": workloads.WORKLOADS[args.workload].N,
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": f"{head['weight_copies']} rotating weight copies (>= 2x L2 = {2 * L2_BYTES >> 20} MiB)",
+                       "timing": "K steps in one CUDA graph, events on the launching stream"},
+            "roofline": head["roofline"], "kernel_ms": head["kernel_ms"], "e2e": head["e2e"],
+            "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
+    if others:
+        line["other_workloads"] = others
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,113 @@
+// C ABI of libpq: argument checks, kernel selection by M, launch.
+//
+// Every check runs on the host before anything is enqueued; a failed check
+// returns a pq_status and writes nothing.  The pages' kernels instead trap at
+// entry on a bad extent, which leaves the CUDA context unusable ("Kernel ABI",
+// section "Entry checks"); a shared GPU must never see that.
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+#include "pq.h"
+#include "pq_internal.h"
+
+namespace {
+
+constexpr int64_t kMaxDim = int64_t(1) << 40;
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+
+int map_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return PQ_OK;
+    if (e == cudaErrorInvalidConfiguration || e == cudaErrorNotSupported) return PQ_ERR_UNSUPPORTED;
+    return PQ_ERR_CUDA;
+}
+
+// Shape checks shared by the qdot entry points: sizes >= 0, K a positive
+// multiple of 32, every element count representable.
+int check_qdot_shape(int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K <= 0 || (K % 32) != 0) return PQ_ERR_SHAPE;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return PQ_ERR_SHAPE;
+    // M*K, N*K, M*N and M*N*K/32 must fit in int64
+    const __int128 mk = (__int128)M * K, nk = (__int128)N * K, mn = (__int128)M * N;
+    const __int128 lim = (__int128)INT64_MAX;
+    if (mk > lim || nk > lim || mn > lim || mn * (K / 32) > lim) return PQ_ERR_SHAPE;
+    return PQ_OK;
+}
+
+int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C,
+              int32_t* S, int64_t M, int64_t N, int64_t K, int ws_layout, int path,
+              cudaStream_t stream) {
+    if (path != PQ_PATH_AUTO && path != PQ_PATH_SIMT && path != PQ_PATH_TC) return PQ_ERR_INVALID_ARG;
+    if (ws_layout != PQ_WS_N_KB && ws_layout != PQ_WS_KB_N) return PQ_ERR_INVALID_ARG;
+    int st = check_qdot_shape(M, N, K);
+    if (st != PQ_OK) return st;
+    if (M == 0 || N == 0) return PQ_OK;
+    const bool sums = S != nullptr;
+    if (!A || !W) return PQ_ERR_INVALID_ARG;
+    if (!sums && (!AS || !WS || !C)) return PQ_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(W, 16)) return PQ_ERR_ALIGN;
+    if (sums && !aligned(S, 4)) return PQ_ERR_ALIGN;
+    if (!sums && (!aligned(AS, 4) || !aligned(WS, 4) || !aligned(C, 4))) return PQ_ERR_ALIGN;
+
+    pq::QdotArgs a{A, AS, W, WS, C, S, M, N, K, ws_layout};
+    if (path == PQ_PATH_AUTO) path = (M <= 8) ? PQ_PATH_SIMT : PQ_PATH_TC;
+    cudaError_t e = (path == PQ_PATH_SIMT) ? pq::launch_qdot_simt(a, stream) : pq::launch_qdot_tc(a, stream);
+    return map_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pq_quantize_q8_0(const float* x, int8_t* q, float* s, int64_t rows, int64_t K, cudaStream_t stream) {
+    if (rows < 0 || K <= 0 || (K % 32) != 0 || rows > kMaxDim || K > kMaxDim) return PQ_ERR_SHAPE;
+    if ((__int128)rows * K > (__int128)INT64_MAX) return PQ_ERR_SHAPE;
+    if (rows == 0) return PQ_OK;
+    if (!x || !q || !s) return PQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(q, 16) || !aligned(s, 4)) return PQ_ERR_ALIGN;
+    return map_cuda(pq::launch_quantize(x, q, s, rows, K, stream));
+}
+
+int pq_qdot_q8_0(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C,
+                 int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    return qdot_impl(A, AS, W, WS, C, nullptr, M, N, K, PQ_WS_N_KB, PQ_PATH_AUTO, stream);
+}
+
+int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C,
+                    int64_t M, int64_t N, int64_t K, int ws_layout, int path, cudaStream_t stream) {
+    return qdot_impl(A, AS, W, WS, C, nullptr, M, N, K, ws_layout, path, stream);
+}
+
+int pq_qdot_q8_0_blocksums(const int8_t* A, const int8_t* W, int32_t* S, int64_t M, int64_t N,
+                           int64_t K, int path, cudaStream_t stream) {
+    int st = check_qdot_shape(M, N, K);
+    if (st != PQ_OK) return st;
+    if (M == 0 || N == 0) return PQ_OK;
+    if (!S) return PQ_ERR_INVALID_ARG;
+    if (path == PQ_PATH_AUTO) path = PQ_PATH_SIMT;
+    return qdot_impl(A, nullptr, W, nullptr, nullptr, S, M, N, K, PQ_WS_N_KB, path, stream);
+}
+
+int pq_check_device(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PQ_ERR_CUDA;
+    unsigned status = 0;
+    if (pq::read_and_clear_status(&status) != cudaSuccess) return PQ_ERR_CUDA;
+    return status ? PQ_ERR_TIMEOUT : PQ_OK;
+}
+
+const char* pq_strerror(int code) {
+    switch (code) {
+        case PQ_OK: return "ok";
+        case PQ_ERR_INVALID_ARG: return "invalid argument (null pointer or unknown code)";
+        case PQ_ERR_SHAPE: return "bad shape (negative size, K not a positive multiple of 32, or overflow)";
+        case PQ_ERR_ALIGN: return "misaligned base pointer";
+        case PQ_ERR_CUDA: return "CUDA runtime error";
+        case PQ_ERR_TIMEOUT: return "a bounded on-device wait gave up";
+        case PQ_ERR_UNSUPPORTED: return "unsupported device or shape for this path";
+        default: return "unknown pq_status";
+    }
+}
+
+int pq_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// Device helpers shared by the kernels of libpq (sm_103a): vector loads with
+// cache hints, packed byte arithmetic.  Inline PTX is written here by hand.
+#pragma once
+#include <cstdint>
+
+namespace pq {
+
+struct u32x8 {
+    uint32_t v[8];
+};
+
+// One Q8_0 block of bytes (32 B) in one 256-bit load, read-only path, not kept
+// in L1: the weight stream is touched once per launch.
+__device__ __forceinline__ u32x8 ld_stream_v8(const void* p) {
+    u32x8 r;
+    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]),
+                   "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
+                 : "l"(p));
+    return r;
+}
+
+// Same block, kept in L1: activation rows are re-read by every warp of a CTA.
+__device__ __forceinline__ u32x8 ld_cached_v8(const void* p) {
+    u32x8 r;
+    asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]),
+                   "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
+                 : "l"(p));
+    return r;
+}
+
+// A 32-byte block from a base that is only 16-byte aligned: two 128-bit loads.
+__device__ __forceinline__ u32x8 ld_stream_2v4(const void* p) {
+    u32x8 r;
+    asm("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]) : "l"(p));
+    asm("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
+                 : "l"(static_cast<const char*>(p) + 16));
+    return r;
+}
+
+template <bool kV8, bool kStream>
+__device__ __forceinline__ u32x8 ld_block(const void* p) {
+    if constexpr (kV8) {
+        if constexpr (kStream) return ld_stream_v8(p);
+        else return ld_cached_v8(p);
+    } else {
+        return ld_stream_2v4(p);
+    }
+}
+
+__device__ __forceinline__ float ld_f32_nc(const float* p) {
+    float r;
+    asm("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(p));
+    return r;
+}
+
+// Sum of the 32 signed-byte products of two Q8_0 blocks: eight dp4a.
+__device__ __forceinline__ int block_dot(const u32x8& a, const u32x8& w) {
+    int s = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) s = __dp4a(static_cast<int>(a.v[t]), static_cast<int>(w.v[t]), s);
+    return s;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
+}  // namespace pq

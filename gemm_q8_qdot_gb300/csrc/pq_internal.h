@@ -1,0 +1,33 @@
+// Host-side interface between the C-ABI layer (pq_api.cu) and the kernel
+// launchers.  Launchers assume validated arguments and return a cudaError_t.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+namespace pq {
+
+struct QdotArgs {
+    const int8_t* A;
+    const float* AS;
+    const int8_t* W;
+    const float* WS;
+    float* C;        // f32 [M, N] result, or null in block-sum mode
+    int32_t* S;      // int32 [M, N, K/32] block sums, or null
+    int64_t M, N, K;
+    int ws_layout;   // 0: WS [N, K/32]; 1: WS [K/32, N]
+};
+
+cudaError_t launch_quantize(const float* x, int8_t* q, float* s, int64_t rows, int64_t K,
+                            cudaStream_t stream);
+
+// dp4a streaming kernel: any M; returns cudaErrorInvalidConfiguration when the
+// grid would exceed the device limits.
+cudaError_t launch_qdot_simt(const QdotArgs& a, cudaStream_t stream);
+
+// tcgen05 tensor-core kernel.  cudaErrorNotSupported if the device is not sm_103.
+cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream);
+
+// Reads and clears the device status word (set by a bounded wait that gave up).
+cudaError_t read_and_clear_status(unsigned* status);
+
+}  // namespace pq

@@ -1,0 +1,146 @@
+/*
+ * pq.h — C ABI of the Q8_0 block-scaled contraction library (libpq.so) for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What it computes (Phobos documentation, "Quantized built-ins and formats",
+ * section "Q8_0", and "Phobos Language Spec", section 10 "Quantized
+ * built-ins", Q8_0 table):
+ *
+ *   Q8_0 stores signed bytes with one scale per block of 32 values;
+ *   activations are quantized the same way, so
+ *
+ *     C[i, j] = sum over blocks b of AS[i, b] * WS[j, b]
+ *                 * sum over k in b of A[i, k] * W[j, k]
+ *
+ *   with the inner (block) sum in integers.  A is [M, K] int8, AS [M, K/32]
+ *   f32, W [N, K] int8, WS [N, K/32] f32 (qdot_t's layout; qmma_t's
+ *   [K/32, N] is selected with PQ_WS_KB_N), C [M, N] f32.
+ *
+ * Conventions shared by every entry point:
+ *
+ *   Memory.  All tensors are row-major and dense (the innermost index is
+ *   contiguous, no padding).  Every pointer is a DEVICE pointer owned by the
+ *   caller; the library never frees it, keeps it, or allocates per call.
+ *   Base alignment: int8 tensors (A, W, q) and f32 inputs read as vectors
+ *   (x) start on a 16-byte boundary; the f32 scale planes and C on a 4-byte
+ *   boundary.  (The pages ask 16 bytes of every tensor base, "Kernel ABI",
+ *   section "Memory layout and alignment".)
+ *
+ *   Streams.  Work is enqueued on `stream` (0 = the legacy default stream) and
+ *   runs asynchronously: PQ_OK means "validated and enqueued".  Results are
+ *   visible after the stream is synchronized.
+ *
+ *   Errors.  Every precondition is checked on the host BEFORE anything is
+ *   launched, and a failed check returns a negative pq_status with nothing
+ *   enqueued and no byte written (the pages' kernels trap on a bad extent and
+ *   leave the CUDA context unusable, "Kernel ABI", "Entry checks"; this
+ *   library never traps).  PQ_ERR_CUDA reports a launch failure returned by
+ *   the CUDA runtime.  Empty problems (M == 0, N == 0 or rows == 0) return
+ *   PQ_OK and launch nothing.
+ *
+ *   Shapes.  K must be a positive multiple of 32 (one whole Q8_0 block).  M
+ *   and N need not be multiples of any tile: the kernels mask ragged edges
+ *   themselves.  All sizes are int64; products such as M*K must fit in int64
+ *   and the grid limits of the device (checked, PQ_ERR_SHAPE).
+ *
+ *   Values.  Any int8 is a valid qdot operand, including -128 (which the
+ *   quantizer never emits).  Scales may be any finite f32.  NaN or Inf inputs
+ *   give unspecified outputs.
+ */
+#ifndef PQ_H
+#define PQ_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PQ_OK = 0,
+    PQ_ERR_INVALID_ARG = -1, /* null pointer, unknown path or layout code */
+    PQ_ERR_SHAPE = -2,       /* negative size, K not a positive multiple of 32, size overflow */
+    PQ_ERR_ALIGN = -3,       /* a base pointer below the alignment stated above */
+    PQ_ERR_CUDA = -4,        /* the CUDA runtime refused a launch or a query */
+    PQ_ERR_TIMEOUT = -5,     /* a bounded on-device wait gave up (reported by pq_check_device) */
+    PQ_ERR_UNSUPPORTED = -6  /* the device is not sm_103 / the path cannot take this shape */
+} pq_status;
+
+/* Kernel path selector for pq_qdot_q8_0_ex / pq_qdot_q8_0_blocksums. */
+enum {
+    PQ_PATH_AUTO = 0,  /* by M: the dp4a streaming kernels for small M, tensor cores above */
+    PQ_PATH_SIMT = 1,  /* dp4a (CUDA-core) streaming kernel, any M */
+    PQ_PATH_TC = 2     /* tcgen05 tensor-core kernel (f16 operands, exact integer block sums) */
+};
+
+/* Layout of the weight-scale plane WS. */
+enum {
+    PQ_WS_N_KB = 0,  /* WS [N, K/32]: qdot_t */
+    PQ_WS_KB_N = 1   /* WS [K/32, N]: qmma_t ("w_scales is [K/32, N], transposed relative to qdot_t") */
+};
+
+/*
+ * Row quantizer f32 -> Q8_0 ("Quantized built-ins and formats", section
+ * "Q8_0": one f32 scale per 32 signed bytes; activations are quantized the
+ * same way as weights).  For every row r and block b of 32 elements:
+ *   amax = max |x|,  d = amax / 127 (IEEE f32 division),
+ *   q = round(x / d) with ties to even (the spec's round(), section 9),
+ *   clamped to [-127, 127];  a block with d == 0 stores q = 0.
+ * x: f32 [rows, K] (16-byte aligned), q: int8 [rows, K] (16-byte aligned),
+ * s: f32 [rows, K/32] (4-byte aligned).  Outputs are overwritten.  x must
+ * not overlap q or s.
+ */
+int pq_quantize_q8_0(const float* x, int8_t* q, float* s,
+                     int64_t rows, int64_t K, cudaStream_t stream);
+
+/*
+ * qdot_t: C[M, N] = Q8_0 contraction of A [M, K] with W [N, K] as stated at
+ * the top of this header ("Quantized built-ins and formats", section "Q8_0";
+ * the example kernel's argument order A, AS, W, WS, C).  C is overwritten
+ * (the pages' example assigns the result).  The kernel is chosen by M.
+ * C must not overlap any input.
+ */
+int pq_qdot_q8_0(const int8_t* A, const float* AS, const int8_t* W, const float* WS,
+                 float* C, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * As pq_qdot_q8_0, with the weight-scale layout (PQ_WS_N_KB for qdot_t,
+ * PQ_WS_KB_N for qmma_t, spec section 10) and the kernel path chosen by the
+ * caller (PQ_PATH_*).  PQ_ERR_UNSUPPORTED if the chosen path cannot take
+ * the shape.
+ */
+int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const float* WS,
+                    float* C, int64_t M, int64_t N, int64_t K,
+                    int ws_layout, int path, cudaStream_t stream);
+
+/*
+ * The integer stage alone, for verification: S[i, j, b] = sum over k in
+ * block b of A[i, k] * W[j, k] ("Quantized built-ins and formats": "the
+ * inner sum in integers"), computed by the engine of `path` (PQ_PATH_SIMT:
+ * dp4a; PQ_PATH_TC: the tensor-core MMA with f32 accumulation, exact because
+ * every partial sum is an integer below 2^24).  S: int32 [M, N, K/32],
+ * 4-byte aligned, overwritten.  |S| <= 32 * 128 * 128 = 524288.
+ */
+int pq_qdot_q8_0_blocksums(const int8_t* A, const int8_t* W, int32_t* S,
+                           int64_t M, int64_t N, int64_t K, int path, cudaStream_t stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears this library's device status
+ * word for the current device.  Returns PQ_OK, PQ_ERR_TIMEOUT if a kernel's
+ * bounded wait gave up since the last check (its output is then invalid), or
+ * PQ_ERR_CUDA if the synchronize failed.
+ */
+int pq_check_device(cudaStream_t stream);
+
+/* A static, human-readable name for a pq_status code. */
+const char* pq_strerror(int code);
+
+/* ABI version of this header: major * 100 + minor. */
+int pq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PQ_H */

@@ -1,0 +1,113 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+* libpq.so builds for sm_103a and exports every function include/pq.h declares;
+* every precondition is rejected on the host with the documented pq_status
+  before anything is launched (these calls never reach the device, so they
+  are safe on a machine without a GPU and on a GPU machine alike).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gemm_q8_qdot_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pq_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_qdot_q8_0_blocksums",
+              "pq_check_device", "pq_strerror", "pq_version"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in include/pq.h but not exported"
+    assert set(binding.EXPORTS) <= set(declared_functions())
+
+
+def test_version_and_strerror(lib):
+    assert lib.pq_version() == 100
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.pq_strerror(code).decode()
+    assert "unknown" in lib.pq_strerror(99).decode()
+
+
+# Fake, never-dereferenced device addresses: a failed check returns before any CUDA call.
+P16 = 0x10000000          # 16-byte (and 256-byte) aligned
+P8 = 0x10000008           # 8-byte aligned only
+P2 = 0x10000002
+
+
+def qdot(lib, A=P16, AS=P16, W=P16, WS=P16, C=P16, M=1, N=1, K=32, layout=0, path=0):
+    return lib.pq_qdot_q8_0_ex(A, AS, W, WS, C, M, N, K, layout, path, None)
+
+
+@pytest.mark.parametrize("K", [0, -32, 16, 33, 100])
+def test_bad_k(lib, K):
+    assert qdot(lib, K=K) == binding.PQ_ERR_SHAPE
+    assert lib.pq_qdot_q8_0(P16, P16, P16, P16, P16, 1, 1, K, None) == binding.PQ_ERR_SHAPE
+    assert lib.pq_quantize_q8_0(P16, P16, P16, 1, K, None) == binding.PQ_ERR_SHAPE
+    assert lib.pq_qdot_q8_0_blocksums(P16, P16, P16, 1, 1, K, 1, None) == binding.PQ_ERR_SHAPE
+
+
+def test_negative_and_overflowing_sizes(lib):
+    assert qdot(lib, M=-1) == binding.PQ_ERR_SHAPE
+    assert qdot(lib, N=-5) == binding.PQ_ERR_SHAPE
+    assert qdot(lib, M=1 << 41) == binding.PQ_ERR_SHAPE
+    assert qdot(lib, M=1 << 30, N=1 << 30, K=1 << 30) == binding.PQ_ERR_SHAPE
+    assert lib.pq_quantize_q8_0(P16, P16, P16, -1, 32, None) == binding.PQ_ERR_SHAPE
+    assert lib.pq_quantize_q8_0(P16, P16, P16, 1 << 40, 1 << 30, None) == binding.PQ_ERR_SHAPE
+
+
+def test_empty_problems_are_noops(lib):
+    # M == 0 or N == 0 is valid and launches nothing, even with null pointers
+    assert qdot(lib, A=None, AS=None, W=None, WS=None, C=None, M=0) == binding.PQ_OK
+    assert qdot(lib, A=None, AS=None, W=None, WS=None, C=None, N=0) == binding.PQ_OK
+    assert lib.pq_quantize_q8_0(None, None, None, 0, 32, None) == binding.PQ_OK
+    assert lib.pq_qdot_q8_0_blocksums(None, None, None, 0, 4, 64, 1, None) == binding.PQ_OK
+
+
+@pytest.mark.parametrize("which", ["A", "AS", "W", "WS", "C"])
+def test_null_pointers(lib, which):
+    assert qdot(lib, **{which: None}) == binding.PQ_ERR_INVALID_ARG
+
+
+def test_null_quantize_and_sums(lib):
+    assert lib.pq_quantize_q8_0(None, P16, P16, 1, 32, None) == binding.PQ_ERR_INVALID_ARG
+    assert lib.pq_quantize_q8_0(P16, None, P16, 1, 32, None) == binding.PQ_ERR_INVALID_ARG
+    assert lib.pq_quantize_q8_0(P16, P16, None, 1, 32, None) == binding.PQ_ERR_INVALID_ARG
+    assert lib.pq_qdot_q8_0_blocksums(P16, P16, None, 1, 1, 32, 1, None) == binding.PQ_ERR_INVALID_ARG
+
+
+def test_alignment(lib):
+    assert qdot(lib, A=P8) == binding.PQ_ERR_ALIGN
+    assert qdot(lib, W=P8) == binding.PQ_ERR_ALIGN
+    assert qdot(lib, AS=P2) == binding.PQ_ERR_ALIGN
+    assert qdot(lib, WS=P2) == binding.PQ_ERR_ALIGN
+    assert qdot(lib, C=P2) == binding.PQ_ERR_ALIGN
+    assert lib.pq_quantize_q8_0(P8, P16, P16, 1, 32, None) == binding.PQ_ERR_ALIGN
+    assert lib.pq_quantize_q8_0(P16, P8, P16, 1, 32, None) == binding.PQ_ERR_ALIGN
+    assert lib.pq_quantize_q8_0(P16, P16, P2, 1, 32, None) == binding.PQ_ERR_ALIGN
+    assert lib.pq_qdot_q8_0_blocksums(P16, P16, P2, 1, 1, 32, 1, None) == binding.PQ_ERR_ALIGN
+
+
+def test_unknown_codes(lib):
+    assert qdot(lib, path=7) == binding.PQ_ERR_INVALID_ARG
+    assert qdot(lib, layout=3) == binding.PQ_ERR_INVALID_ARG
+    assert lib.pq_qdot_q8_0_blocksums(P16, P16, P16, 1, 1, 32, 9, None) == binding.PQ_ERR_INVALID_ARG

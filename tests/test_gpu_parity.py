@@ -1,0 +1,219 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Bars: quantized bytes and f32 scales bit-identical; integer block sums
+identical; qdot_t outputs within |C - out| <= 1e-5 * sum_b |t_b| + 1e-6 of
+the oracle's double result (t_b the per-block terms), element by element.
+Inputs are seeded (gemm_q8_qdot_gb300.workloads); every expected value comes
+from the oracle, never from the GPU.
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_q8_qdot_gb300 import workloads
+from tests import golden_io
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().numpy()
+
+
+def assert_bytes_equal(q_gpu, s_gpu, q_ref, s_ref):
+    q_gpu, s_gpu = host(q_gpu), host(s_gpu)
+    bad = np.nonzero(q_gpu != q_ref)
+    assert bad[0].size == 0, f"{bad[0].size} quantized bytes differ, first at {[b[0] for b in bad]}"
+    sb = np.nonzero(s_gpu.view(np.uint32) != s_ref.view(np.uint32))
+    assert sb[0].size == 0, f"{sb[0].size} scales differ, first at {[b[0] for b in sb]}"
+
+
+def assert_within_bound(C, out, bound, what=""):
+    C = host(C).astype(np.float64) if isinstance(C, torch.Tensor) else C.astype(np.float64)
+    err = np.abs(C - out)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err / bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; worst at {i}: "
+                             f"gpu {C[i]!r} oracle {out[i]!r} bound {bound[i]!r}")
+
+
+def rand_operands(seed, M, N, K, lo=-128, hi=127):
+    rng = np.random.default_rng(seed)
+    a = workloads.random_int8(rng, (M, K), lo, hi)
+    w = workloads.random_int8(rng, (N, K), lo, hi)
+    a_s = workloads.random_scales(rng, (M, K // 32), 1e-3, 10.0)
+    w_s = workloads.random_scales(rng, (N, K // 32), 1e-4, 1.0)
+    return a, a_s, w, w_s
+
+
+@functools.lru_cache(maxsize=None)
+def quantized_workload(name):
+    """Oracle-quantized operands of a workload (the inputs both sides share)."""
+    wl = workloads.WORKLOADS[name]
+    x = workloads.activations(wl)
+    w = workloads.weights(wl)
+    qa, sa = oracle.quantize_q8_0(x)
+    qw, sw = oracle.quantize_q8_0(w)
+    return x, w, qa, sa, qw, sw
+
+
+# ------------------------------------------------------------------ quantizer
+
+def test_quantize_golden_blocks(pq):
+    for name, x, d, q in golden_io.quantize_blocks():
+        qg, sg = pq.quantize_q8_0(dev(x[None, :]))
+        torch.cuda.synchronize()
+        assert host(qg)[0].tolist() == q.tolist(), name
+        assert host(sg)[0, 0].view(np.uint32) == np.float32(d).view(np.uint32), name
+
+
+@pytest.mark.parametrize("rows,K", [(1, 32), (3, 96), (65, 256), (257, 4096), (5, 14336)])
+def test_quantize_random(pq, rows, K):
+    rng = np.random.default_rng(rows * 1000 + K)
+    x = rng.standard_normal((rows, K)).astype(np.float32)
+    x *= np.exp(rng.uniform(-30, 30, size=(rows, 1))).astype(np.float32)
+    x[0, :32] = 0.0                                               # zero block
+    if K >= 64:
+        x[-1, 32:64] = (rng.integers(-126, 126, 32) + 0.5).astype(np.float32)  # ties at d = 1
+        x[-1, 32] = 127.0
+    q_ref, s_ref = oracle.quantize_q8_0(x)
+    qg, sg = pq.quantize_q8_0(dev(x))
+    torch.cuda.synchronize()
+    assert_bytes_equal(qg, sg, q_ref, s_ref)
+
+
+@pytest.mark.parametrize("name", list(workloads.WORKLOADS))
+def test_quantize_workload_full(pq, name):
+    x, w, qa, sa, qw, sw = quantized_workload(name)
+    qg, sg = pq.quantize_q8_0(dev(x))
+    assert_bytes_equal(qg, sg, qa, sa)
+    qg, sg = pq.quantize_q8_0(dev(w))
+    assert_bytes_equal(qg, sg, qw, sw)
+
+
+def test_quantize_output_bounds(pq):
+    """Stores stay inside q [rows, K] and s [rows, K/32]: guard bytes around both."""
+    rows, K = 7, 96
+    x = np.random.default_rng(1).standard_normal((rows, K)).astype(np.float32)
+    qbuf = torch.full((rows * K + 64,), 0x5A, dtype=torch.int8, device=DEV)
+    sbuf = torch.full((rows * K // 32 + 16,), 7.25, dtype=torch.float32, device=DEV)
+    q = qbuf[16:16 + rows * K].view(rows, K)
+    s = sbuf[4:4 + rows * K // 32].view(rows, K // 32)
+    pq.quantize_q8_0(dev(x), q, s)
+    torch.cuda.synchronize()
+    qh, sh = host(qbuf), host(sbuf)
+    assert np.all(qh[:16] == 0x5A) and np.all(qh[16 + rows * K:] == 0x5A)
+    assert np.all(sh[:4] == 7.25) and np.all(sh[4 + rows * K // 32:] == 7.25)
+    q_ref, s_ref = oracle.quantize_q8_0(x)
+    assert_bytes_equal(q, s, q_ref, s_ref)
+
+
+# ------------------------------------------------------------------ qdot, small shapes
+
+SMALL_SHAPES = [(1, 1, 32), (1, 7, 64), (1, 64, 256), (1, 300, 1056), (2, 9, 96), (3, 17, 128),
+                (5, 33, 256), (8, 64, 512), (13, 70, 160), (1, 2, 14336)]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL_SHAPES)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_qdot_simt_small(pq, M, N, K, layout):
+    a, a_s, w, w_s = rand_operands(M * 7 + N * 13 + K, M, N, K)
+    out, bound = oracle.qdot(a, a_s, w, w_s)
+    ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+    C = pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(ws), ws_layout=layout, path=pq.PATH_SIMT)
+    torch.cuda.synchronize()
+    assert_within_bound(C, out, bound, f"simt M={M} N={N} K={K} layout={layout}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 5, 32), (2, 9, 96), (4, 33, 256), (5, 64, 1024), (1, 3, 14336)])
+def test_blocksums_simt_exact(pq, M, N, K):
+    a, _, w, _ = rand_operands(M + N + K, M, N, K)
+    a[:, :32] = -128
+    w[:, :32] = -128   # block 0: 32 * 16384 = 524288, the largest block sum
+    S_ref = oracle.blocksums(a, w)
+    S = pq.qdot_q8_0_blocksums(dev(a), dev(w), path=pq.PATH_SIMT)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(S).astype(np.int64), S_ref)
+
+
+def test_qdot_16byte_aligned_operands(pq):
+    """Bases 16 but not 32 bytes aligned take the two-128-bit-load variant."""
+    M, N, K = 3, 40, 256
+    a, a_s, w, w_s = rand_operands(99, M, N, K)
+    out, bound = oracle.qdot(a, a_s, w, w_s)
+    abuf = torch.zeros(M * K + 16, dtype=torch.int8, device=DEV)
+    wbuf = torch.zeros(N * K + 16, dtype=torch.int8, device=DEV)
+    A = abuf[16:].view(M, K)
+    W = wbuf[16:].view(N, K)
+    A.copy_(dev(a))
+    W.copy_(dev(w))
+    assert A.data_ptr() % 32 == 16 and W.data_ptr() % 32 == 16
+    C = pq.qdot_q8_0_ex(A, dev(a_s), W, dev(w_s), path=pq.PATH_SIMT)
+    torch.cuda.synchronize()
+    assert_within_bound(C, out, bound, "16-byte aligned")
+
+
+def test_qdot_output_guard_and_empty(pq):
+    M, N, K = 2, 37, 64
+    a, a_s, w, w_s = rand_operands(5, M, N, K)
+    out, bound = oracle.qdot(a, a_s, w, w_s)
+    cbuf = torch.full((M * N + 64,), -3.5, dtype=torch.float32, device=DEV)
+    C = cbuf[32:32 + M * N].view(M, N)
+    pq.qdot_q8_0(dev(a), dev(a_s), dev(w), dev(w_s), C)
+    torch.cuda.synchronize()
+    ch = host(cbuf)
+    assert np.all(ch[:32] == -3.5) and np.all(ch[32 + M * N:] == -3.5)
+    assert_within_bound(C, out, bound, "guarded")
+    # empty problems leave C untouched
+    pq.qdot_q8_0(dev(a[:0]), dev(a_s[:0]), dev(w), dev(w_s), C[:0])
+    torch.cuda.synchronize()
+
+
+def test_qdot_extreme_values(pq):
+    """All -128 against all -128 (largest block sums) and against +127, scale 0 blocks."""
+    M, N, K = 2, 24, 4096
+    a = np.full((M, K), -128, np.int8)
+    w = np.full((N, K), -128, np.int8)
+    w[1::2] = 127
+    a_s = np.ones((M, K // 32), np.float32)
+    w_s = np.full((N, K // 32), 0.5, np.float32)
+    w_s[:, 3] = 0.0
+    out, bound = oracle.qdot(a, a_s, w, w_s)
+    C = pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(w_s), path=pq.PATH_SIMT)
+    torch.cuda.synchronize()
+    assert_within_bound(C, out, bound, "extremes")
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def sampled_check(C, qa, sa, qw, sw, rows, cols, what):
+    out, bound = oracle.qdot(qa[rows], sa[rows], qw[cols], sw[cols])
+    assert_within_bound(host(C)[np.ix_(rows, cols)], out, bound, what)
+
+
+@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if workloads.WORKLOADS[n].M <= 8])
+def test_qdot_workload_full_simt(pq, name):
+    """The decode / small-batch workloads at full size, the launch the benchmark times."""
+    x, w, qa, sa, qw, sw = quantized_workload(name)
+    M, N = qa.shape[0], qw.shape[0]
+    A, AS = pq.quantize_q8_0(dev(x))
+    W, WS = pq.quantize_q8_0(dev(w))
+    C = pq.qdot_q8_0(A, AS, W, WS)
+    torch.cuda.synchronize()
+    if M * N * qa.shape[1] <= 2e8:
+        out, bound = oracle.qdot(qa, sa, qw, sw)
+        assert_within_bound(C, out, bound, name)
+    else:
+        rng = np.random.default_rng(0)
+        cols = np.sort(rng.choice(N, 1024, replace=False))
+        sampled_check(C, qa, sa, qw, sw, np.arange(M), cols, name)
