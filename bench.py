@@ -269,25 +269,51 @@ class Problem:
         return wl.weight_bytes + wl.M * wl.K + 4 * wl.M * (wl.K // 32) + 4 * wl.M * wl.N
 
 
+def _capture(prob: Problem, first: int, steps: int, stream, events=None, only_qdot=False):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for t in range(steps):
+            if only_qdot:
+                c = (first + t) % prob.copies
+                prob.pq.qdot_q8_0(prob.A, prob.AS, prob.W[c], prob.WS[c], prob.C)
+            else:
+                prob.step(first + t, events[t] if events else None)
+    return g
+
+
+def _replay_ms(g, stream) -> float:
+    import torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
 def time_graph(prob: Problem, steps: int, warmup: int, world: int, sampler=None):
+    """Times K steps captured in one graph; returns the step-region time and per-kernel durations.
+
+    The timed graph holds the K steps and nothing else.  Per-kernel durations
+    come from replaying the same K steps captured with an external timing event
+    around each kernel (the event nodes add their own latency, so these
+    durations are upper bounds); a graph of the K qdot launches alone gives a
+    second figure (its launch gaps included).
+    """
     import torch
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
-    # warm-up graph and timed graph (the timed one carries per-kernel event nodes)
     with torch.cuda.stream(stream):
         for t in range(2):
             prob.step(t)  # eager warm-up of the launch path
     stream.synchronize()
-    g_warm = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_warm, stream=stream):
-        for t in range(warmup):
-            prob.step(t)
+    g_warm = _capture(prob, 0, warmup, stream)
+    g = _capture(prob, warmup, steps, stream)
     evs = [[make_event() for _ in range(3)] for _ in range(steps)]
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for t in range(steps):
-            prob.step(warmup + t, evs[t])
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g_ev = _capture(prob, warmup, steps, stream, events=evs)
+    g_qdot = _capture(prob, warmup, steps, stream, only_qdot=True)
     g_warm.replay()
     torch.cuda.synchronize()
     barrier(world)
@@ -295,19 +321,16 @@ def time_graph(prob: Problem, steps: int, warmup: int, world: int, sampler=None)
     if sampler:
         sampler.start()
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        g.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
+    ms = _replay_ms(g, stream)
     t1 = time.perf_counter()
     barrier(world)
     if sampler:
         sampler.stop()
-    ms = start.elapsed_time(end)
+    _replay_ms(g_ev, stream)
     quant_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in evs)
     qdot_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in evs)
-    return ms, quant_ms, qdot_ms, (t0, t1)
+    qdot_only_ms = _replay_ms(g_qdot, stream) / steps
+    return ms, quant_ms, qdot_ms, qdot_only_ms, (t0, t1)
 
 
 def time_e2e(prob: Problem, steps: int, warmup: int):
@@ -348,7 +371,7 @@ def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str):
 def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sampler=None, e2e=False):
     wl = workloads.WORKLOADS[name]
     prob = Problem(pq, wl, device)
-    ms, quant_ms, qdot_ms, window = time_graph(prob, steps, warmup, world, sampler)
+    ms, quant_ms, qdot_ms, qdot_only_ms, window = time_graph(prob, steps, warmup, world, sampler)
     per_rank_s = ms * 1e-3
     if wl.M == 1 or wl.M <= 64:
         units, unit = wl.weight_bytes * steps, "GB/s"
@@ -358,7 +381,8 @@ def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sample
         scale = 1e12
     value, t_max = aggregate(units, per_rank_s, world, device)
     res = {"value": round(value / scale, 3), "unit": unit, "ms_per_step": round(t_max * 1e3 / steps, 5),
-           "kernel_ms": {"quantize": round(quant_ms, 5), "qdot": round(qdot_ms, 5)},
+           "kernel_ms": {"quantize": round(quant_ms, 5), "qdot": round(qdot_ms, 5),
+                         "qdot_graph_only": round(qdot_only_ms, 5)},
            "roofline": roofline_for(prob, qdot_ms, peaks, peak_src), "weight_copies": prob.copies,
            "window": window}
     if e2e:

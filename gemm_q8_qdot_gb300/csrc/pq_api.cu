@@ -8,6 +8,7 @@
 #include <cuda_runtime_api.h>
 
 #include "pq.h"
+#include "pq_debug.h"
 #include "pq_internal.h"
 
 namespace {
@@ -50,9 +51,16 @@ int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS
     if (!sums && (!aligned(AS, 4) || !aligned(WS, 4) || !aligned(C, 4))) return PQ_ERR_ALIGN;
 
     pq::QdotArgs a{A, AS, W, WS, C, S, M, N, K, ws_layout};
-    if (path == PQ_PATH_AUTO) path = (M <= 8) ? PQ_PATH_SIMT : PQ_PATH_TC;
-    cudaError_t e = (path == PQ_PATH_SIMT) ? pq::launch_qdot_simt(a, stream) : pq::launch_qdot_tc(a, stream);
-    return map_cuda(e);
+    if (path == PQ_PATH_SIMT) return map_cuda(pq::launch_qdot_simt(a, stream));
+    if (path == PQ_PATH_TC) return map_cuda(pq::launch_qdot_tc(a, stream));
+    // automatic: the dp4a streaming kernel while it keeps up with HBM (M <= 8),
+    // the tensor cores above; shapes the tensor-core kernel cannot take
+    // (K % 128 != 0) go to the dp4a kernel, which takes every shape
+    if (M > 8) {
+        cudaError_t e = pq::launch_qdot_tc(a, stream);
+        if (e != cudaErrorNotSupported) return map_cuda(e);
+    }
+    return map_cuda(pq::launch_qdot_simt(a, stream));
 }
 
 }  // namespace
@@ -109,5 +117,11 @@ const char* pq_strerror(int code) {
 }
 
 int pq_version(void) { return 100; }
+
+int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles) {
+    if (skip_stage < -1) return PQ_ERR_INVALID_ARG;
+    pq::set_tc_test_hooks(skip_stage, timeout_cycles);
+    return PQ_OK;
+}
 
 }  // extern "C"

@@ -9,11 +9,15 @@ struct u32x8 {
     uint32_t v[8];
 };
 
-// One Q8_0 block of bytes (32 B) in one 256-bit load, read-only path, not kept
-// in L1: the weight stream is touched once per launch.
+// Every global load here is volatile and coherent (no .nc): the kernels are
+// launched as programmatic dependents, so data written by the preceding kernel
+// is read only after griddepcontrol.wait, and no load may move above it.
+
+// One Q8_0 block of bytes (32 B) in one 256-bit load, not kept in L1: the
+// weight stream is touched once per launch.
 __device__ __forceinline__ u32x8 ld_stream_v8(const void* p) {
     u32x8 r;
-    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm volatile("ld.global.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]),
                    "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
                  : "l"(p));
@@ -23,7 +27,7 @@ __device__ __forceinline__ u32x8 ld_stream_v8(const void* p) {
 // Same block, kept in L1: activation rows are re-read by every warp of a CTA.
 __device__ __forceinline__ u32x8 ld_cached_v8(const void* p) {
     u32x8 r;
-    asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]),
                    "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
                  : "l"(p));
@@ -33,9 +37,20 @@ __device__ __forceinline__ u32x8 ld_cached_v8(const void* p) {
 // A 32-byte block from a base that is only 16-byte aligned: two 128-bit loads.
 __device__ __forceinline__ u32x8 ld_stream_2v4(const void* p) {
     u32x8 r;
-    asm("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]) : "l"(p));
-    asm("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
+                 : "l"(static_cast<const char*>(p) + 16));
+    return r;
+}
+
+// 16-byte-aligned variant of ld_cached_v8.
+__device__ __forceinline__ u32x8 ld_cached_2v4(const void* p) {
+    u32x8 r;
+    asm volatile("ld.global.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]) : "l"(p));
+    asm volatile("ld.global.v4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
                  : "l"(static_cast<const char*>(p) + 16));
     return r;
@@ -47,15 +62,31 @@ __device__ __forceinline__ u32x8 ld_block(const void* p) {
         if constexpr (kStream) return ld_stream_v8(p);
         else return ld_cached_v8(p);
     } else {
-        return ld_stream_2v4(p);
+        if constexpr (kStream) return ld_stream_2v4(p);
+        else return ld_cached_2v4(p);
     }
 }
 
-__device__ __forceinline__ float ld_f32_nc(const float* p) {
+__device__ __forceinline__ float ld_f32(const float* p) {
     float r;
-    asm("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(p));
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(r) : "l"(p));
     return r;
 }
+
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).  A
+// hint only: L2 is the point of coherence, so a later load after pdl_wait still
+// sees every write of the preceding kernel.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch.  pdl_trigger lets the next kernel on the
+// stream be scheduled now (it still waits for this grid's completion before
+// touching our outputs); pdl_wait blocks until the preceding grid has
+// completed and its writes are visible.  Both are no-ops for a launch without
+// the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Sum of the 32 signed-byte products of two Q8_0 blocks: eight dp4a.
 __device__ __forceinline__ int block_dot(const u32x8& a, const u32x8& w) {

@@ -17,6 +17,26 @@ struct QdotArgs {
     int ws_layout;   // 0: WS [N, K/32]; 1: WS [K/32, N]
 };
 
+// Launches `kernel` with programmatic stream serialization allowed: it may be
+// scheduled while the previous kernel on the stream is still running, and
+// orders itself with griddepcontrol.wait (pdl_wait) before touching data that
+// kernel may have written.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_quantize(const float* x, int8_t* q, float* s, int64_t rows, int64_t K,
                             cudaStream_t stream);
 
@@ -29,5 +49,10 @@ cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream);
 
 // Reads and clears the device status word (set by a bounded wait that gave up).
 cudaError_t read_and_clear_status(unsigned* status);
+
+// Test hooks of the tensor-core kernel: skip one producer stage so that the
+// consumers' bounded waits give up (-1: off), and the wait limit in SM clock
+// cycles (0: the default of about two seconds).
+void set_tc_test_hooks(int inject_skip_stage, unsigned long long timeout_cycles);
 
 }  // namespace pq

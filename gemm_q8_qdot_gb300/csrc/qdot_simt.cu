@@ -21,6 +21,11 @@
 //     U * COLS * 32 bytes of weights in flight;
 //   * the lanes' partial sums meet in an xor butterfly (sum<over ctx.lane>)
 //     and lane 0 stores.
+// The kernel is launched as a programmatic dependent: before
+// griddepcontrol.wait it only asks L2 to prefetch its weight rows (a hint that
+// cannot return stale data), so the weight stream from HBM overlaps the tail
+// of the kernel that produced the activations (normally the quantizer); every
+// load proper comes after the wait.
 // Ragged M and N are masked (no slice has to be in bounds, unlike the pages'
 // @aligned(N = TN) example).
 //
@@ -42,7 +47,17 @@ qdot_simt_kernel(QdotArgs p) {
     const int64_t N = p.N, M = p.M, K = p.K, KB = K >> 5;
     const int64_t j0 = (static_cast<int64_t>(blockIdx.x) * kWarps + warp) * COLS;
     const int64_t i0 = static_cast<int64_t>(blockIdx.y) * MR;
+    pdl_trigger();
     if (j0 >= N) return;  // warp-uniform; no CTA-wide synchronisation below
+    if (lane < COLS && j0 + lane < N) {
+        // one bulk L2 prefetch per weight row (K bytes) and scale row; rows of a
+        // 16-byte aligned base stay 16-byte aligned since K % 32 == 0
+        prefetch_l2(p.W + (j0 + lane) * K, static_cast<uint32_t>(K < (int64_t(1) << 30) ? K : (int64_t(1) << 30)));
+        if (WSL == 0 && !SUMS && (KB * 4) % 16 == 0 &&
+            (reinterpret_cast<uintptr_t>(p.WS + (j0 + lane) * KB) & 15) == 0)
+            prefetch_l2(p.WS + (j0 + lane) * KB, static_cast<uint32_t>(KB * 4));
+    }
+    pdl_wait();
 
     bool jv[COLS];
     const int8_t* wrow[COLS];
@@ -80,7 +95,7 @@ qdot_simt_kernel(QdotArgs p) {
                 if (bv && jv[c]) {
                     wv[u][c] = ld_block<V8, true>(wrow[c] + b * 32);
                     if constexpr (!SUMS)
-                        wsv[u][c] = ld_f32_nc(WSL == 0 ? p.WS + (j0 + c) * KB + b : p.WS + b * N + (j0 + c));
+                        wsv[u][c] = ld_f32(WSL == 0 ? p.WS + (j0 + c) * KB + b : p.WS + b * N + (j0 + c));
                 } else {
 #pragma unroll
                     for (int t = 0; t < 8; ++t) wv[u][c].v[t] = 0u;
@@ -97,7 +112,7 @@ qdot_simt_kernel(QdotArgs p) {
             for (int r = 0; r < MR; ++r) {
                 if (bv && iv[r]) {
                     av[u][r] = ld_block<V8, false>(arow[r] + b * 32);
-                    if constexpr (!SUMS) asv[u][r] = ld_f32_nc(p.AS + (i0 + r) * KB + b);
+                    if constexpr (!SUMS) asv[u][r] = ld_f32(p.AS + (i0 + r) * KB + b);
                 } else {
 #pragma unroll
                     for (int t = 0; t < 8; ++t) av[u][r].v[t] = 0u;
@@ -138,11 +153,8 @@ cudaError_t launch_tile(const QdotArgs& a, bool v8, cudaStream_t stream) {
     const int64_t gy = (a.M + MR - 1) / MR;
     if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
-    if (v8)
-        qdot_simt_kernel<MR, COLS, U, true, SUMS, WSL><<<grid, kWarps * 32, 0, stream>>>(a);
-    else
-        qdot_simt_kernel<MR, COLS, U, false, SUMS, WSL><<<grid, kWarps * 32, 0, stream>>>(a);
-    return cudaGetLastError();
+    if (v8) return launch_pdl(qdot_simt_kernel<MR, COLS, U, true, SUMS, WSL>, grid, dim3(kWarps * 32), 0, stream, a);
+    return launch_pdl(qdot_simt_kernel<MR, COLS, U, false, SUMS, WSL>, grid, dim3(kWarps * 32), 0, stream, a);
 }
 
 template <bool SUMS, int WSL>

@@ -34,16 +34,22 @@ __device__ __forceinline__ uint32_t pack4(float a, float b, float c, float e, fl
     return q_byte(a, d) | (q_byte(b, d) << 8) | (q_byte(c, d) << 16) | (q_byte(e, d) << 24);
 }
 
+// x may be written by the preceding kernel: coherent load, kept after pdl_wait.
 __device__ __forceinline__ float4 ld_stream_f4(const float* p) {
     float4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-        : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(p));
+    asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(p) : "memory");
     return r;
 }
 
 __global__ void __launch_bounds__(kThreads)
 quantize_q8_0_kernel(const float* __restrict__ x, int8_t* __restrict__ q, float* __restrict__ s,
                      int64_t nblocks) {
+    // Let the next kernel (typically qdot_t) be scheduled now, so that it can
+    // stream its weights while this one runs; then wait for whatever wrote x
+    // (and read q, s) before us.
+    pdl_trigger();
+    pdl_wait();
     const int64_t g = static_cast<int64_t>(blockIdx.x) * kBlocksPerCta + (threadIdx.x >> 2);
     const int sub = threadIdx.x & 3;
     const bool live = g < nblocks;
@@ -75,8 +81,8 @@ cudaError_t launch_quantize(const float* x, int8_t* q, float* s, int64_t rows, i
     const int64_t nblocks = rows * (K / 32);
     const int64_t grid = (nblocks + kBlocksPerCta - 1) / kBlocksPerCta;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    quantize_q8_0_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(x, q, s, nblocks);
-    return cudaGetLastError();
+    return launch_pdl(quantize_q8_0_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, stream,
+                      x, q, s, nblocks);
 }
 
 }  // namespace pq

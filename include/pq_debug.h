@@ -1,0 +1,30 @@
+/*
+ * pq_debug.h — test-only hooks of libpq.  Not part of the computation; used by
+ * the failure-detection tests.  The Phobos pages have no counterpart: their
+ * kernels trap on a bad extent ("Kernel ABI", "Entry checks") and a trapping
+ * CTA of a persistent kernel leaves the others waiting for good, which a
+ * shared GPU must never see.  libpq instead bounds every on-device wait.
+ */
+#ifndef PQ_DEBUG_H
+#define PQ_DEBUG_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Makes the next tensor-core qdot launches (PQ_PATH_TC) skip pipeline stage
+ * `skip_stage` in the producer (-1 turns it off), so that every consumer's
+ * bounded wait gives up after `timeout_cycles` SM clock cycles (0 restores the
+ * default limit of about two seconds).  The kernel then drains its copies and
+ * MMAs in flight, frees its tensor memory and returns without writing C; the
+ * next pq_check_device returns PQ_ERR_TIMEOUT.  Host state, process-wide, not
+ * thread-safe; returns PQ_ERR_INVALID_ARG for skip_stage < -1.
+ */
+int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PQ_DEBUG_H */

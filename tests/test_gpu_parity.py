@@ -217,3 +217,62 @@ def test_qdot_workload_full_simt(pq, name):
         rng = np.random.default_rng(0)
         cols = np.sort(rng.choice(N, 1024, replace=False))
         sampled_check(C, qa, sa, qw, sw, np.arange(M), cols, name)
+
+
+# ------------------------------------------------------------------ tensor-core path
+
+TC_SHAPES = [(1, 16, 128), (9, 100, 256), (16, 128, 128), (17, 300, 384), (33, 130, 128), (64, 257, 512),
+             (65, 64, 256), (130, 200, 128), (256, 384, 1024), (300, 129, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", TC_SHAPES)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_qdot_tc_small(pq, M, N, K, layout):
+    a, a_s, w, w_s = rand_operands(M * 31 + N * 7 + K + layout, M, N, K)
+    out, bound = oracle.qdot(a, a_s, w, w_s)
+    ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+    C = pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(ws), ws_layout=layout, path=pq.PATH_TC)
+    pq.check_device()
+    assert_within_bound(C, out, bound, f"tc M={M} N={N} K={K} layout={layout}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (20, 70, 256), (64, 128, 128), (100, 140, 256), (128, 256, 512)])
+def test_blocksums_tc_exact(pq, M, N, K):
+    a, _, w, _ = rand_operands(M + 3 * N + K, M, N, K)
+    a[:, :32] = -128
+    w[:, :32] = -128
+    a[:, 32:64] = 127
+    S_ref = oracle.blocksums(a, w)
+    S = pq.qdot_q8_0_blocksums(dev(a), dev(w), path=pq.PATH_TC)
+    pq.check_device()
+    assert np.array_equal(host(S).astype(np.int64), S_ref)
+
+
+def test_qdot_tc_unsupported_k(pq):
+    """The tensor-core path needs K % 128 == 0; the explicit path says so, auto falls back."""
+    M, N, K = 20, 40, 96
+    a, a_s, w, w_s = rand_operands(4, M, N, K)
+    with pytest.raises(pq.PQError) as ei:
+        pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(w_s), path=pq.PATH_TC)
+    assert ei.value.code == pq.PQ_ERR_UNSUPPORTED
+    out, bound = oracle.qdot(a, a_s, w, w_s)
+    C = pq.qdot_q8_0(dev(a), dev(a_s), dev(w), dev(w_s))
+    pq.check_device()
+    assert_within_bound(C, out, bound, "auto fallback")
+
+
+@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if workloads.WORKLOADS[n].M > 8])
+def test_qdot_workload_full_tc(pq, name):
+    """Small-batch (M = 16, 64) and prompt (M = 512) workloads at full size, as benchmarked."""
+    x, w, qa, sa, qw, sw = quantized_workload(name)
+    M, N = qa.shape[0], qw.shape[0]
+    A, AS = pq.quantize_q8_0(dev(x))
+    W, WS = pq.quantize_q8_0(dev(w))
+    C = pq.qdot_q8_0(A, AS, W, WS)
+    pq.check_device()
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(M, min(M, 24), replace=False))
+    cols = np.sort(np.concatenate([rng.choice(N, 384, replace=False), [0, N - 1]]))
+    sampled_check(C, qa, sa, qw, sw, rows, np.unique(cols), name)
+    # a property at full size: every row of C is finite
+    assert torch.isfinite(C).all()

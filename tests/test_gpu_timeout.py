@@ -1,0 +1,52 @@
+"""Failure detection on the GPU without a fault: a bounded wait is made to run out.
+
+The tensor-core kernel's producer is told (test hook, include/pq_debug.h) to
+skip one pipeline stage, so the consumers' waits on that stage never complete.
+Every wait is bounded: the kernel must give up within its limit, record the
+timeout in the library's status word, drain its work in flight, free its
+tensor memory and return.  The test checks the reported status and that the
+context stays usable (a normal launch afterwards gives correct results).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_q8_qdot_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _hook(lib, stage, cycles):
+    lib.pq_debug_set_tc_fault.argtypes = [ctypes.c_int, ctypes.c_ulonglong]
+    lib.pq_debug_set_tc_fault.restype = ctypes.c_int
+    assert lib.pq_debug_set_tc_fault(stage, cycles) == 0
+
+
+@pytest.mark.parametrize("M", [16, 256])
+def test_tc_bounded_wait_gives_up_and_recovers(pq, M):
+    lib = pq.load()
+    rng = np.random.default_rng(M)
+    N, K = 256, 512
+    a = workloads.random_int8(rng, (M, K))
+    w = workloads.random_int8(rng, (N, K))
+    a_s = workloads.random_scales(rng, (M, K // 32))
+    w_s = workloads.random_scales(rng, (N, K // 32))
+    A, AS, W, WS = (torch.from_numpy(v).cuda() for v in (a, a_s, w, w_s))
+    pq.check_device()  # clean status before
+    try:
+        _hook(lib, 1, 20_000_000)  # ~10 ms at 2 GHz
+        C = torch.full((M, N), 123.0, device="cuda")
+        pq.qdot_q8_0_ex(A, AS, W, WS, C, path=pq.PATH_TC)
+        with pytest.raises(pq.PQError) as ei:
+            pq.check_device()
+        assert ei.value.code == pq.PQ_ERR_TIMEOUT
+    finally:
+        _hook(lib, -1, 0)
+    # the context is still usable and the next launch is correct
+    C = pq.qdot_q8_0_ex(A, AS, W, WS, path=pq.PATH_TC)
+    pq.check_device()
+    out, bound = oracle.qdot(a, a_s, w, w_s)
+    assert np.all(np.abs(C.cpu().numpy().astype(np.float64) - out) <= bound)
