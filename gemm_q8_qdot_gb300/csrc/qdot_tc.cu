@@ -58,14 +58,14 @@ __device__ unsigned g_pq_status;
 
 namespace {
 
-constexpr int BM = 128;      // X rows per tile (MMA M, TMEM lanes)
+constexpr int BM = 128;      // rows of the MMA's A operand per tile (MMA M, TMEM lanes)
 constexpr int KS = 64;       // K elements per pipeline stage (two Q8_0 blocks)
 constexpr int GROUP = 4;     // Q8_0 blocks per scale group (128 K, two stages)
 
 struct TcParams {
-    const float* xs;          // scale of X row p, block b: xs[p * xs_r + b * xs_b]
+    const float* xs;          // scale of MMA-A row p, block b: xs[p * xs_r + b * xs_b]
     int64_t xs_r, xs_b;
-    const float* ys;          // scale of Y row q, block b: ys[q * ys_r + b * ys_b]
+    const float* ys;          // scale of MMA-B row q, block b: ys[q * ys_r + b * ys_b]
     int64_t ys_r, ys_b;
     float* C;                 // C[p * ldp + q * ldq]
     int64_t ldp, ldq;
@@ -73,13 +73,19 @@ struct TcParams {
     int64_t sp, sq;
     int64_t P, Q, K;
     int groups_per_split;
+    int splits;               // K splits per tile
+    int tiles_q;              // tiles along Q
+    int units;                // tiles_p * tiles_q * splits work units, taken round-robin by the CTAs
     int atomic;               // split-K: red.add into a zeroed C
     int vec_store;            // ldq == 1, Q % 4 == 0, C 16-byte aligned: float4 stores
     int inject_skip_stage;    // test hook: the producer skips this stage (-1: off)
     unsigned long long timeout_cycles;
 };
 
-template <int BN, int NCONV, int NEPI, int S8, int S16>
+// SWAP = false: MMA-A = activations (f16, by TMA), MMA-B = weights (int8 by
+// TMA, converted).  SWAP = true: MMA-A = weights (converted), MMA-B =
+// activations.  The weight tile is always the converted one.
+template <int BN, int NCONV, int NEPI, int S8, int S16, bool SWAP>
 struct Cfg {
     static constexpr int kThreads = 32 * (2 + NCONV + NEPI);
     static constexpr int kE0 = 2 + NCONV;                 // first epilogue warp
@@ -87,24 +93,27 @@ struct Cfg {
     static constexpr int kTmemCols = (kNbuf * BN <= 32) ? 32 : (kNbuf * BN <= 64) ? 64 : (kNbuf * BN <= 128) ? 128
                                      : (kNbuf * BN <= 256) ? 256 : 512;
     static constexpr int kCW = BN / (NEPI / 4);          // columns per epilogue warp
-    static constexpr int kCH = kCW < 32 ? kCW : 32;       // columns per tcgen05.ld
-    static constexpr int kX8 = BM * KS;                   // int8 X tile bytes
-    static constexpr int kY8 = BN * KS;
-    static constexpr int kX16 = BM * KS * 2;              // f16 X tile bytes
-    static constexpr int kY16 = BN * KS * 2;
-    static constexpr int kOffX8 = 0;
-    static constexpr int kOffY8 = kOffX8 + S8 * kX8;
-    static constexpr int kOffX16 = kOffY8 + S8 * kY8;
-    static constexpr int kOffY16 = kOffX16 + S16 * kX16;
-    static constexpr int kOffYs = kOffY16 + S16 * kY16;   // 2 x [GROUP][BN] f32
+    static constexpr int kCH = kCW < 16 ? kCW : 16;       // columns per tcgen05.ld
+    static constexpr int kCR = SWAP ? BM : BN;            // converted (weight) rows per stage
+    static constexpr int kFR = SWAP ? BN : BM;            // f16 (activation) rows per stage
+    static constexpr int kW8 = kCR * KS;                  // int8 weight tile bytes
+    static constexpr int kA16 = BM * KS * 2;              // f16 MMA-A tile bytes
+    static constexpr int kB16 = BN * KS * 2;              // f16 MMA-B tile bytes
+    static constexpr int kF16 = kFR * KS * 2;             // bytes the TMA brings per f16 stage
+    static constexpr int kOffW8 = 0;
+    static constexpr int kOffA16 = kOffW8 + S8 * kW8;
+    static constexpr int kOffB16 = kOffA16 + S16 * kA16;
+    static constexpr int kOffYs = kOffB16 + S16 * kB16;   // 2 x [GROUP][BN] f32
     static constexpr int kOffBar = kOffYs + 2 * GROUP * BN * 4;
     static constexpr int kNumBars = 2 * S8 + 2 * S16 + 2 * kNbuf + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;    // + alignment slack
+    static constexpr int kOctPerWarp = kCR / 8 / NCONV;   // row octets each converter warp takes
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
     static_assert(NEPI == 4 || NEPI == 8, "epilogue warps cover the four TMEM lane quadrants");
     static_assert(kCW % kCH == 0 && kCH % 8 == 0, "epilogue column chunks");
-    static_assert(kX8 % 1024 == 0 && kY8 % 1024 == 0 && kX16 % 1024 == 0 && kY16 % 1024 == 0, "1024-B tiles");
+    static_assert(kCR % (8 * NCONV) == 0, "converter work splits evenly");
+    static_assert(kW8 % 1024 == 0 && kA16 % 1024 == 0 && kB16 % 1024 == 0, "1024-B aligned tiles");
 };
 
 __device__ __forceinline__ void set_abort(volatile int* abort_flag) {
@@ -121,12 +130,14 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, vol
     if (*abort_flag) return false;
     if (tc::mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (true) {
+    for (uint32_t n = 1;; ++n) {
         if (tc::mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (static_cast<unsigned long long>(clock64() - t0) > limit) {
-            set_abort(abort_flag);
-            return false;
+        if ((n & 31) == 0) {
+            if (*abort_flag) return false;
+            if (static_cast<unsigned long long>(clock64() - t0) > limit) {
+                set_abort(abort_flag);
+                return false;
+            }
         }
     }
 }
@@ -155,11 +166,33 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
-template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS>
-__global__ void __launch_bounds__(Cfg<BN, NCONV, NEPI, S8, S16>::kThreads, MINB)
-qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+// Activation pre-pass: int8 [rows, K] -> f16 [rows, K] (exact), 16 bytes per
+// thread.  The tensor-core kernel then loads activation tiles with TMA straight
+// into the MMA operand layout, so that only the weights are converted in it.
+__global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict__ src, __half* __restrict__ dst,
+                                                        int64_t n16) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+    if (i >= n16) return;
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(src + i * 16) : "memory");
+    uint4 o0, o1;
+    i8x4_to_f16x4(v.x, o0.x, o0.y);
+    i8x4_to_f16x4(v.y, o0.z, o0.w);
+    i8x4_to_f16x4(v.z, o1.x, o1.y);
+    i8x4_to_f16x4(v.w, o1.z, o1.w);
+    uint4* d = reinterpret_cast<uint4*>(dst + i * 16);
+    d[0] = o0;
+    d[1] = o1;
+}
+
+template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SWAP, bool SUMS>
+__global__ void __launch_bounds__(Cfg<BN, NCONV, NEPI, S8, S16, SWAP>::kThreads, MINB)
+qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                const TcParams prm) {
-    using CF = Cfg<BN, NCONV, NEPI, S8, S16>;
+    using CF = Cfg<BN, NCONV, NEPI, S8, S16, SWAP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::kOffBar);
@@ -178,13 +211,22 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     const int lane = threadIdx.x & 31;
     const unsigned long long limit = prm.timeout_cycles;
 
-    const int64_t p0 = static_cast<int64_t>(blockIdx.x) * BM;
-    const int64_t q0 = static_cast<int64_t>(blockIdx.y) * BN;
     const int ngroups = static_cast<int>(prm.K / (KS * 2));
-    const int g_begin = static_cast<int>(blockIdx.z) * prm.groups_per_split;
-    const int g_end = min(ngroups, g_begin + prm.groups_per_split);
-    const int nst = 2 * max(0, g_end - g_begin);  // stages of this CTA
-    const int st0 = 2 * g_begin;
+    // work unit u -> (tile along P, tile along Q, K split); stages of the unit
+    struct Unit {
+        int64_t p0, q0;
+        int g_begin, nst;
+    };
+    auto unit = [&](int u) {
+        Unit r;
+        const int z = u % prm.splits;
+        const int t = u / prm.splits;
+        r.q0 = static_cast<int64_t>(t % prm.tiles_q) * BN;
+        r.p0 = static_cast<int64_t>(t / prm.tiles_q) * BM;
+        r.g_begin = z * prm.groups_per_split;
+        r.nst = 2 * max(0, min(ngroups, r.g_begin + prm.groups_per_split) - r.g_begin);
+        return r;
+    };
 
     pdl_trigger();
     if (threadIdx.x == 0) {
@@ -193,7 +235,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             tc::mbar_init(&empty8[i], NCONV);
         }
         for (int i = 0; i < S16; ++i) {
-            tc::mbar_init(&full16[i], NCONV);
+            tc::mbar_init(&full16[i], NCONV + 1);  // the converters + the producer's TMA
             tc::mbar_init(&empty16[i], 1);
         }
         for (int i = 0; i < CF::kNbuf; ++i) {
@@ -203,8 +245,8 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         tc::mbar_init(drain, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
-        tc::tma_prefetch_map(&tmX);
-        tc::tma_prefetch_map(&tmY);
+        tc::tma_prefetch_map(&tmW);
+        tc::tma_prefetch_map(&tmA);
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, CF::kTmemCols);
@@ -220,47 +262,70 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
-            for (int i = 0; i < nst; ++i) {
-                const int s = i % S8;
-                if (!bounded_wait(&empty8[s], ((i / S8) & 1) ^ 1, abort_flag, limit)) continue;
-                issued = i + 1;
-                if (i == prm.inject_skip_stage) continue;  // test hook: never arrives
-                tc::mbar_arrive_expect_tx(&full8[s], CF::kX8 + CF::kY8);
-                const int kx = (st0 + i) * KS;
-                tc::tma_load_2d(smem + CF::kOffX8 + s * CF::kX8, &tmX, &full8[s], kx, static_cast<int>(p0));
-                tc::tma_load_2d(smem + CF::kOffY8 + s * CF::kY8, &tmY, &full8[s], kx, static_cast<int>(q0));
+            int issued8 = 0, issued16 = 0;
+            int gi = 0;  // stage counter over all units of this CTA
+            for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
+                const Unit un = unit(u);
+                const int w_row = static_cast<int>(SWAP ? un.p0 : un.q0);
+                const int a_row = static_cast<int>(SWAP ? un.q0 : un.p0);
+                for (int i = 0; i < un.nst; ++i, ++gi) {
+                    const int s16 = gi % S16, s8 = gi % S8;
+                    const int kx = (2 * un.g_begin + i) * KS;
+                    if (bounded_wait(&empty16[s16], ((gi / S16) & 1) ^ 1, abort_flag, limit)) {
+                        issued16 = gi + 1;
+                        tc::mbar_arrive_expect_tx(&full16[s16], CF::kF16);
+                        uint8_t* dst =
+                            SWAP ? smem + CF::kOffB16 + s16 * CF::kB16 : smem + CF::kOffA16 + s16 * CF::kA16;
+                        tc::tma_load_2d(dst, &tmA, &full16[s16], kx, a_row);
+                    }
+                    if (bounded_wait(&empty8[s8], ((gi / S8) & 1) ^ 1, abort_flag, limit)) {
+                        issued8 = gi + 1;
+                        if (gi == prm.inject_skip_stage) continue;  // test hook: never arrives
+                        tc::mbar_arrive_expect_tx(&full8[s8], CF::kW8);
+                        tc::tma_load_2d(smem + CF::kOffW8 + s8 * CF::kW8, &tmW, &full8[s8], kx, w_row);
+                    }
+                }
             }
             // copies in flight land before the CTA may exit
-            for (int i = max(0, issued - S8); i < issued; ++i)
+            for (int i = max(0, issued8 - S8); i < issued8; ++i)
                 if (i != prm.inject_skip_stage) drain_wait(&full8[i % S8], (i / S8) & 1, limit);
+            // an f16 stage completes with its TMA bytes and the converters' arrivals,
+            // which the converters make for every stage, also after an abort
+            for (int i = max(0, issued16 - S16); i < issued16; ++i)
+                drain_wait(&full16[i % S16], (i / S16) & 1, limit);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_f16_f32(BM, BN);
-            int g = 0;
-            for (int i = 0; i < nst; ++i) {
-                const int s = i % S16;
-                const bool ok = bounded_wait(&full16[s], (i / S16) & 1, abort_flag, limit);
-                if (ok) tc::tc_fence_after_sync();
-                const uint32_t xa = tc::smem_u32(smem + CF::kOffX16 + s * CF::kX16);
-                const uint32_t ya = tc::smem_u32(smem + CF::kOffY16 + s * CF::kY16);
+            int g = 0, gi = 0;
+            for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
+                const int nst = unit(u).nst;
+                for (int i = 0; i < nst; ++i, ++gi) {
+                    const int s = gi % S16;
+                    const bool ok = bounded_wait(&full16[s], (gi / S16) & 1, abort_flag, limit);
+                    if (ok) tc::tc_fence_after_sync();
+                    const uint32_t xa = tc::smem_u32(smem + CF::kOffA16 + s * CF::kA16);
+                    const uint32_t ya = tc::smem_u32(smem + CF::kOffB16 + s * CF::kB16);
 #pragma unroll
-                for (int bb = 0; bb < 2; ++bb, ++g) {
-                    const int buf = g % CF::kNbuf;
-                    if (!ok || !bounded_wait(&tempty[buf], ((g / CF::kNbuf) & 1) ^ 1, abort_flag, limit)) continue;
-                    tc::tc_fence_after_sync();
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+                    for (int bb = 0; bb < 2; ++bb, ++g) {
+                        const int buf = g % CF::kNbuf;
+                        if (!ok || !bounded_wait(&tempty[buf], ((g / CF::kNbuf) & 1) ^ 1, abort_flag, limit))
+                            continue;
+                        tc::tc_fence_after_sync();
+                        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t koff = static_cast<uint32_t>((bb * 2 + kk) * 32);  // 16 f16 = 32 B
-                        tc::umma_f16(d, tc::sw128_kmajor_desc(xa + koff), tc::sw128_kmajor_desc(ya + koff), idesc,
-                                     kk);
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint32_t koff = static_cast<uint32_t>((bb * 2 + kk) * 32);  // 16 f16 = 32 B
+                            tc::umma_f16(d, tc::sw128_kmajor_desc(xa + koff), tc::sw128_kmajor_desc(ya + koff),
+                                         idesc, kk);
+                        }
+                        tc::umma_commit(&tfull[buf]);
                     }
-                    tc::umma_commit(&tfull[buf]);
+                    // release the f16 stage once its MMAs completed (also after an abort,
+                    // so that the producer's drain sees every issued stage released)
+                    tc::umma_commit(&empty16[s]);
                 }
-                if (ok) tc::umma_commit(&empty16[s]);
             }
             tc::umma_commit(drain);  // arrives when every MMA issued above has completed
             drain_wait(drain, 0, limit);
@@ -270,64 +335,71 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int cw = warp - 2;
         const int r_in = lane & 7;  // row within an octet
         const int c8 = lane >> 3;   // 16-byte chunk of a 64-byte int8 row
-        constexpr int kOctets = (BM + BN) / 8;
-        for (int i = 0; i < nst; ++i) {
-            const int s8 = i % S8, s16 = i % S16;
-            int ok = 0;
-            if (lane == 0)
-                ok = bounded_wait(&full8[s8], (i / S8) & 1, abort_flag, limit) &&
-                     bounded_wait(&empty16[s16], ((i / S16) & 1) ^ 1, abort_flag, limit);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (ok) {
-                const uint8_t* x8 = smem + CF::kOffX8 + s8 * CF::kX8;
-                const uint8_t* y8 = smem + CF::kOffY8 + s8 * CF::kY8;
-                uint8_t* x16 = smem + CF::kOffX16 + s16 * CF::kX16;
-                uint8_t* y16 = smem + CF::kOffY16 + s16 * CF::kY16;
-                for (int o = cw; o < kOctets; o += NCONV) {
-                    const bool isx = o < BM / 8;
-                    const int row = (isx ? o : o - BM / 8) * 8 + r_in;
-                    const uint8_t* src = (isx ? x8 : y8) + row * KS + ((c8 ^ ((row >> 1) & 3)) << 4);
-                    uint8_t* dst = (isx ? x16 : y16) + row * (KS * 2);
-                    const uint4 v = *reinterpret_cast<const uint4*>(src);
-                    uint4 o0, o1;
-                    i8x4_to_f16x4(v.x, o0.x, o0.y);
-                    i8x4_to_f16x4(v.y, o0.z, o0.w);
-                    i8x4_to_f16x4(v.z, o1.x, o1.y);
-                    i8x4_to_f16x4(v.w, o1.z, o1.w);
-                    const int j0 = 2 * c8, j1 = 2 * c8 + 1;
-                    *reinterpret_cast<uint4*>(dst + ((j0 ^ (row & 7)) << 4)) = o0;
-                    *reinterpret_cast<uint4*>(dst + ((j1 ^ (row & 7)) << 4)) = o1;
+        int gi = 0;
+        for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
+            const int nst = unit(u).nst;
+            for (int i = 0; i < nst; ++i, ++gi) {
+                const int s8 = gi % S8, s16 = gi % S16;
+                int ok = 0;
+                if (lane == 0)
+                    ok = bounded_wait(&full8[s8], (gi / S8) & 1, abort_flag, limit) &&
+                         bounded_wait(&empty16[s16], ((gi / S16) & 1) ^ 1, abort_flag, limit);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (ok) {
+                    const uint8_t* w8 = smem + CF::kOffW8 + s8 * CF::kW8;
+                    uint8_t* w16 = SWAP ? smem + CF::kOffA16 + s16 * CF::kA16 : smem + CF::kOffB16 + s16 * CF::kB16;
+                    uint4 v[CF::kOctPerWarp];
+#pragma unroll
+                    for (int t = 0; t < CF::kOctPerWarp; ++t) {  // all loads first
+                        const int row = (cw + t * NCONV) * 8 + r_in;
+                        v[t] = *reinterpret_cast<const uint4*>(w8 + row * KS + ((c8 ^ ((row >> 1) & 3)) << 4));
+                    }
+#pragma unroll
+                    for (int t = 0; t < CF::kOctPerWarp; ++t) {
+                        const int row = (cw + t * NCONV) * 8 + r_in;
+                        uint4 o0, o1;
+                        i8x4_to_f16x4(v[t].x, o0.x, o0.y);
+                        i8x4_to_f16x4(v[t].y, o0.z, o0.w);
+                        i8x4_to_f16x4(v[t].z, o1.x, o1.y);
+                        i8x4_to_f16x4(v[t].w, o1.z, o1.w);
+                        uint8_t* dst = w16 + row * (KS * 2);
+                        *reinterpret_cast<uint4*>(dst + (((2 * c8) ^ (row & 7)) << 4)) = o0;
+                        *reinterpret_cast<uint4*>(dst + (((2 * c8 + 1) ^ (row & 7)) << 4)) = o1;
+                    }
+                    tc::fence_proxy_async_smem();
                 }
-                tc::fence_proxy_async_smem();
-            }
-            __syncwarp();
-            if (ok && lane == 0) {
-                tc::mbar_arrive(&empty8[s8]);
-                tc::mbar_arrive(&full16[s16]);
+                __syncwarp();
+                if (lane == 0) {
+                    // arrive even after an abort, so that full16 completes for stages
+                    // whose f16 bytes the producer already issued
+                    tc::mbar_arrive(&empty8[s8]);
+                    tc::mbar_arrive(&full16[s16]);
+                }
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        constexpr int NCH = CF::kCW / CF::kCH;
         const int e = warp - CF::kE0;
         const int quad = warp & 3;
         const int cb = (e >> 2) * CF::kCW;
         const int et = e * 32 + lane;  // 0 .. 32 * NEPI - 1
-        const int64_t p = p0 + quad * 32 + lane;
-        const bool pv = p < prm.P;
+        const int prow = quad * 32 + lane;
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-        const int ngs = nst / 2;  // scale groups of this CTA
 
         float acc[CF::kCW];
 #pragma unroll
         for (int t = 0; t < CF::kCW; ++t) acc[t] = 0.0f;
 
-        // scale prefetch: own row's 4 X scales, and one Y column's 4 scales per thread
-        auto load_scales = [&](int G, float (&xr)[GROUP], float (&yr)[GROUP]) {
-            const int64_t b0 = static_cast<int64_t>(g_begin + G) * GROUP;
+        // scales of scale group G of unit un: this thread's MMA-A row (4 blocks) and,
+        // for et < BN, MMA-B row q0 + et (4 blocks)
+        auto load_scales = [&](const Unit& un, int G, float (&xr)[GROUP], float (&yr)[GROUP]) {
+            const int64_t b0 = static_cast<int64_t>(un.g_begin + G) * GROUP;
+            const int64_t p = un.p0 + prow;
+            const int64_t q = un.q0 + et;
 #pragma unroll
             for (int bb = 0; bb < GROUP; ++bb) {
-                xr[bb] = pv ? ld_f32(prm.xs + p * prm.xs_r + (b0 + bb) * prm.xs_b) : 0.0f;
-                const int64_t q = q0 + et;
+                xr[bb] = p < prm.P ? ld_f32(prm.xs + p * prm.xs_r + (b0 + bb) * prm.xs_b) : 0.0f;
                 yr[bb] = (et < BN && q < prm.Q) ? ld_f32(prm.ys + q * prm.ys_r + (b0 + bb) * prm.ys_b) : 0.0f;
             }
         };
@@ -339,81 +411,117 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         };
 
         float xs_cur[GROUP], xs_nxt[GROUP], ysr[GROUP];
-        if (!SUMS && ngs > 0) {
-            load_scales(0, xs_cur, ysr);
+        int u = blockIdx.x;
+        Unit cu = unit(u < prm.units ? u : 0);
+        int G = 0;
+        if (!SUMS && u < prm.units && cu.nst > 0) {
+            load_scales(cu, 0, xs_cur, ysr);
             store_ys(0, ysr);
         }
         tc::named_bar_sync(1, NEPI * 32);
-        int g = 0;
-        for (int G = 0; G < ngs; ++G) {
-            if (!SUMS && G + 1 < ngs) load_scales(G + 1, xs_nxt, ysr);
+        int g = 0, gg = 0;  // block and scale-group counters over all units of this CTA
+        while (u < prm.units) {
+            const int ngs = cu.nst / 2;
+            // position after this group: the next group of this unit, or the next unit
+            int un_u = u, Gn = G + 1;
+            Unit nu = cu;
+            if (Gn >= ngs) {
+                un_u = u + gridDim.x;
+                Gn = 0;
+                if (un_u < prm.units) nu = unit(un_u);
+            }
+            const bool has_next = un_u < prm.units && nu.nst > 0;
+            if (!SUMS && has_next) load_scales(nu, Gn, xs_nxt, ysr);
+            if (ngs > 0) {
+                const int64_t p = cu.p0 + prow;
+                const bool pv = p < prm.P;
 #pragma unroll
-            for (int bb = 0; bb < GROUP; ++bb, ++g) {
-                const int buf = g % CF::kNbuf;
-                int ok = 0;
-                if (lane == 0) ok = bounded_wait(&tfull[buf], (g / CF::kNbuf) & 1, abort_flag, limit);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) continue;
-                tc::tc_fence_after_sync();
-                const float* ysb = ys_s + ((G & 1) * GROUP + bb) * BN + cb;
-                const int64_t b = static_cast<int64_t>(g_begin) * GROUP + g;
+                for (int bb = 0; bb < GROUP; ++bb, ++g) {
+                    const int buf = g % CF::kNbuf;
+                    int ok = 0;
+                    if (lane == 0) ok = bounded_wait(&tfull[buf], (g / CF::kNbuf) & 1, abort_flag, limit);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) continue;
+                    tc::tc_fence_after_sync();
+                    const float* ysb = ys_s + ((gg & 1) * GROUP + bb) * BN + cb;
+                    const int64_t b = static_cast<int64_t>(cu.g_begin + G) * GROUP + bb;
+                    const uint32_t tb = t_lane + static_cast<uint32_t>(buf * BN + cb);
+                    uint32_t ra[CF::kCH], rb[CF::kCH];
+                    tc::TmemLd<CF::kCH>::load(tb, ra);
+                    tc::TmemLd<CF::kCH>::wait(ra);
 #pragma unroll
-                for (int c = 0; c < CF::kCW / CF::kCH; ++c) {
-                    float sv[CF::kCH];
-                    tc::TmemLd<CF::kCH>::run(t_lane + static_cast<uint32_t>(buf * BN + cb + c * CF::kCH), sv);
-                    if constexpr (SUMS) {
-                        if (pv) {
+                    for (int c = 0; c < NCH; ++c) {
+                        uint32_t(&cur)[CF::kCH] = (c & 1) ? rb : ra;
+                        uint32_t(&nxt)[CF::kCH] = (c & 1) ? ra : rb;
+                        if (c + 1 < NCH)
+                            tc::TmemLd<CF::kCH>::load(tb + static_cast<uint32_t>((c + 1) * CF::kCH), nxt);
+                        if constexpr (SUMS) {
+                            if (pv) {
 #pragma unroll
-                            for (int t = 0; t < CF::kCH; ++t) {
-                                const int64_t q = q0 + cb + c * CF::kCH + t;
-                                if (q < prm.Q) prm.S[p * prm.sp + q * prm.sq + b] = static_cast<int32_t>(sv[t]);
+                                for (int t = 0; t < CF::kCH; ++t) {
+                                    const int64_t q = cu.q0 + cb + c * CF::kCH + t;
+                                    if (q < prm.Q)
+                                        prm.S[p * prm.sp + q * prm.sq + b] =
+                                            static_cast<int32_t>(__uint_as_float(cur[t]));
+                                }
+                            }
+                        } else {
+                            const float xsb = xs_cur[bb];
+#pragma unroll
+                            for (int t = 0; t < CF::kCH; t += 4) {
+                                const float4 y4 = *reinterpret_cast<const float4*>(ysb + c * CF::kCH + t);
+                                float* a4 = acc + c * CF::kCH + t;
+                                a4[0] = fmaf(xsb * y4.x, __uint_as_float(cur[t + 0]), a4[0]);
+                                a4[1] = fmaf(xsb * y4.y, __uint_as_float(cur[t + 1]), a4[1]);
+                                a4[2] = fmaf(xsb * y4.z, __uint_as_float(cur[t + 2]), a4[2]);
+                                a4[3] = fmaf(xsb * y4.w, __uint_as_float(cur[t + 3]), a4[3]);
                             }
                         }
-                    } else {
-                        const float xsb = xs_cur[bb];
+                        if (c + 1 < NCH) tc::TmemLd<CF::kCH>::wait(nxt);
+                    }
+                    tc::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&tempty[buf]);
+                }
+                if (!SUMS && G + 1 == ngs) {
+                    // last group of the unit: write its tile and start the next from zero
+                    if (*abort_flag == 0 && pv) {
+                        if (prm.vec_store) {
 #pragma unroll
-                        for (int t = 0; t < CF::kCH; t += 4) {
-                            const float4 y4 = *reinterpret_cast<const float4*>(ysb + c * CF::kCH + t);
-                            acc[c * CF::kCH + t + 0] = fmaf(xsb * y4.x, sv[t + 0], acc[c * CF::kCH + t + 0]);
-                            acc[c * CF::kCH + t + 1] = fmaf(xsb * y4.y, sv[t + 1], acc[c * CF::kCH + t + 1]);
-                            acc[c * CF::kCH + t + 2] = fmaf(xsb * y4.z, sv[t + 2], acc[c * CF::kCH + t + 2]);
-                            acc[c * CF::kCH + t + 3] = fmaf(xsb * y4.w, sv[t + 3], acc[c * CF::kCH + t + 3]);
+                            for (int t = 0; t < CF::kCW; t += 4) {
+                                const int64_t q = cu.q0 + cb + t;
+                                if (q < prm.Q)
+                                    *reinterpret_cast<float4*>(prm.C + p * prm.ldp + q) =
+                                        make_float4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int t = 0; t < CF::kCW; ++t) {
+                                const int64_t q = cu.q0 + cb + t;
+                                if (q < prm.Q) {
+                                    float* dst = prm.C + p * prm.ldp + q * prm.ldq;
+                                    if (prm.atomic)
+                                        atomicAdd(dst, acc[t]);
+                                    else
+                                        *dst = acc[t];
+                                }
+                            }
                         }
                     }
+#pragma unroll
+                    for (int t = 0; t < CF::kCW; ++t) acc[t] = 0.0f;
                 }
-                tc::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&tempty[buf]);
             }
-            if (!SUMS && G + 1 < ngs) {
-                store_ys((G + 1) & 1, ysr);
+            if (!SUMS && has_next) {
+                store_ys((gg + 1) & 1, ysr);
 #pragma unroll
                 for (int bb = 0; bb < GROUP; ++bb) xs_cur[bb] = xs_nxt[bb];
             }
             tc::named_bar_sync(1, NEPI * 32);
-        }
-        if (!SUMS && *abort_flag == 0 && pv) {
-            if (prm.vec_store) {
-#pragma unroll
-                for (int t = 0; t < CF::kCW; t += 4) {
-                    const int64_t q = q0 + cb + t;
-                    if (q < prm.Q)
-                        *reinterpret_cast<float4*>(prm.C + p * prm.ldp + q) =
-                            make_float4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]);
-                }
-            } else {
-#pragma unroll
-                for (int t = 0; t < CF::kCW; ++t) {
-                    const int64_t q = q0 + cb + t;
-                    if (q < prm.Q) {
-                        float* dst = prm.C + p * prm.ldp + q * prm.ldq;
-                        if (prm.atomic)
-                            atomicAdd(dst, acc[t]);
-                        else
-                            *dst = acc[t];
-                    }
-                }
-            }
+            ++gg;
+            if (un_u != u) cu = nu;
+            u = un_u;
+            G = Gn;
         }
     }
 
@@ -458,17 +566,31 @@ bool make_i8_map(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// f16 [rows, K] row-major, box {64 elements = 128 bytes, box_rows}, 128-byte
+// swizzle: the tile lands in the UMMA K-major SW128 layout.
+bool make_f16_map(CUtensorMap* map, const __half* base, int64_t rows, int64_t K, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(KS), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct DeviceInfo {
     int sms = 0;
     bool ok = false;
 };
 
-DeviceInfo device_info() {
+constexpr int kMaxDevices = 64;
+
+DeviceInfo device_info(int dev) {
     static std::mutex mu;
-    static DeviceInfo cache[64];
-    static bool have[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return {};
+    static DeviceInfo cache[kMaxDevices];
+    static bool have[kMaxDevices] = {};
     std::lock_guard<std::mutex> lk(mu);
     if (!have[dev]) {
         int major = 0, minor = 0, sms = 0;
@@ -482,25 +604,53 @@ DeviceInfo device_info() {
     return cache[dev];
 }
 
+// Per-device workspace for the f16 copy of the activations: allocated on first
+// use, grown (never shrunk) when a larger M*K arrives, kept until exit.
+std::mutex g_ws_mu;
+void* g_ws_ptr[kMaxDevices] = {};
+size_t g_ws_bytes[kMaxDevices] = {};
+
+cudaError_t workspace(int dev, size_t bytes, void** out) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    if (g_ws_bytes[dev] < bytes) {
+        if (g_ws_ptr[dev]) {
+            cudaError_t e = cudaFree(g_ws_ptr[dev]);  // synchronizes: no launch still reads it
+            if (e != cudaSuccess) return e;
+            g_ws_ptr[dev] = nullptr;
+            g_ws_bytes[dev] = 0;
+        }
+        const size_t want = std::max<size_t>(bytes, size_t(1) << 20);
+        cudaError_t e = cudaMalloc(&g_ws_ptr[dev], want);
+        if (e != cudaSuccess) {
+            g_ws_ptr[dev] = nullptr;
+            return e;
+        }
+        g_ws_bytes[dev] = want;
+    }
+    *out = g_ws_ptr[dev];
+    return cudaSuccess;
+}
+
 int g_inject_skip_stage = -1;
 unsigned long long g_timeout_cycles = 4000000000ull;  // ~2 s at 2 GHz
 
-template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS>
-cudaError_t launch_cfg(const CUtensorMap& mx, const CUtensorMap& my, const TcParams& prm, int64_t gx, int64_t gy,
-                       int splits, cudaStream_t stream) {
-    using CF = Cfg<BN, NCONV, NEPI, S8, S16>;
-    auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SUMS>;
+template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SWAP, bool SUMS>
+cudaError_t launch_cfg(const CUtensorMap& mw, const CUtensorMap& ma, const TcParams& prm, int64_t grid,
+                       cudaStream_t stream) {
+    using CF = Cfg<BN, NCONV, NEPI, S8, S16, SWAP>;
+    auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SWAP, SUMS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::kSmem);
     if (e != cudaSuccess) return e;
-    if (gx > 0x7fffffffLL || gy > 65535 || splits > 65535) return cudaErrorInvalidConfiguration;
-    return launch_pdl(kern, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(splits)),
-                      dim3(CF::kThreads), static_cast<size_t>(CF::kSmem), stream, mx, my, prm);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(CF::kThreads), static_cast<size_t>(CF::kSmem),
+                      stream, mw, ma, prm);
 }
 
 template <bool SUMS>
 cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
-    const DeviceInfo dev = device_info();
-    if (!dev.ok) return cudaErrorNotSupported;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorNotSupported;
+    const DeviceInfo info = device_info(dev);
+    if (!info.ok) return cudaErrorNotSupported;
     if (a.K % (KS * 2) != 0) return cudaErrorNotSupported;
     if (a.K > 0x7fffffffLL || a.M > 0x7fffffffLL || a.N > 0x7fffffffLL) return cudaErrorNotSupported;
     const int64_t KB = a.K / 32;
@@ -508,8 +658,6 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
     TcParams prm{};
     const int64_t P = swap ? a.N : a.M;
     const int64_t Q = swap ? a.M : a.N;
-    const int8_t* X = swap ? a.W : a.A;
-    const int8_t* Y = swap ? a.A : a.W;
     // scale planes: AS [M, KB]; WS [N, KB] (layout 0) or [KB, N] (layout 1)
     const int64_t ws_r = a.ws_layout == 0 ? KB : 1, ws_b = a.ws_layout == 0 ? 1 : a.N;
     if (swap) {
@@ -535,27 +683,53 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
     const int64_t gx = (P + BM - 1) / BM;
     const int64_t gy = (Q + BN - 1) / BN;
     const int ngroups = static_cast<int>(a.K / (KS * 2));
-    // split K when the tiles alone leave SMs idle (two CTAs fit an SM on the swapped path)
-    int splits = 1;
+    // Persistent CTAs, one per SM, take the work units round-robin.  K is split
+    // when the tiles are too few for the SMs: the smallest split count whose
+    // units spread evenly (the busiest SM within ~5% of the mean), each split
+    // keeping at least two scale groups.
     const int64_t tiles = gx * gy;
-    const int64_t slots = static_cast<int64_t>(dev.sms) * (swap ? 2 : 1);
-    if (tiles < slots) splits = static_cast<int>(std::min<int64_t>(ngroups, std::max<int64_t>(1, slots / tiles)));
+    const int64_t sms = info.sms;
+    int splits = 1;
+    if (tiles < 4 * sms) {
+        for (int s = 1; s <= std::max(1, ngroups / 2); ++s) {
+            const int64_t units = tiles * s;
+            const double per_sm = static_cast<double>(units) / sms;
+            const int64_t busiest = (units + sms - 1) / sms;
+            splits = s;
+            if (units >= sms && busiest <= per_sm * 1.05 + 1e-9) break;
+        }
+    }
     prm.groups_per_split = (ngroups + splits - 1) / splits;
     splits = (ngroups + prm.groups_per_split - 1) / prm.groups_per_split;
+    if (tiles * splits > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    prm.splits = splits;
+    prm.tiles_q = static_cast<int>(gy);
+    prm.units = static_cast<int>(tiles * splits);
+    const int64_t grid = std::min<int64_t>(prm.units, sms);
     prm.atomic = (!SUMS && splits > 1) ? 1 : 0;
     prm.vec_store = (!SUMS && !swap && !prm.atomic && (Q % 4 == 0) &&
                      (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0) ? 1 : 0;
 
-    CUtensorMap mx, my;
-    if (!make_i8_map(&mx, X, P, a.K, BM) || !make_i8_map(&my, Y, Q, a.K, BN)) return cudaErrorInvalidValue;
+    // f16 copy of the activations in the workspace, by a pre-pass kernel
+    void* ws = nullptr;
+    cudaError_t e = workspace(dev, static_cast<size_t>(a.M * a.K) * sizeof(__half), &ws);
+    if (e != cudaSuccess) return e;
+    __half* a16 = static_cast<__half*>(ws);
+    CUtensorMap mw, ma;
+    if (!make_i8_map(&mw, a.W, a.N, a.K, swap ? BM : BN) || !make_f16_map(&ma, a16, a.M, a.K, swap ? BN : BM))
+        return cudaErrorInvalidValue;
+    const int64_t n16 = a.M * a.K / 16;
+    e = launch_pdl(i8_to_f16_kernel, dim3(static_cast<unsigned>((n16 + 255) / 256)), dim3(256), 0, stream, a.A, a16,
+                   n16);
+    if (e != cudaSuccess) return e;
     if (prm.atomic) {
-        cudaError_t e = cudaMemsetAsync(a.C, 0, static_cast<size_t>(a.M * a.N) * sizeof(float), stream);
+        e = cudaMemsetAsync(a.C, 0, static_cast<size_t>(a.M * a.N) * sizeof(float), stream);
         if (e != cudaSuccess) return e;
     }
-    if (!swap) return launch_cfg<128, 2, 8, 4, 4, 1, SUMS>(mx, my, prm, gx, gy, splits, stream);
-    if (BN == 16) return launch_cfg<16, 2, 4, 3, 3, 2, SUMS>(mx, my, prm, gx, gy, splits, stream);
-    if (BN == 32) return launch_cfg<32, 2, 4, 3, 3, 2, SUMS>(mx, my, prm, gx, gy, splits, stream);
-    return launch_cfg<64, 2, 4, 3, 3, 2, SUMS>(mx, my, prm, gx, gy, splits, stream);
+    if (!swap) return launch_cfg<128, 2, 8, 4, 4, 1, false, SUMS>(mw, ma, prm, grid, stream);
+    if (BN == 16) return launch_cfg<16, 4, 8, 4, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
+    if (BN == 32) return launch_cfg<32, 4, 8, 4, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
+    return launch_cfg<64, 4, 8, 4, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
 }
 
 }  // namespace
