@@ -61,6 +61,7 @@ namespace {
 constexpr int BM = 128;      // rows of the MMA's A operand per tile (MMA M, TMEM lanes)
 constexpr int KS = 64;       // K elements per pipeline stage (two Q8_0 blocks)
 constexpr int GROUP = 4;     // Q8_0 blocks per scale group (128 K, two stages)
+constexpr int SSLOTS = 4;    // scale ring slots (groups prefetched SSLOTS - 1 ahead)
 
 struct TcParams {
     const float* xs;          // scale of MMA-A row p, block b: xs[p * xs_r + b * xs_b]
@@ -103,8 +104,9 @@ struct Cfg {
     static constexpr int kOffW8 = 0;
     static constexpr int kOffA16 = kOffW8 + S8 * kW8;
     static constexpr int kOffB16 = kOffA16 + S16 * kA16;
-    static constexpr int kOffYs = kOffB16 + S16 * kB16;   // 2 x [GROUP][BN] f32
-    static constexpr int kOffBar = kOffYs + 2 * GROUP * BN * 4;
+    static constexpr int kSlot = GROUP * (BM + BN);        // floats per scale slot: xs [4][128], ys [4][BN]
+    static constexpr int kOffYs = kOffB16 + S16 * kB16;   // SSLOTS x scale slot
+    static constexpr int kOffBar = kOffYs + SSLOTS * kSlot * 4;
     static constexpr int kNumBars = 2 * S8 + 2 * S16 + 2 * kNbuf + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;    // + alignment slack
@@ -391,50 +393,79 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 #pragma unroll
         for (int t = 0; t < CF::kCW; ++t) acc[t] = 0.0f;
 
-        // scales of scale group G of unit un: this thread's MMA-A row (4 blocks) and,
-        // for et < BN, MMA-B row q0 + et (4 blocks)
-        auto load_scales = [&](const Unit& un, int G, float (&xr)[GROUP], float (&yr)[GROUP]) {
+        // Scale ring: slot = [GROUP][BM] MMA-A row scales, then [GROUP][BN] MMA-B row
+        // scales, filled with cp.async SSLOTS - 1 scale groups ahead of their use.
+        // Epilogue threads of the first column half copy their row's 4 scales;
+        // those of the second half copy one MMA-B row's 4 scales each.
+        auto prefetch = [&](const Unit& un, int G, int slot) {
+            float* xs_d = ys_s + slot * CF::kSlot;
+            float* ys_d = xs_d + GROUP * BM;
             const int64_t b0 = static_cast<int64_t>(un.g_begin + G) * GROUP;
-            const int64_t p = un.p0 + prow;
-            const int64_t q = un.q0 + et;
+            if (e < 4) {
+                const int64_t p = un.p0 + prow;
 #pragma unroll
-            for (int bb = 0; bb < GROUP; ++bb) {
-                xr[bb] = p < prm.P ? ld_f32(prm.xs + p * prm.xs_r + (b0 + bb) * prm.xs_b) : 0.0f;
-                yr[bb] = (et < BN && q < prm.Q) ? ld_f32(prm.ys + q * prm.ys_r + (b0 + bb) * prm.ys_b) : 0.0f;
+                for (int bb = 0; bb < GROUP; ++bb) {
+                    if (p < prm.P) tc::cp_async_4(xs_d + bb * BM + prow, prm.xs + p * prm.xs_r + (b0 + bb) * prm.xs_b);
+                    else xs_d[bb * BM + prow] = 0.0f;
+                }
+            } else {
+                const int qi = et - 4 * 32;
+                const int64_t q = un.q0 + qi;
+                if (qi < BN) {
+#pragma unroll
+                    for (int bb = 0; bb < GROUP; ++bb) {
+                        if (q < prm.Q) tc::cp_async_4(ys_d + bb * BN + qi, prm.ys + q * prm.ys_r + (b0 + bb) * prm.ys_b);
+                        else ys_d[bb * BN + qi] = 0.0f;
+                    }
+                }
             }
         };
-        auto store_ys = [&](int buf, const float (&yr)[GROUP]) {
-            if (et < BN) {
-#pragma unroll
-                for (int bb = 0; bb < GROUP; ++bb) ys_s[(buf * GROUP + bb) * BN + et] = yr[bb];
-            }
-        };
+        static_assert(NEPI == 8 || BN <= 0, "scale prefetch assumes two column halves of epilogue warps");
 
-        float xs_cur[GROUP], xs_nxt[GROUP], ysr[GROUP];
+        // cursor over this CTA's (unit, group) sequence, for the prefetch
+        int pu = blockIdx.x, pG = 0;
+        Unit pun = unit(pu < prm.units ? pu : 0);
+        auto advance = [&](int& uu, int& GG, Unit& un) {
+            if (++GG >= un.nst / 2) {
+                uu += gridDim.x;
+                GG = 0;
+                if (uu < prm.units) un = unit(uu);
+            }
+        };
+        int issued = 0;
+        if (!SUMS) {
+            for (int k = 0; k < SSLOTS - 1; ++k) {
+                if (pu < prm.units) {
+                    prefetch(pun, pG, issued % SSLOTS);
+                    advance(pu, pG, pun);
+                }
+                tc::cp_async_commit();
+                ++issued;
+            }
+        }
+
         int u = blockIdx.x;
         Unit cu = unit(u < prm.units ? u : 0);
         int G = 0;
-        if (!SUMS && u < prm.units && cu.nst > 0) {
-            load_scales(cu, 0, xs_cur, ysr);
-            store_ys(0, ysr);
-        }
-        tc::named_bar_sync(1, NEPI * 32);
         int g = 0, gg = 0;  // block and scale-group counters over all units of this CTA
         while (u < prm.units) {
             const int ngs = cu.nst / 2;
-            // position after this group: the next group of this unit, or the next unit
-            int un_u = u, Gn = G + 1;
-            Unit nu = cu;
-            if (Gn >= ngs) {
-                un_u = u + gridDim.x;
-                Gn = 0;
-                if (un_u < prm.units) nu = unit(un_u);
+            if (!SUMS) {
+                // this group's scales landed (per thread), then visible to all epilogue threads;
+                // the barrier also orders every thread's reads of the slot refilled below
+                tc::cp_async_wait<SSLOTS - 2>();
+                tc::named_bar_sync(1, NEPI * 32);
+                if (pu < prm.units) {
+                    prefetch(pun, pG, issued % SSLOTS);
+                    advance(pu, pG, pun);
+                }
+                tc::cp_async_commit();
+                ++issued;
             }
-            const bool has_next = un_u < prm.units && nu.nst > 0;
-            if (!SUMS && has_next) load_scales(nu, Gn, xs_nxt, ysr);
             if (ngs > 0) {
                 const int64_t p = cu.p0 + prow;
                 const bool pv = p < prm.P;
+                const float* slot = ys_s + (gg % SSLOTS) * CF::kSlot;
 #pragma unroll
                 for (int bb = 0; bb < GROUP; ++bb, ++g) {
                     const int buf = g % CF::kNbuf;
@@ -443,7 +474,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) continue;
                     tc::tc_fence_after_sync();
-                    const float* ysb = ys_s + ((gg & 1) * GROUP + bb) * BN + cb;
+                    const float* ysb = slot + GROUP * BM + bb * BN + cb;
                     const int64_t b = static_cast<int64_t>(cu.g_begin + G) * GROUP + bb;
                     const uint32_t tb = t_lane + static_cast<uint32_t>(buf * BN + cb);
                     uint32_t ra[CF::kCH], rb[CF::kCH];
@@ -466,7 +497,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                                 }
                             }
                         } else {
-                            const float xsb = xs_cur[bb];
+                            const float xsb = slot[bb * BM + prow];
 #pragma unroll
                             for (int t = 0; t < CF::kCH; t += 4) {
                                 const float4 y4 = *reinterpret_cast<const float4*>(ysb + c * CF::kCH + t);
@@ -512,17 +543,10 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     for (int t = 0; t < CF::kCW; ++t) acc[t] = 0.0f;
                 }
             }
-            if (!SUMS && has_next) {
-                store_ys((gg + 1) & 1, ysr);
-#pragma unroll
-                for (int bb = 0; bb < GROUP; ++bb) xs_cur[bb] = xs_nxt[bb];
-            }
-            tc::named_bar_sync(1, NEPI * 32);
             ++gg;
-            if (un_u != u) cu = nu;
-            u = un_u;
-            G = Gn;
+            advance(u, G, cu);
         }
+        if (!SUMS) tc::cp_async_wait<0>();  // no copy may land after the CTA exits
     }
 
     __syncthreads();
@@ -726,10 +750,10 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
         e = cudaMemsetAsync(a.C, 0, static_cast<size_t>(a.M * a.N) * sizeof(float), stream);
         if (e != cudaSuccess) return e;
     }
-    if (!swap) return launch_cfg<128, 2, 8, 4, 4, 1, false, SUMS>(mw, ma, prm, grid, stream);
-    if (BN == 16) return launch_cfg<16, 4, 8, 4, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
-    if (BN == 32) return launch_cfg<32, 4, 8, 4, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
-    return launch_cfg<64, 4, 8, 4, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
+    if (!swap) return launch_cfg<128, 2, 8, 8, 4, 1, false, SUMS>(mw, ma, prm, grid, stream);
+    if (BN == 16) return launch_cfg<16, 4, 8, 8, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
+    if (BN == 32) return launch_cfg<32, 4, 8, 8, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
+    return launch_cfg<64, 4, 8, 8, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
 }
 
 }  // namespace
