@@ -75,7 +75,7 @@ struct TcParams {
     int64_t P, Q, K;
     int groups_per_split;
     int splits;               // K splits per tile
-    int tiles_q;              // tiles along Q
+    int tiles_p;              // tiles along P
     int units;                // tiles_p * tiles_q * splits work units, taken round-robin by the CTAs
     int atomic;               // split-K: red.add into a zeroed C
     int vec_store;            // ldq == 1, Q % 4 == 0, C 16-byte aligned: float4 stores
@@ -83,10 +83,9 @@ struct TcParams {
     unsigned long long timeout_cycles;
 };
 
-// SWAP = false: MMA-A = activations (f16, by TMA), MMA-B = weights (int8 by
-// TMA, converted).  SWAP = true: MMA-A = weights (converted), MMA-B =
-// activations.  The weight tile is always the converted one.
-template <int BN, int NCONV, int NEPI, int S8, int S16, bool SWAP>
+// MMA-A ("X", 128 rows per tile) and MMA-B ("Y", BN rows) both arrive as int8
+// by TMA into the int8 ring and are converted to f16 by the converter warps.
+template <int BN, int NCONV, int NEPI, int S8, int S16>
 struct Cfg {
     static constexpr int kThreads = 32 * (2 + NCONV + NEPI);
     static constexpr int kE0 = 2 + NCONV;                 // first epilogue warp
@@ -95,27 +94,27 @@ struct Cfg {
                                      : (kNbuf * BN <= 256) ? 256 : 512;
     static constexpr int kCW = BN / (NEPI / 4);          // columns per epilogue warp
     static constexpr int kCH = kCW < 16 ? kCW : 16;       // columns per tcgen05.ld
-    static constexpr int kCR = SWAP ? BM : BN;            // converted (weight) rows per stage
-    static constexpr int kFR = SWAP ? BN : BM;            // f16 (activation) rows per stage
-    static constexpr int kW8 = kCR * KS;                  // int8 weight tile bytes
-    static constexpr int kA16 = BM * KS * 2;              // f16 MMA-A tile bytes
-    static constexpr int kB16 = BN * KS * 2;              // f16 MMA-B tile bytes
-    static constexpr int kF16 = kFR * KS * 2;             // bytes the TMA brings per f16 stage
-    static constexpr int kOffW8 = 0;
-    static constexpr int kOffA16 = kOffW8 + S8 * kW8;
-    static constexpr int kOffB16 = kOffA16 + S16 * kA16;
+    static constexpr int kX8 = BM * KS;                   // int8 X tile bytes
+    static constexpr int kY8 = BN * KS;
+    static constexpr int kX16 = BM * KS * 2;              // f16 X tile bytes
+    static constexpr int kY16 = BN * KS * 2;
+    static constexpr int kOffX8 = 0;
+    static constexpr int kOffY8 = kOffX8 + S8 * kX8;
+    static constexpr int kOffX16 = kOffY8 + S8 * kY8;
+    static constexpr int kOffY16 = kOffX16 + S16 * kX16;
     static constexpr int kSlot = GROUP * (BM + BN);        // floats per scale slot: xs [4][128], ys [4][BN]
-    static constexpr int kOffYs = kOffB16 + S16 * kB16;   // SSLOTS x scale slot
+    static constexpr int kOffYs = kOffY16 + S16 * kY16;   // SSLOTS x scale slot
     static constexpr int kOffBar = kOffYs + SSLOTS * kSlot * 4;
     static constexpr int kNumBars = 2 * S8 + 2 * S16 + 2 * kNbuf + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;    // + alignment slack
-    static constexpr int kOctPerWarp = kCR / 8 / NCONV;   // row octets each converter warp takes
+    static constexpr int kOct = (BM + BN) / 8;            // row octets converted per stage
+    static constexpr int kOctPerWarp = (kOct + NCONV - 1) / NCONV;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
-    static_assert(NEPI == 4 || NEPI == 8, "epilogue warps cover the four TMEM lane quadrants");
+    static_assert(NEPI == 8, "epilogue warps: two column halves over the four TMEM lane quadrants");
     static_assert(kCW % kCH == 0 && kCH % 8 == 0, "epilogue column chunks");
-    static_assert(kCR % (8 * NCONV) == 0, "converter work splits evenly");
-    static_assert(kW8 % 1024 == 0 && kA16 % 1024 == 0 && kB16 % 1024 == 0, "1024-B aligned tiles");
+    static_assert(kX8 % 1024 == 0 && kY8 % 1024 == 0 && kX16 % 1024 == 0 && kY16 % 1024 == 0, "1024-B tiles");
+    static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 __device__ __forceinline__ void set_abort(volatile int* abort_flag) {
@@ -168,33 +167,11 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
-// Activation pre-pass: int8 [rows, K] -> f16 [rows, K] (exact), 16 bytes per
-// thread.  The tensor-core kernel then loads activation tiles with TMA straight
-// into the MMA operand layout, so that only the weights are converted in it.
-__global__ void __launch_bounds__(256) i8_to_f16_kernel(const int8_t* __restrict__ src, __half* __restrict__ dst,
-                                                        int64_t n16) {
-    pdl_trigger();
-    pdl_wait();
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
-    if (i >= n16) return;
-    uint4 v;
-    asm volatile("ld.global.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(src + i * 16) : "memory");
-    uint4 o0, o1;
-    i8x4_to_f16x4(v.x, o0.x, o0.y);
-    i8x4_to_f16x4(v.y, o0.z, o0.w);
-    i8x4_to_f16x4(v.z, o1.x, o1.y);
-    i8x4_to_f16x4(v.w, o1.z, o1.w);
-    uint4* d = reinterpret_cast<uint4*>(dst + i * 16);
-    d[0] = o0;
-    d[1] = o1;
-}
-
-template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SWAP, bool SUMS>
-__global__ void __launch_bounds__(Cfg<BN, NCONV, NEPI, S8, S16, SWAP>::kThreads, MINB)
-qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS>
+__global__ void __launch_bounds__(Cfg<BN, NCONV, NEPI, S8, S16>::kThreads, MINB)
+qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
                const TcParams prm) {
-    using CF = Cfg<BN, NCONV, NEPI, S8, S16, SWAP>;
+    using CF = Cfg<BN, NCONV, NEPI, S8, S16>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::kOffBar);
@@ -207,7 +184,8 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     uint64_t* drain = tempty + CF::kNbuf;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + CF::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + CF::kOffMisc + 4);
-    float* ys_s = reinterpret_cast<float*>(smem + CF::kOffYs);
+    const uint32_t sbase = tc::smem_u32(smem);  // the same bytes in the shared window
+    const uint32_t ys_sa = sbase + CF::kOffYs;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -221,10 +199,12 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     };
     auto unit = [&](int u) {
         Unit r;
+        // the P tile varies fastest: CTAs running at the same time share Q tiles
+        // (the operand with more tiles) and spread their reads of the P operand
         const int z = u % prm.splits;
         const int t = u / prm.splits;
-        r.q0 = static_cast<int64_t>(t % prm.tiles_q) * BN;
-        r.p0 = static_cast<int64_t>(t / prm.tiles_q) * BM;
+        r.p0 = static_cast<int64_t>(t % prm.tiles_p) * BM;
+        r.q0 = static_cast<int64_t>(t / prm.tiles_p) * BN;
         r.g_begin = z * prm.groups_per_split;
         r.nst = 2 * max(0, min(ngroups, r.g_begin + prm.groups_per_split) - r.g_begin);
         return r;
@@ -237,7 +217,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             tc::mbar_init(&empty8[i], NCONV);
         }
         for (int i = 0; i < S16; ++i) {
-            tc::mbar_init(&full16[i], NCONV + 1);  // the converters + the producer's TMA
+            tc::mbar_init(&full16[i], NCONV);
             tc::mbar_init(&empty16[i], 1);
         }
         for (int i = 0; i < CF::kNbuf; ++i) {
@@ -247,8 +227,8 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         tc::mbar_init(drain, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
-        tc::tma_prefetch_map(&tmW);
-        tc::tma_prefetch_map(&tmA);
+        tc::tma_prefetch_map(&tmX);
+        tc::tma_prefetch_map(&tmY);
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, CF::kTmemCols);
@@ -264,37 +244,24 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued8 = 0, issued16 = 0;
+            int issued8 = 0;
             int gi = 0;  // stage counter over all units of this CTA
             for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
                 const Unit un = unit(u);
-                const int w_row = static_cast<int>(SWAP ? un.p0 : un.q0);
-                const int a_row = static_cast<int>(SWAP ? un.q0 : un.p0);
                 for (int i = 0; i < un.nst; ++i, ++gi) {
-                    const int s16 = gi % S16, s8 = gi % S8;
+                    const int s8 = gi % S8;
                     const int kx = (2 * un.g_begin + i) * KS;
-                    if (bounded_wait(&empty16[s16], ((gi / S16) & 1) ^ 1, abort_flag, limit)) {
-                        issued16 = gi + 1;
-                        tc::mbar_arrive_expect_tx(&full16[s16], CF::kF16);
-                        uint8_t* dst =
-                            SWAP ? smem + CF::kOffB16 + s16 * CF::kB16 : smem + CF::kOffA16 + s16 * CF::kA16;
-                        tc::tma_load_2d(dst, &tmA, &full16[s16], kx, a_row);
-                    }
-                    if (bounded_wait(&empty8[s8], ((gi / S8) & 1) ^ 1, abort_flag, limit)) {
-                        issued8 = gi + 1;
-                        if (gi == prm.inject_skip_stage) continue;  // test hook: never arrives
-                        tc::mbar_arrive_expect_tx(&full8[s8], CF::kW8);
-                        tc::tma_load_2d(smem + CF::kOffW8 + s8 * CF::kW8, &tmW, &full8[s8], kx, w_row);
-                    }
+                    if (!bounded_wait(&empty8[s8], ((gi / S8) & 1) ^ 1, abort_flag, limit)) continue;
+                    issued8 = gi + 1;
+                    if (gi == prm.inject_skip_stage) continue;  // test hook: never arrives
+                    tc::mbar_arrive_expect_tx(&full8[s8], CF::kX8 + CF::kY8);
+                    tc::tma_load_2d(smem + CF::kOffX8 + s8 * CF::kX8, &tmX, &full8[s8], kx, static_cast<int>(un.p0));
+                    tc::tma_load_2d(smem + CF::kOffY8 + s8 * CF::kY8, &tmY, &full8[s8], kx, static_cast<int>(un.q0));
                 }
             }
             // copies in flight land before the CTA may exit
             for (int i = max(0, issued8 - S8); i < issued8; ++i)
                 if (i != prm.inject_skip_stage) drain_wait(&full8[i % S8], (i / S8) & 1, limit);
-            // an f16 stage completes with its TMA bytes and the converters' arrivals,
-            // which the converters make for every stage, also after an abort
-            for (int i = max(0, issued16 - S16); i < issued16; ++i)
-                drain_wait(&full16[i % S16], (i / S16) & 1, limit);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -307,8 +274,8 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     const int s = gi % S16;
                     const bool ok = bounded_wait(&full16[s], (gi / S16) & 1, abort_flag, limit);
                     if (ok) tc::tc_fence_after_sync();
-                    const uint32_t xa = tc::smem_u32(smem + CF::kOffA16 + s * CF::kA16);
-                    const uint32_t ya = tc::smem_u32(smem + CF::kOffB16 + s * CF::kB16);
+                    const uint32_t xa = sbase + CF::kOffX16 + s * CF::kX16;
+                    const uint32_t ya = sbase + CF::kOffY16 + s * CF::kY16;
 #pragma unroll
                     for (int bb = 0; bb < 2; ++bb, ++g) {
                         const int buf = g % CF::kNbuf;
@@ -324,8 +291,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                         }
                         tc::umma_commit(&tfull[buf]);
                     }
-                    // release the f16 stage once its MMAs completed (also after an abort,
-                    // so that the producer's drain sees every issued stage released)
+                    // release the f16 stage once its MMAs completed
                     tc::umma_commit(&empty16[s]);
                 }
             }
@@ -348,32 +314,42 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                          bounded_wait(&empty16[s16], ((gi / S16) & 1) ^ 1, abort_flag, limit);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (ok) {
-                    const uint8_t* w8 = smem + CF::kOffW8 + s8 * CF::kW8;
-                    uint8_t* w16 = SWAP ? smem + CF::kOffA16 + s16 * CF::kA16 : smem + CF::kOffB16 + s16 * CF::kB16;
+                    const uint32_t x8 = sbase + CF::kOffX8 + s8 * CF::kX8;
+                    const uint32_t y8 = sbase + CF::kOffY8 + s8 * CF::kY8;
+                    const uint32_t x16 = sbase + CF::kOffX16 + s16 * CF::kX16;
+                    const uint32_t y16 = sbase + CF::kOffY16 + s16 * CF::kY16;
                     uint4 v[CF::kOctPerWarp];
 #pragma unroll
                     for (int t = 0; t < CF::kOctPerWarp; ++t) {  // all loads first
-                        const int row = (cw + t * NCONV) * 8 + r_in;
-                        v[t] = *reinterpret_cast<const uint4*>(w8 + row * KS + ((c8 ^ ((row >> 1) & 3)) << 4));
+                        const int o = cw + t * NCONV;
+                        if (o < CF::kOct) {
+                            const bool isx = o < BM / 8;
+                            const int row = (isx ? o : o - BM / 8) * 8 + r_in;
+                            v[t] = tc::lds128((isx ? x8 : y8) + row * KS + ((c8 ^ ((row >> 1) & 3)) << 4));
+                        }
                     }
 #pragma unroll
                     for (int t = 0; t < CF::kOctPerWarp; ++t) {
-                        const int row = (cw + t * NCONV) * 8 + r_in;
-                        uint4 o0, o1;
-                        i8x4_to_f16x4(v[t].x, o0.x, o0.y);
-                        i8x4_to_f16x4(v[t].y, o0.z, o0.w);
-                        i8x4_to_f16x4(v[t].z, o1.x, o1.y);
-                        i8x4_to_f16x4(v[t].w, o1.z, o1.w);
-                        uint8_t* dst = w16 + row * (KS * 2);
-                        *reinterpret_cast<uint4*>(dst + (((2 * c8) ^ (row & 7)) << 4)) = o0;
-                        *reinterpret_cast<uint4*>(dst + (((2 * c8 + 1) ^ (row & 7)) << 4)) = o1;
+                        const int o = cw + t * NCONV;
+                        if (o < CF::kOct) {
+                            const bool isx = o < BM / 8;
+                            const int row = (isx ? o : o - BM / 8) * 8 + r_in;
+                            uint4 o0, o1;
+                            i8x4_to_f16x4(v[t].x, o0.x, o0.y);
+                            i8x4_to_f16x4(v[t].y, o0.z, o0.w);
+                            i8x4_to_f16x4(v[t].z, o1.x, o1.y);
+                            i8x4_to_f16x4(v[t].w, o1.z, o1.w);
+                            const uint32_t dst = (isx ? x16 : y16) + row * (KS * 2);
+                            tc::sts128(dst + (((2 * c8) ^ (row & 7)) << 4), o0);
+                            tc::sts128(dst + (((2 * c8 + 1) ^ (row & 7)) << 4), o1);
+                        }
                     }
                     tc::fence_proxy_async_smem();
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    // arrive even after an abort, so that full16 completes for stages
-                    // whose f16 bytes the producer already issued
+                    // arrive also after an abort: the producer's drain and every later
+                    // wait then find the barriers in a consistent phase
                     tc::mbar_arrive(&empty8[s8]);
                     tc::mbar_arrive(&full16[s16]);
                 }
@@ -398,15 +374,16 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         // Epilogue threads of the first column half copy their row's 4 scales;
         // those of the second half copy one MMA-B row's 4 scales each.
         auto prefetch = [&](const Unit& un, int G, int slot) {
-            float* xs_d = ys_s + slot * CF::kSlot;
-            float* ys_d = xs_d + GROUP * BM;
+            const uint32_t xs_d = ys_sa + slot * CF::kSlot * 4;
+            const uint32_t ys_d = xs_d + GROUP * BM * 4;
             const int64_t b0 = static_cast<int64_t>(un.g_begin + G) * GROUP;
             if (e < 4) {
                 const int64_t p = un.p0 + prow;
 #pragma unroll
                 for (int bb = 0; bb < GROUP; ++bb) {
-                    if (p < prm.P) tc::cp_async_4(xs_d + bb * BM + prow, prm.xs + p * prm.xs_r + (b0 + bb) * prm.xs_b);
-                    else xs_d[bb * BM + prow] = 0.0f;
+                    const uint32_t d = xs_d + (bb * BM + prow) * 4;
+                    if (p < prm.P) tc::cp_async_4(d, prm.xs + p * prm.xs_r + (b0 + bb) * prm.xs_b);
+                    else tc::sts32f(d, 0.0f);
                 }
             } else {
                 const int qi = et - 4 * 32;
@@ -414,8 +391,9 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 if (qi < BN) {
 #pragma unroll
                     for (int bb = 0; bb < GROUP; ++bb) {
-                        if (q < prm.Q) tc::cp_async_4(ys_d + bb * BN + qi, prm.ys + q * prm.ys_r + (b0 + bb) * prm.ys_b);
-                        else ys_d[bb * BN + qi] = 0.0f;
+                        const uint32_t d = ys_d + (bb * BN + qi) * 4;
+                        if (q < prm.Q) tc::cp_async_4(d, prm.ys + q * prm.ys_r + (b0 + bb) * prm.ys_b);
+                        else tc::sts32f(d, 0.0f);
                     }
                 }
             }
@@ -465,7 +443,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             if (ngs > 0) {
                 const int64_t p = cu.p0 + prow;
                 const bool pv = p < prm.P;
-                const float* slot = ys_s + (gg % SSLOTS) * CF::kSlot;
+                const uint32_t slot = ys_sa + (gg % SSLOTS) * CF::kSlot * 4;
 #pragma unroll
                 for (int bb = 0; bb < GROUP; ++bb, ++g) {
                     const int buf = g % CF::kNbuf;
@@ -474,7 +452,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) continue;
                     tc::tc_fence_after_sync();
-                    const float* ysb = slot + GROUP * BM + bb * BN + cb;
+                    const uint32_t ysb = slot + (GROUP * BM + bb * BN + cb) * 4;
                     const int64_t b = static_cast<int64_t>(cu.g_begin + G) * GROUP + bb;
                     const uint32_t tb = t_lane + static_cast<uint32_t>(buf * BN + cb);
                     uint32_t ra[CF::kCH], rb[CF::kCH];
@@ -497,10 +475,10 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                                 }
                             }
                         } else {
-                            const float xsb = slot[bb * BM + prow];
+                            const float xsb = tc::lds32f(slot + (bb * BM + prow) * 4);
 #pragma unroll
                             for (int t = 0; t < CF::kCH; t += 4) {
-                                const float4 y4 = *reinterpret_cast<const float4*>(ysb + c * CF::kCH + t);
+                                const float4 y4 = tc::lds128f(ysb + (c * CF::kCH + t) * 4);
                                 float* a4 = acc + c * CF::kCH + t;
                                 a4[0] = fmaf(xsb * y4.x, __uint_as_float(cur[t + 0]), a4[0]);
                                 a4[1] = fmaf(xsb * y4.y, __uint_as_float(cur[t + 1]), a4[1]);
@@ -590,20 +568,6 @@ bool make_i8_map(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// f16 [rows, K] row-major, box {64 elements = 128 bytes, box_rows}, 128-byte
-// swizzle: the tile lands in the UMMA K-major SW128 layout.
-bool make_f16_map(CUtensorMap* map, const __half* base, int64_t rows, int64_t K, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * 2)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(KS), static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 struct DeviceInfo {
     int sms = 0;
     bool ok = false;
@@ -628,45 +592,18 @@ DeviceInfo device_info(int dev) {
     return cache[dev];
 }
 
-// Per-device workspace for the f16 copy of the activations: allocated on first
-// use, grown (never shrunk) when a larger M*K arrives, kept until exit.
-std::mutex g_ws_mu;
-void* g_ws_ptr[kMaxDevices] = {};
-size_t g_ws_bytes[kMaxDevices] = {};
-
-cudaError_t workspace(int dev, size_t bytes, void** out) {
-    std::lock_guard<std::mutex> lk(g_ws_mu);
-    if (g_ws_bytes[dev] < bytes) {
-        if (g_ws_ptr[dev]) {
-            cudaError_t e = cudaFree(g_ws_ptr[dev]);  // synchronizes: no launch still reads it
-            if (e != cudaSuccess) return e;
-            g_ws_ptr[dev] = nullptr;
-            g_ws_bytes[dev] = 0;
-        }
-        const size_t want = std::max<size_t>(bytes, size_t(1) << 20);
-        cudaError_t e = cudaMalloc(&g_ws_ptr[dev], want);
-        if (e != cudaSuccess) {
-            g_ws_ptr[dev] = nullptr;
-            return e;
-        }
-        g_ws_bytes[dev] = want;
-    }
-    *out = g_ws_ptr[dev];
-    return cudaSuccess;
-}
-
 int g_inject_skip_stage = -1;
 unsigned long long g_timeout_cycles = 4000000000ull;  // ~2 s at 2 GHz
 
-template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SWAP, bool SUMS>
-cudaError_t launch_cfg(const CUtensorMap& mw, const CUtensorMap& ma, const TcParams& prm, int64_t grid,
+template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS>
+cudaError_t launch_cfg(const CUtensorMap& mx, const CUtensorMap& my, const TcParams& prm, int64_t grid,
                        cudaStream_t stream) {
-    using CF = Cfg<BN, NCONV, NEPI, S8, S16, SWAP>;
-    auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SWAP, SUMS>;
+    using CF = Cfg<BN, NCONV, NEPI, S8, S16>;
+    auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SUMS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::kSmem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(CF::kThreads), static_cast<size_t>(CF::kSmem),
-                      stream, mw, ma, prm);
+                      stream, mx, my, prm);
 }
 
 template <bool SUMS>
@@ -727,33 +664,26 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
     splits = (ngroups + prm.groups_per_split - 1) / prm.groups_per_split;
     if (tiles * splits > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     prm.splits = splits;
-    prm.tiles_q = static_cast<int>(gy);
+    prm.tiles_p = static_cast<int>(gx);
     prm.units = static_cast<int>(tiles * splits);
     const int64_t grid = std::min<int64_t>(prm.units, sms);
     prm.atomic = (!SUMS && splits > 1) ? 1 : 0;
     prm.vec_store = (!SUMS && !swap && !prm.atomic && (Q % 4 == 0) &&
                      (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0) ? 1 : 0;
 
-    // f16 copy of the activations in the workspace, by a pre-pass kernel
-    void* ws = nullptr;
-    cudaError_t e = workspace(dev, static_cast<size_t>(a.M * a.K) * sizeof(__half), &ws);
-    if (e != cudaSuccess) return e;
-    __half* a16 = static_cast<__half*>(ws);
-    CUtensorMap mw, ma;
-    if (!make_i8_map(&mw, a.W, a.N, a.K, swap ? BM : BN) || !make_f16_map(&ma, a16, a.M, a.K, swap ? BN : BM))
-        return cudaErrorInvalidValue;
-    const int64_t n16 = a.M * a.K / 16;
-    e = launch_pdl(i8_to_f16_kernel, dim3(static_cast<unsigned>((n16 + 255) / 256)), dim3(256), 0, stream, a.A, a16,
-                   n16);
-    if (e != cudaSuccess) return e;
+    CUtensorMap mx, my;
+    const int8_t* X = swap ? a.W : a.A;
+    const int8_t* Y = swap ? a.A : a.W;
+    if (!make_i8_map(&mx, X, P, a.K, BM) || !make_i8_map(&my, Y, Q, a.K, BN)) return cudaErrorInvalidValue;
+    cudaError_t e = cudaSuccess;
     if (prm.atomic) {
         e = cudaMemsetAsync(a.C, 0, static_cast<size_t>(a.M * a.N) * sizeof(float), stream);
         if (e != cudaSuccess) return e;
     }
-    if (!swap) return launch_cfg<128, 2, 8, 8, 4, 1, false, SUMS>(mw, ma, prm, grid, stream);
-    if (BN == 16) return launch_cfg<16, 4, 8, 8, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
-    if (BN == 32) return launch_cfg<32, 4, 8, 8, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
-    return launch_cfg<64, 4, 8, 8, 4, 1, true, SUMS>(mw, ma, prm, grid, stream);
+    if (!swap) return launch_cfg<128, 2, 8, 8, 2, 1, SUMS>(mx, my, prm, grid, stream);
+    if (BN == 16) return launch_cfg<16, 4, 8, 10, 3, 1, SUMS>(mx, my, prm, grid, stream);
+    if (BN == 32) return launch_cfg<32, 4, 8, 10, 3, 1, SUMS>(mx, my, prm, grid, stream);
+    return launch_cfg<64, 4, 8, 8, 3, 1, SUMS>(mx, my, prm, grid, stream);
 }
 
 }  // namespace
