@@ -69,7 +69,8 @@ def source_digest(files) -> str:
 
 KERNEL_SOURCES = {
     "qdot_simt": ["gemm_q8_qdot_gb300/csrc/qdot_simt.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
-    "qdot_tc": ["gemm_q8_qdot_gb300/csrc/qdot_tc.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
+    "qdot_tc": ["gemm_q8_qdot_gb300/csrc/qdot_tc.cu", "gemm_q8_qdot_gb300/csrc/tc_ptx.cuh",
+                "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
     "quantize": ["gemm_q8_qdot_gb300/csrc/quantize.cu"],
 }
 
