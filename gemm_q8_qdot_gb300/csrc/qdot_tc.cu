@@ -41,6 +41,7 @@
 // bounded waits, TMEM is freed and the kernel returns.  The host reads the
 // status with pq_check_device.  No trap, no unbounded spin.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -59,9 +60,9 @@ __device__ unsigned g_pq_status;
 namespace {
 
 constexpr int BM = 128;      // rows of the MMA's A operand per tile (MMA M, TMEM lanes)
-constexpr int KS = 64;       // K elements per pipeline stage (two Q8_0 blocks)
+constexpr int KS = 64;       // K elements per f16 stage (two Q8_0 blocks)
+constexpr int KS8 = 128;     // K elements per int8 stage (one scale group): 128-byte TMA rows
 constexpr int GROUP = 4;     // Q8_0 blocks per scale group (128 K, two stages)
-constexpr int SSLOTS = 4;    // scale ring slots (groups prefetched SSLOTS - 1 ahead)
 
 struct TcParams {
     const float* xs;          // scale of MMA-A row p, block b: xs[p * xs_r + b * xs_b]
@@ -79,37 +80,50 @@ struct TcParams {
     int units;                // tiles_p * tiles_q * splits work units, taken round-robin by the CTAs
     int atomic;               // split-K: red.add into a zeroed C
     int vec_store;            // ldq == 1, Q % 4 == 0, C 16-byte aligned: float4 stores
+    int has_scales;           // 0 in block-sum mode (no scale planes)
+    int xs_sr, xs_sb;         // scale tile in shared memory: xs(row, blk) at row * xs_sr + blk * xs_sb
+    int ys_sr, ys_sb;
     int inject_skip_stage;    // test hook: the producer skips this stage (-1: off)
     unsigned long long timeout_cycles;
 };
 
 // MMA-A ("X", 128 rows per tile) and MMA-B ("Y", BN rows) both arrive as int8
 // by TMA into the int8 ring and are converted to f16 by the converter warps.
+// The f32 scales of the stage's 4 blocks arrive by TMA with the int8 tiles;
+// the converters turn them into the scale-product MMA's operands (exact 3-way
+// bf16 splits) in the f16 stage.
 template <int BN, int NCONV, int NEPI, int S8, int S16>
 struct Cfg {
     static constexpr int kThreads = 32 * (2 + NCONV + NEPI);
     static constexpr int kE0 = 2 + NCONV;                 // first epilogue warp
-    static constexpr int kNbuf = (512 / BN) < 4 ? (512 / BN) : 4;
-    static constexpr int kTmemCols = (kNbuf * BN <= 32) ? 32 : (kNbuf * BN <= 64) ? 64 : (kNbuf * BN <= 128) ? 128
-                                     : (kNbuf * BN <= 256) ? 256 : 512;
+    static constexpr int kNbuf = (256 / BN) < 4 ? (256 / BN) : 4;  // TMEM buffers of S and P
+    static constexpr int kTmemCols = (2 * kNbuf * BN <= 32) ? 32 : (2 * kNbuf * BN <= 64) ? 64
+                                     : (2 * kNbuf * BN <= 128) ? 128 : (2 * kNbuf * BN <= 256) ? 256 : 512;
     static constexpr int kCW = BN / (NEPI / 4);          // columns per epilogue warp
     static constexpr int kCH = kCW < 16 ? kCW : 16;       // columns per tcgen05.ld
-    static constexpr int kX8 = BM * KS;                   // int8 X tile bytes
-    static constexpr int kY8 = BN * KS;
+    static constexpr int kX8 = BM * KS8;                  // int8 X tile bytes (one TMA box)
+    static constexpr int kY8 = BN * KS8;
+    static constexpr int kXS = BM * GROUP * 4;            // f32 scales of the stage's 4 blocks
+    static constexpr int kYS = BN * GROUP * 4;
     static constexpr int kX16 = BM * KS * 2;              // f16 X tile bytes
     static constexpr int kY16 = BN * KS * 2;
+    static constexpr int kXP = BM * 32;                   // scale-product operand, one block: [rows][16] bf16
+    static constexpr int kYP = BN * 32;
     static constexpr int kOffX8 = 0;
     static constexpr int kOffY8 = kOffX8 + S8 * kX8;
     static constexpr int kOffX16 = kOffY8 + S8 * kY8;
     static constexpr int kOffY16 = kOffX16 + S16 * kX16;
-    static constexpr int kSlot = GROUP * (BM + BN);        // floats per scale slot: xs [4][128], ys [4][BN]
-    static constexpr int kOffYs = kOffY16 + S16 * kY16;   // SSLOTS x scale slot
-    static constexpr int kOffBar = kOffYs + SSLOTS * kSlot * 4;
+    static constexpr int kOffXP = kOffY16 + S16 * kY16;   // S16 x 2 blocks
+    static constexpr int kOffYP = kOffXP + S16 * 2 * kXP;
+    static constexpr int kOffXS = kOffYP + S16 * 2 * kYP;  // S8 x scale tiles, with the int8 stages
+    static constexpr int kOffYS = kOffXS + S8 * kXS;
+    static constexpr int kOffBar = kOffYS + S8 * kYS;
     static constexpr int kNumBars = 2 * S8 + 2 * S16 + 2 * kNbuf + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;    // + alignment slack
-    static constexpr int kOct = (BM + BN) / 8;            // row octets converted per stage
+    static constexpr int kOct = (BM + BN) / 8;            // row octets converted per f16 stage
     static constexpr int kOctPerWarp = (kOct + NCONV - 1) / NCONV;
+    static constexpr int kSplitPerThread = ((BM + BN) * 2 + NCONV * 32 - 1) / (NCONV * 32);
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
     static_assert(NEPI == 8, "epilogue warps: two column halves over the four TMEM lane quadrants");
     static_assert(kCW % kCH == 0 && kCH % 8 == 0, "epilogue column chunks");
@@ -167,9 +181,22 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
+// Exact split of an f32 into three bf16 whose sum is the value (normal range).
+__device__ __forceinline__ void split3_bf16(float x, uint32_t& h, uint32_t& m, uint32_t& l) {
+    const __nv_bfloat16 bh = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(bh);
+    const __nv_bfloat16 bm = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(bm);
+    const __nv_bfloat16 bl = __float2bfloat16_rn(r2);
+    h = __bfloat16_as_ushort(bh);
+    m = __bfloat16_as_ushort(bm);
+    l = __bfloat16_as_ushort(bl);
+}
+
 template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS>
 __global__ void __launch_bounds__(Cfg<BN, NCONV, NEPI, S8, S16>::kThreads, MINB)
 qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+               const __grid_constant__ CUtensorMap tmXS, const __grid_constant__ CUtensorMap tmYS,
                const TcParams prm) {
     using CF = Cfg<BN, NCONV, NEPI, S8, S16>;
     extern __shared__ uint8_t smem_raw[];
@@ -185,7 +212,6 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + CF::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + CF::kOffMisc + 4);
     const uint32_t sbase = tc::smem_u32(smem);  // the same bytes in the shared window
-    const uint32_t ys_sa = sbase + CF::kOffYs;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -229,6 +255,10 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         tc::fence_mbar_init();
         tc::tma_prefetch_map(&tmX);
         tc::tma_prefetch_map(&tmY);
+        if (prm.has_scales) {
+            tc::tma_prefetch_map(&tmXS);
+            tc::tma_prefetch_map(&tmYS);
+        }
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, CF::kTmemCols);
@@ -242,21 +272,35 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     pdl_wait();
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ producer
+        // One int8 stage = one scale group = 128 K = two f16 stages: the int8
+        // tiles of X and Y and their f32 scales, four TMA boxes on one barrier.
         if (lane == 0) {
+            const uint32_t tx = CF::kX8 + CF::kY8 + (prm.has_scales ? CF::kXS + CF::kYS : 0);
             int issued8 = 0;
-            int gi = 0;  // stage counter over all units of this CTA
+            int gi = 0;  // int8-stage counter over all units of this CTA
             for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
                 const Unit un = unit(u);
-                for (int i = 0; i < un.nst; ++i, ++gi) {
+                const int n8 = un.nst / 2;
+                for (int i = 0; i < n8; ++i, ++gi) {
                     const int s8 = gi % S8;
-                    const int kx = (2 * un.g_begin + i) * KS;
+                    const int g = un.g_begin + i;  // scale group = int8 stage along K
                     if (!bounded_wait(&empty8[s8], ((gi / S8) & 1) ^ 1, abort_flag, limit)) continue;
                     issued8 = gi + 1;
                     if (gi == prm.inject_skip_stage) continue;  // test hook: never arrives
-                    tc::mbar_arrive_expect_tx(&full8[s8], CF::kX8 + CF::kY8);
-                    tc::tma_load_2d(smem + CF::kOffX8 + s8 * CF::kX8, &tmX, &full8[s8], kx, static_cast<int>(un.p0));
-                    tc::tma_load_2d(smem + CF::kOffY8 + s8 * CF::kY8, &tmY, &full8[s8], kx, static_cast<int>(un.q0));
+                    tc::mbar_arrive_expect_tx(&full8[s8], tx);
+                    tc::tma_load_2d(smem + CF::kOffX8 + s8 * CF::kX8, &tmX, &full8[s8], g * KS8, static_cast<int>(un.p0));
+                    tc::tma_load_2d(smem + CF::kOffY8 + s8 * CF::kY8, &tmY, &full8[s8], g * KS8, static_cast<int>(un.q0));
+                    if (prm.has_scales) {
+                        // row-major planes: box {4 blocks, rows}; block-major: box {rows, 4 blocks}
+                        const int b0 = g * GROUP;
+                        tc::tma_load_2d(smem + CF::kOffXS + s8 * CF::kXS, &tmXS, &full8[s8],
+                                        prm.xs_sb == 1 ? b0 : static_cast<int>(un.p0),
+                                        prm.xs_sb == 1 ? static_cast<int>(un.p0) : b0);
+                        tc::tma_load_2d(smem + CF::kOffYS + s8 * CF::kYS, &tmYS, &full8[s8],
+                                        prm.ys_sb == 1 ? b0 : static_cast<int>(un.q0),
+                                        prm.ys_sb == 1 ? static_cast<int>(un.q0) : b0);
+                    }
                 }
             }
             // copies in flight land before the CTA may exit
@@ -267,6 +311,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_f16_f32(BM, BN);
+            constexpr uint32_t idesc_p = tc::idesc_bf16_f32(BM, BN);
             int g = 0, gi = 0;
             for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
                 const int nst = unit(u).nst;
@@ -282,13 +327,18 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         if (!ok || !bounded_wait(&tempty[buf], ((g / CF::kNbuf) & 1) ^ 1, abort_flag, limit))
                             continue;
                         tc::tc_fence_after_sync();
-                        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+                        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * 2 * BN);
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint32_t koff = static_cast<uint32_t>((bb * 2 + kk) * 32);  // 16 f16 = 32 B
                             tc::umma_f16(d, tc::sw128_kmajor_desc(xa + koff), tc::sw128_kmajor_desc(ya + koff),
                                          idesc, kk);
                         }
+                        // P = (split xs) . (split ys)^T: the scale products of this block
+                        const uint32_t xp = sbase + CF::kOffXP + (s * 2 + bb) * CF::kXP;
+                        const uint32_t yp = sbase + CF::kOffYP + (s * 2 + bb) * CF::kYP;
+                        tc::umma_f16(d + BN, tc::noswz_kmajor_desc(xp, 128, 256), tc::noswz_kmajor_desc(yp, 128, 256),
+                                     idesc_p, 0);
                         tc::umma_commit(&tfull[buf]);
                     }
                     // release the f16 stage once its MMAs completed
@@ -300,59 +350,99 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         }
     } else if (warp < CF::kE0) {
         // ------------------------------------------------------------ converters
+        // each int8 stage (128 K) becomes two f16 stages (64 K each)
         const int cw = warp - 2;
-        const int r_in = lane & 7;  // row within an octet
-        const int c8 = lane >> 3;   // 16-byte chunk of a 64-byte int8 row
-        int gi = 0;
+        const int ct = cw * 32 + lane;  // 0 .. 32 * NCONV - 1
+        const int r_in = lane & 7;      // row within an octet
+        const int c4 = lane >> 3;       // 16-byte chunk within this half's 64 bytes of an int8 row
+        int g8 = 0, g16 = 0;
         for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
-            const int nst = unit(u).nst;
-            for (int i = 0; i < nst; ++i, ++gi) {
-                const int s8 = gi % S8, s16 = gi % S16;
-                int ok = 0;
-                if (lane == 0)
-                    ok = bounded_wait(&full8[s8], (gi / S8) & 1, abort_flag, limit) &&
-                         bounded_wait(&empty16[s16], ((gi / S16) & 1) ^ 1, abort_flag, limit);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (ok) {
-                    const uint32_t x8 = sbase + CF::kOffX8 + s8 * CF::kX8;
-                    const uint32_t y8 = sbase + CF::kOffY8 + s8 * CF::kY8;
-                    const uint32_t x16 = sbase + CF::kOffX16 + s16 * CF::kX16;
-                    const uint32_t y16 = sbase + CF::kOffY16 + s16 * CF::kY16;
-                    uint4 v[CF::kOctPerWarp];
+            const int n8 = unit(u).nst / 2;
+            for (int i = 0; i < n8; ++i, ++g8) {
+                const int s8 = g8 % S8;
+                int ok8 = 0;
+                if (lane == 0) ok8 = bounded_wait(&full8[s8], (g8 / S8) & 1, abort_flag, limit);
+                ok8 = __shfl_sync(0xffffffffu, ok8, 0);
+                const uint32_t x8 = sbase + CF::kOffX8 + s8 * CF::kX8;
+                const uint32_t y8 = sbase + CF::kOffY8 + s8 * CF::kY8;
+                const uint32_t xs8 = sbase + CF::kOffXS + s8 * CF::kXS;
+                const uint32_t ys8 = sbase + CF::kOffYS + s8 * CF::kYS;
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h, ++g16) {
+                    const int s16 = g16 % S16;
+                    int ok = 0;
+                    if (lane == 0)
+                        ok = ok8 && bounded_wait(&empty16[s16], ((g16 / S16) & 1) ^ 1, abort_flag, limit);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (ok) {
+                        const uint32_t x16 = sbase + CF::kOffX16 + s16 * CF::kX16;
+                        const uint32_t y16 = sbase + CF::kOffY16 + s16 * CF::kY16;
+                        const int c8 = h * 4 + c4;  // 16-byte chunk of the 128-byte int8 row
+                        uint4 v[CF::kOctPerWarp];
 #pragma unroll
-                    for (int t = 0; t < CF::kOctPerWarp; ++t) {  // all loads first
-                        const int o = cw + t * NCONV;
-                        if (o < CF::kOct) {
-                            const bool isx = o < BM / 8;
-                            const int row = (isx ? o : o - BM / 8) * 8 + r_in;
-                            v[t] = tc::lds128((isx ? x8 : y8) + row * KS + ((c8 ^ ((row >> 1) & 3)) << 4));
+                        for (int t = 0; t < CF::kOctPerWarp; ++t) {  // all loads first
+                            const int o = cw + t * NCONV;
+                            if (o < CF::kOct) {
+                                const bool isx = o < BM / 8;
+                                const int row = (isx ? o : o - BM / 8) * 8 + r_in;
+                                v[t] = tc::lds128((isx ? x8 : y8) + row * KS8 + ((c8 ^ (row & 7)) << 4));
+                            }
                         }
-                    }
 #pragma unroll
-                    for (int t = 0; t < CF::kOctPerWarp; ++t) {
-                        const int o = cw + t * NCONV;
-                        if (o < CF::kOct) {
-                            const bool isx = o < BM / 8;
-                            const int row = (isx ? o : o - BM / 8) * 8 + r_in;
-                            uint4 o0, o1;
-                            i8x4_to_f16x4(v[t].x, o0.x, o0.y);
-                            i8x4_to_f16x4(v[t].y, o0.z, o0.w);
-                            i8x4_to_f16x4(v[t].z, o1.x, o1.y);
-                            i8x4_to_f16x4(v[t].w, o1.z, o1.w);
-                            const uint32_t dst = (isx ? x16 : y16) + row * (KS * 2);
-                            tc::sts128(dst + (((2 * c8) ^ (row & 7)) << 4), o0);
-                            tc::sts128(dst + (((2 * c8 + 1) ^ (row & 7)) << 4), o1);
+                        for (int t = 0; t < CF::kOctPerWarp; ++t) {
+                            const int o = cw + t * NCONV;
+                            if (o < CF::kOct) {
+                                const bool isx = o < BM / 8;
+                                const int row = (isx ? o : o - BM / 8) * 8 + r_in;
+                                uint4 o0, o1;
+                                i8x4_to_f16x4(v[t].x, o0.x, o0.y);
+                                i8x4_to_f16x4(v[t].y, o0.z, o0.w);
+                                i8x4_to_f16x4(v[t].z, o1.x, o1.y);
+                                i8x4_to_f16x4(v[t].w, o1.z, o1.w);
+                                const uint32_t dst = (isx ? x16 : y16) + row * (KS * 2);
+                                tc::sts128(dst + (((2 * c4) ^ (row & 7)) << 4), o0);
+                                tc::sts128(dst + (((2 * c4 + 1) ^ (row & 7)) << 4), o1);
+                            }
                         }
+                        // scale-product operands of this f16 stage's two blocks: row r, block bb ->
+                        // 16 bf16 [h h h m m m l l l 0..] (X) or [h m l h m l h m l 0..] (Y),
+                        // K-major without swizzle: 8-row x 16-byte core matrices, the two
+                        // K halves 128 B apart, 8-row groups 256 B apart
+#pragma unroll
+                        for (int t = 0; t < CF::kSplitPerThread; ++t) {
+                            const int w = ct + t * NCONV * 32;
+                            if (w < (BM + BN) * 2) {
+                                const int bb = w / (BM + BN);
+                                const int r = w - bb * (BM + BN);
+                                const int blk = h * 2 + bb;  // block within the scale group
+                                const bool isx = r < BM;
+                                const int row = isx ? r : r - BM;
+                                const float sc = tc::lds32f(isx ? xs8 + (row * prm.xs_sr + blk * prm.xs_sb) * 4
+                                                                : ys8 + (row * prm.ys_sr + blk * prm.ys_sb) * 4);
+                                uint32_t sh, sm, sl3;
+                                split3_bf16(sc, sh, sm, sl3);
+                                uint4 k0;
+                                if (isx)
+                                    k0 = make_uint4(sh | (sh << 16), sh | (sm << 16), sm | (sm << 16), sl3 | (sl3 << 16));
+                                else
+                                    k0 = make_uint4(sh | (sm << 16), sl3 | (sh << 16), sm | (sl3 << 16), sh | (sm << 16));
+                                const uint4 k1 = make_uint4(sl3, 0u, 0u, 0u);
+                                const uint32_t base = sbase + (isx ? CF::kOffXP + (s16 * 2 + bb) * CF::kXP
+                                                                   : CF::kOffYP + (s16 * 2 + bb) * CF::kYP);
+                                const uint32_t a0 = base + (row >> 3) * 256 + (row & 7) * 16;
+                                tc::sts128(a0, k0);
+                                tc::sts128(a0 + 128, k1);
+                            }
+                        }
+                        tc::fence_proxy_async_smem();
                     }
-                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    // arrive also after an abort: the producer's drain and every later wait
+                    // then find the barriers in a consistent phase
+                    if (lane == 0) tc::mbar_arrive(&full16[s16]);
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    // arrive also after an abort: the producer's drain and every later
-                    // wait then find the barriers in a consistent phase
-                    tc::mbar_arrive(&empty8[s8]);
-                    tc::mbar_arrive(&full16[s16]);
-                }
+                if (lane == 0) tc::mbar_arrive(&empty8[s8]);
             }
         }
     } else {
@@ -361,7 +451,6 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int e = warp - CF::kE0;
         const int quad = warp & 3;
         const int cb = (e >> 2) * CF::kCW;
-        const int et = e * 32 + lane;  // 0 .. 32 * NEPI - 1
         const int prow = quad * 32 + lane;
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
 
@@ -369,162 +458,83 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 #pragma unroll
         for (int t = 0; t < CF::kCW; ++t) acc[t] = 0.0f;
 
-        // Scale ring: slot = [GROUP][BM] MMA-A row scales, then [GROUP][BN] MMA-B row
-        // scales, filled with cp.async SSLOTS - 1 scale groups ahead of their use.
-        // Epilogue threads of the first column half copy their row's 4 scales;
-        // those of the second half copy one MMA-B row's 4 scales each.
-        auto prefetch = [&](const Unit& un, int G, int slot) {
-            const uint32_t xs_d = ys_sa + slot * CF::kSlot * 4;
-            const uint32_t ys_d = xs_d + GROUP * BM * 4;
-            const int64_t b0 = static_cast<int64_t>(un.g_begin + G) * GROUP;
-            if (e < 4) {
-                const int64_t p = un.p0 + prow;
-#pragma unroll
-                for (int bb = 0; bb < GROUP; ++bb) {
-                    const uint32_t d = xs_d + (bb * BM + prow) * 4;
-                    if (p < prm.P) tc::cp_async_4(d, prm.xs + p * prm.xs_r + (b0 + bb) * prm.xs_b);
-                    else tc::sts32f(d, 0.0f);
-                }
-            } else {
-                const int qi = et - 4 * 32;
-                const int64_t q = un.q0 + qi;
-                if (qi < BN) {
-#pragma unroll
-                    for (int bb = 0; bb < GROUP; ++bb) {
-                        const uint32_t d = ys_d + (bb * BN + qi) * 4;
-                        if (q < prm.Q) tc::cp_async_4(d, prm.ys + q * prm.ys_r + (b0 + bb) * prm.ys_b);
-                        else tc::sts32f(d, 0.0f);
-                    }
-                }
-            }
-        };
-        static_assert(NEPI == 8 || BN <= 0, "scale prefetch assumes two column halves of epilogue warps");
-
-        // cursor over this CTA's (unit, group) sequence, for the prefetch
-        int pu = blockIdx.x, pG = 0;
-        Unit pun = unit(pu < prm.units ? pu : 0);
-        auto advance = [&](int& uu, int& GG, Unit& un) {
-            if (++GG >= un.nst / 2) {
-                uu += gridDim.x;
-                GG = 0;
-                if (uu < prm.units) un = unit(uu);
-            }
-        };
-        int issued = 0;
-        if (!SUMS) {
-            for (int k = 0; k < SSLOTS - 1; ++k) {
-                if (pu < prm.units) {
-                    prefetch(pun, pG, issued % SSLOTS);
-                    advance(pu, pG, pun);
-                }
-                tc::cp_async_commit();
-                ++issued;
-            }
-        }
-
-        int u = blockIdx.x;
-        Unit cu = unit(u < prm.units ? u : 0);
-        int G = 0;
-        int g = 0, gg = 0;  // block and scale-group counters over all units of this CTA
-        while (u < prm.units) {
-            const int ngs = cu.nst / 2;
-            if (!SUMS) {
-                // this group's scales landed (per thread), then visible to all epilogue threads;
-                // the barrier also orders every thread's reads of the slot refilled below
-                tc::cp_async_wait<SSLOTS - 2>();
-                tc::named_bar_sync(1, NEPI * 32);
-                if (pu < prm.units) {
-                    prefetch(pun, pG, issued % SSLOTS);
-                    advance(pu, pG, pun);
-                }
-                tc::cp_async_commit();
-                ++issued;
-            }
-            if (ngs > 0) {
-                const int64_t p = cu.p0 + prow;
-                const bool pv = p < prm.P;
-                const uint32_t slot = ys_sa + (gg % SSLOTS) * CF::kSlot * 4;
-#pragma unroll
-                for (int bb = 0; bb < GROUP; ++bb, ++g) {
-                    const int buf = g % CF::kNbuf;
-                    int ok = 0;
-                    if (lane == 0) ok = bounded_wait(&tfull[buf], (g / CF::kNbuf) & 1, abort_flag, limit);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) continue;
-                    tc::tc_fence_after_sync();
-                    const uint32_t ysb = slot + (GROUP * BM + bb * BN + cb) * 4;
-                    const int64_t b = static_cast<int64_t>(cu.g_begin + G) * GROUP + bb;
-                    const uint32_t tb = t_lane + static_cast<uint32_t>(buf * BN + cb);
-                    uint32_t ra[CF::kCH], rb[CF::kCH];
-                    tc::TmemLd<CF::kCH>::load(tb, ra);
-                    tc::TmemLd<CF::kCH>::wait(ra);
+        int g = 0;  // block counter over all units of this CTA
+        for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
+            const Unit cu = unit(u);
+            const int nblk = cu.nst * 2;
+            const int64_t p = cu.p0 + prow;
+            const bool pv = p < prm.P;
+            for (int k = 0; k < nblk; ++k, ++g) {
+                const int buf = g % CF::kNbuf;
+                int ok = 0;
+                if (lane == 0) ok = bounded_wait(&tfull[buf], (g / CF::kNbuf) & 1, abort_flag, limit);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) continue;
+                tc::tc_fence_after_sync();
+                const uint32_t ts = t_lane + static_cast<uint32_t>(buf * 2 * BN + cb);
+                if constexpr (SUMS) {
+                    const int64_t b = static_cast<int64_t>(cu.g_begin) * GROUP + k;
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) {
-                        uint32_t(&cur)[CF::kCH] = (c & 1) ? rb : ra;
-                        uint32_t(&nxt)[CF::kCH] = (c & 1) ? ra : rb;
-                        if (c + 1 < NCH)
-                            tc::TmemLd<CF::kCH>::load(tb + static_cast<uint32_t>((c + 1) * CF::kCH), nxt);
-                        if constexpr (SUMS) {
-                            if (pv) {
+                        uint32_t sv[CF::kCH];
+                        tc::TmemLd<CF::kCH>::load(ts + c * CF::kCH, sv);
+                        tc::TmemLd<CF::kCH>::wait(sv);
+                        if (pv) {
 #pragma unroll
-                                for (int t = 0; t < CF::kCH; ++t) {
-                                    const int64_t q = cu.q0 + cb + c * CF::kCH + t;
-                                    if (q < prm.Q)
-                                        prm.S[p * prm.sp + q * prm.sq + b] =
-                                            static_cast<int32_t>(__uint_as_float(cur[t]));
-                                }
-                            }
-                        } else {
-                            const float xsb = tc::lds32f(slot + (bb * BM + prow) * 4);
-#pragma unroll
-                            for (int t = 0; t < CF::kCH; t += 4) {
-                                const float4 y4 = tc::lds128f(ysb + (c * CF::kCH + t) * 4);
-                                float* a4 = acc + c * CF::kCH + t;
-                                a4[0] = fmaf(xsb * y4.x, __uint_as_float(cur[t + 0]), a4[0]);
-                                a4[1] = fmaf(xsb * y4.y, __uint_as_float(cur[t + 1]), a4[1]);
-                                a4[2] = fmaf(xsb * y4.z, __uint_as_float(cur[t + 2]), a4[2]);
-                                a4[3] = fmaf(xsb * y4.w, __uint_as_float(cur[t + 3]), a4[3]);
-                            }
-                        }
-                        if (c + 1 < NCH) tc::TmemLd<CF::kCH>::wait(nxt);
-                    }
-                    tc::tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&tempty[buf]);
-                }
-                if (!SUMS && G + 1 == ngs) {
-                    // last group of the unit: write its tile and start the next from zero
-                    if (*abort_flag == 0 && pv) {
-                        if (prm.vec_store) {
-#pragma unroll
-                            for (int t = 0; t < CF::kCW; t += 4) {
-                                const int64_t q = cu.q0 + cb + t;
+                            for (int t = 0; t < CF::kCH; ++t) {
+                                const int64_t q = cu.q0 + cb + c * CF::kCH + t;
                                 if (q < prm.Q)
-                                    *reinterpret_cast<float4*>(prm.C + p * prm.ldp + q) =
-                                        make_float4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int t = 0; t < CF::kCW; ++t) {
-                                const int64_t q = cu.q0 + cb + t;
-                                if (q < prm.Q) {
-                                    float* dst = prm.C + p * prm.ldp + q * prm.ldq;
-                                    if (prm.atomic)
-                                        atomicAdd(dst, acc[t]);
-                                    else
-                                        *dst = acc[t];
-                                }
+                                    prm.S[p * prm.sp + q * prm.sq + b] = static_cast<int32_t>(__uint_as_float(sv[t]));
                             }
                         }
                     }
+                } else {
 #pragma unroll
-                    for (int t = 0; t < CF::kCW; ++t) acc[t] = 0.0f;
+                    for (int c = 0; c < NCH; ++c) {
+                        uint32_t sv[CF::kCH], pvv[CF::kCH];
+                        tc::TmemLd<CF::kCH>::load(ts + c * CF::kCH, sv);
+                        tc::TmemLd<CF::kCH>::load(ts + BN + c * CF::kCH, pvv);
+                        tc::TmemLd<CF::kCH>::wait(sv);
+                        tc::TmemLd<CF::kCH>::wait(pvv);
+#pragma unroll
+                        for (int t = 0; t < CF::kCH; ++t)
+                            acc[c * CF::kCH + t] =
+                                fmaf(__uint_as_float(pvv[t]), __uint_as_float(sv[t]), acc[c * CF::kCH + t]);
+                    }
                 }
+                tc::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&tempty[buf]);
             }
-            ++gg;
-            advance(u, G, cu);
+            if constexpr (!SUMS) {
+                // the unit's last block: write its tile and start the next from zero
+                if (*abort_flag == 0 && pv) {
+                    if (prm.vec_store) {
+#pragma unroll
+                        for (int t = 0; t < CF::kCW; t += 4) {
+                            const int64_t q = cu.q0 + cb + t;
+                            if (q < prm.Q)
+                                *reinterpret_cast<float4*>(prm.C + p * prm.ldp + q) =
+                                    make_float4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < CF::kCW; ++t) {
+                            const int64_t q = cu.q0 + cb + t;
+                            if (q < prm.Q) {
+                                float* dst = prm.C + p * prm.ldp + q * prm.ldq;
+                                if (prm.atomic)
+                                    atomicAdd(dst, acc[t]);
+                                else
+                                    *dst = acc[t];
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < CF::kCW; ++t) acc[t] = 0.0f;
+            }
         }
-        if (!SUMS) tc::cp_async_wait<0>();  // no copy may land after the CTA exits
     }
 
     __syncthreads();
@@ -554,17 +564,34 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// int8 [rows, K] row-major, box {64 bytes of K, box_rows}, 64-byte swizzle,
-// zero fill outside the tensor (ragged rows read as 0).
+// int8 [rows, K] row-major, box {128 bytes of K, box_rows}, 128-byte swizzle,
+// zero fill outside the tensor (ragged rows read as 0).  Boxes of 16 KB and
+// more keep the TMA unit's few outstanding operations per SM busy enough to
+// stream from HBM at full rate.
 bool make_i8_map(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(KS), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(KS8), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// f32 plane [outer, inner] with the given row stride in bytes, box {box_inner,
+// box_outer}, no swizzle, zero fill outside.
+bool make_f32_map(CUtensorMap* map, const float* base, int64_t inner, int64_t outer, int64_t stride_bytes,
+                  int box_inner, int box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -596,14 +623,13 @@ int g_inject_skip_stage = -1;
 unsigned long long g_timeout_cycles = 4000000000ull;  // ~2 s at 2 GHz
 
 template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS>
-cudaError_t launch_cfg(const CUtensorMap& mx, const CUtensorMap& my, const TcParams& prm, int64_t grid,
-                       cudaStream_t stream) {
+cudaError_t launch_cfg(const CUtensorMap* maps, const TcParams& prm, int64_t grid, cudaStream_t stream) {
     using CF = Cfg<BN, NCONV, NEPI, S8, S16>;
     auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SUMS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::kSmem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(CF::kThreads), static_cast<size_t>(CF::kSmem),
-                      stream, mx, my, prm);
+                      stream, maps[0], maps[1], maps[2], maps[3], prm);
 }
 
 template <bool SUMS>
@@ -671,19 +697,45 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
     prm.vec_store = (!SUMS && !swap && !prm.atomic && (Q % 4 == 0) &&
                      (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0) ? 1 : 0;
 
-    CUtensorMap mx, my;
+    CUtensorMap maps[4];
     const int8_t* X = swap ? a.W : a.A;
     const int8_t* Y = swap ? a.A : a.W;
-    if (!make_i8_map(&mx, X, P, a.K, BM) || !make_i8_map(&my, Y, Q, a.K, BN)) return cudaErrorInvalidValue;
+    if (!make_i8_map(&maps[0], X, P, a.K, BM) || !make_i8_map(&maps[1], Y, Q, a.K, BN)) return cudaErrorInvalidValue;
+    prm.has_scales = SUMS ? 0 : 1;
+    if (!SUMS) {
+        // scale planes by TMA: rows of 16-byte multiples from a 16-byte aligned base
+        auto plane = [&](CUtensorMap* m, const float* base, int64_t r_stride, int64_t b_stride, int64_t rows,
+                         int box_rows, int& sr, int& sb) -> cudaError_t {
+            if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0) return cudaErrorNotSupported;
+            if (b_stride == 1) {  // [rows, KB]: box {4 blocks, box_rows} -> smem [row][4]
+                if ((r_stride * 4) % 16 != 0) return cudaErrorNotSupported;
+                sr = GROUP; sb = 1;
+                return make_f32_map(m, base, KB, rows, r_stride * 4, GROUP, box_rows) ? cudaSuccess
+                                                                                     : cudaErrorInvalidValue;
+            }
+            // [KB, rows]: box {box_rows, 4 blocks} -> smem [4][row]
+            if ((b_stride * 4) % 16 != 0) return cudaErrorNotSupported;
+            sr = 1; sb = box_rows;
+            return make_f32_map(m, base, rows, KB, b_stride * 4, box_rows, GROUP) ? cudaSuccess
+                                                                                 : cudaErrorInvalidValue;
+        };
+        cudaError_t e1 = plane(&maps[2], prm.xs, prm.xs_r, prm.xs_b, P, BM, prm.xs_sr, prm.xs_sb);
+        if (e1 != cudaSuccess) return e1;
+        e1 = plane(&maps[3], prm.ys, prm.ys_r, prm.ys_b, Q, BN, prm.ys_sr, prm.ys_sb);
+        if (e1 != cudaSuccess) return e1;
+    } else {
+        maps[2] = maps[0];
+        maps[3] = maps[1];
+    }
     cudaError_t e = cudaSuccess;
     if (prm.atomic) {
         e = cudaMemsetAsync(a.C, 0, static_cast<size_t>(a.M * a.N) * sizeof(float), stream);
         if (e != cudaSuccess) return e;
     }
-    if (!swap) return launch_cfg<128, 2, 8, 8, 2, 1, SUMS>(mx, my, prm, grid, stream);
-    if (BN == 16) return launch_cfg<16, 4, 8, 10, 3, 1, SUMS>(mx, my, prm, grid, stream);
-    if (BN == 32) return launch_cfg<32, 4, 8, 10, 3, 1, SUMS>(mx, my, prm, grid, stream);
-    return launch_cfg<64, 4, 8, 8, 3, 1, SUMS>(mx, my, prm, grid, stream);
+    if (!swap) return launch_cfg<128, 4, 8, 3, 2, 1, SUMS>(maps, prm, grid, stream);
+    if (BN == 16) return launch_cfg<16, 4, 8, 6, 2, 1, SUMS>(maps, prm, grid, stream);
+    if (BN == 32) return launch_cfg<32, 4, 8, 6, 2, 1, SUMS>(maps, prm, grid, stream);
+    return launch_cfg<64, 4, 8, 5, 2, 1, SUMS>(maps, prm, grid, stream);
 }
 
 }  // namespace

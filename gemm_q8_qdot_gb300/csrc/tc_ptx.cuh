@@ -159,6 +159,31 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor for a K-major operand tile without swizzle:
+// 8-row x 16-byte core matrices; `lbo` = bytes between the core matrices of
+// one row group that are adjacent along K, `sbo` = bytes between 8-row groups.
+__device__ __forceinline__ uint64_t noswz_kmajor_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3fffu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3fffu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3fffu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;  // swizzle mode 0: none
+}
+
+// Instruction descriptor, kind::f16 with bf16 A and B (bits 7-9, 10-12 = 1),
+// f32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// cp.async arrive-on: `bar` receives one arrival once every cp.async this
+// thread issued before has completed (no pending-count increment).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Instruction descriptor, kind::f16: f32 accumulator (bits 4-5 = 1), A and B
 // f16 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits
 // 17-22, M >> 4 at bits 24-28.

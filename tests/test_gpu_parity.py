@@ -231,9 +231,33 @@ def test_qdot_tc_small(pq, M, N, K, layout):
     a, a_s, w, w_s = rand_operands(M * 31 + N * 7 + K + layout, M, N, K)
     out, bound = oracle.qdot(a, a_s, w, w_s)
     ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
-    C = pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(ws), ws_layout=layout, path=pq.PATH_TC)
+    if layout == 1 and N % 4 != 0:
+        # the [K/32, N] scale plane is loaded by TMA only when its rows are 16-byte
+        # multiples: the tensor-core path declines, the automatic path falls back
+        with pytest.raises(pq.PQError) as ei:
+            pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(ws), ws_layout=layout, path=pq.PATH_TC)
+        assert ei.value.code == pq.PQ_ERR_UNSUPPORTED
+        C = pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(ws), ws_layout=layout, path=pq.PATH_AUTO)
+    else:
+        C = pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(ws), ws_layout=layout, path=pq.PATH_TC)
     pq.check_device()
     assert_within_bound(C, out, bound, f"tc M={M} N={N} K={K} layout={layout}")
+
+
+def test_qdot_tc_unaligned_scales_fall_back(pq):
+    """Scale planes 4- but not 16-byte aligned: auto path still correct (dp4a kernel)."""
+    M, N, K = 40, 96, 256
+    a, a_s, w, w_s = rand_operands(17, M, N, K)
+    out, bound = oracle.qdot(a, a_s, w, w_s)
+    buf = torch.zeros(a_s.size + 1, dtype=torch.float32, device=DEV)
+    AS = buf[1:].view(M, K // 32)
+    AS.copy_(dev(a_s))
+    with pytest.raises(pq.PQError) as ei:
+        pq.qdot_q8_0_ex(dev(a), AS, dev(w), dev(w_s), path=pq.PATH_TC)
+    assert ei.value.code == pq.PQ_ERR_UNSUPPORTED
+    C = pq.qdot_q8_0(dev(a), AS, dev(w), dev(w_s))
+    pq.check_device()
+    assert_within_bound(C, out, bound, "unaligned scales")
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 16, 128), (20, 70, 256), (64, 128, 128), (100, 140, 256), (128, 256, 512)])
