@@ -72,6 +72,7 @@ KERNEL_SOURCES = {
     "qdot_tc": ["gemm_q8_qdot_gb300/csrc/qdot_tc.cu", "gemm_q8_qdot_gb300/csrc/tc_ptx.cuh",
                 "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
     "quantize": ["gemm_q8_qdot_gb300/csrc/quantize.cu"],
+    "qdot_fused": ["gemm_q8_qdot_gb300/csrc/qdot_simt.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
 }
 
 
@@ -231,12 +232,19 @@ def aggregate(per_rank_units: float, per_rank_seconds: float, world: int, device
 # ----------------------------------------------------------------------------- our arm
 
 class Problem:
-    """Device buffers of one workload: f32 activations, rotating Q8_0 weight copies, outputs."""
+    """Device buffers of one workload: f32 activations, rotating Q8_0 weight copies, outputs.
 
-    def __init__(self, pq, wl: workloads.Workload, device):
+    A step quantizes the activation rows and contracts them with the weights:
+    for M <= 8 through the one-call fused entry point (pq_quantize_qdot_q8_0,
+    which also writes the quantized rows), otherwise pq_quantize_q8_0 then
+    pq_qdot_q8_0; `fused=False` forces the two-call sequence.
+    """
+
+    def __init__(self, pq, wl: workloads.Workload, device, fused: bool = True):
         import torch
         self.wl = wl
         self.pq = pq
+        self.fused = fused and wl.M <= 8
         x = workloads.activations(wl)
         self.x_host = torch.from_numpy(x).pin_memory()
         self.x = self.x_host.to(device)
@@ -254,20 +262,32 @@ class Problem:
         torch.cuda.synchronize()
 
     def step(self, t: int, events=None):
+        c = t % self.copies
+        if self.fused:
+            if events is not None:
+                events[0].record()
+                events[1].record()
+            self.pq.quantize_qdot_q8_0(self.x, self.W[c], self.WS[c], self.C, A=self.A, AS=self.AS)
+            if events is not None:
+                events[2].record()
+            return
         if events is not None:
             events[0].record()
         self.pq.quantize_q8_0(self.x, self.A, self.AS)
         if events is not None:
             events[1].record()
-        self.pq.qdot_q8_0(self.A, self.AS, self.W[t % self.copies], self.WS[t % self.copies], self.C)
+        self.pq.qdot_q8_0(self.A, self.AS, self.W[c], self.WS[c], self.C)
         if events is not None:
             events[2].record()
 
     @property
     def algorithmic_bytes(self) -> int:
-        """Bytes qdot_t must move per launch: W, WS, A, AS read once, C written once."""
+        """Bytes the dominant kernel must move per launch.  qdot_t: W, WS, A, AS read
+        once, C written once; the fused step reads x (f32) instead of A, AS and also
+        writes A, AS."""
         wl = self.wl
-        return wl.weight_bytes + wl.M * wl.K + 4 * wl.M * (wl.K // 32) + 4 * wl.M * wl.N
+        base = wl.weight_bytes + wl.M * wl.K + 4 * wl.M * (wl.K // 32) + 4 * wl.M * wl.N
+        return base + 4 * wl.M * wl.K if self.fused else base
 
 
 def _capture(prob: Problem, first: int, steps: int, stream, events=None, only_qdot=False):
@@ -275,9 +295,11 @@ def _capture(prob: Problem, first: int, steps: int, stream, events=None, only_qd
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for t in range(steps):
-            if only_qdot:
+            if only_qdot and not prob.fused:
                 c = (first + t) % prob.copies
                 prob.pq.qdot_q8_0(prob.A, prob.AS, prob.W[c], prob.WS[c], prob.C)
+            elif only_qdot:
+                prob.step(first + t)
             else:
                 prob.step(first + t, events[t] if events else None)
     return g
@@ -355,7 +377,7 @@ def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str):
     if wl.M <= 64:
         achieved = prob.algorithmic_bytes / (qdot_ms * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])
-        kernel = "qdot_simt" if wl.M <= 8 else "qdot_tc"
+        kernel = ("qdot_fused" if prob.fused else "qdot_simt") if wl.M <= 8 else "qdot_tc"
         traffic = recorded_traffic(kernel, wl.name)
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
@@ -381,11 +403,23 @@ def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sample
         units, unit = wl.ops * steps, "TOPS"
         scale = 1e12
     value, t_max = aggregate(units, per_rank_s, world, device)
+    kernel_ms = {"qdot_graph_only": round(qdot_only_ms, 5)}
+    if prob.fused:
+        kernel_ms["quantize_qdot_fused"] = round(qdot_ms, 5)
+    else:
+        kernel_ms.update({"quantize": round(quant_ms, 5), "qdot": round(qdot_ms, 5)})
     res = {"value": round(value / scale, 3), "unit": unit, "ms_per_step": round(t_max * 1e3 / steps, 5),
-           "kernel_ms": {"quantize": round(quant_ms, 5), "qdot": round(qdot_ms, 5),
-                         "qdot_graph_only": round(qdot_only_ms, 5)},
+           "step": "pq_quantize_qdot_q8_0 (one kernel)" if prob.fused else "pq_quantize_q8_0 + pq_qdot_q8_0",
+           "kernel_ms": kernel_ms,
            "roofline": roofline_for(prob, qdot_ms, peaks, peak_src), "weight_copies": prob.copies,
            "window": window}
+    if prob.fused:
+        # the same step as two calls (quantizer, then qdot_t), for comparison
+        two = Problem(pq, wl, device, fused=False)
+        ms2, _, q2, _, _ = time_graph(two, steps, warmup, world)
+        res["two_call"] = {"ms_per_step": round(ms2 / steps, 5), "qdot_ms": round(q2, 5),
+                           "value": round(units / (ms2 * 1e-3) / scale, 3)}
+        del two
     if e2e:
         dt, h2d, d2h = time_e2e(prob, steps, warmup)
         ev, _ = aggregate(units, dt, world, device)
@@ -494,7 +528,7 @@ def main(argv=None):
                 others[name] = r
             except pq.PQError as e:
                 others[name] = {"error": str(e)}
-    launches_per_step = 2
+    launches_per_step = 1 if workloads.WORKLOADS[args.workload].M <= 8 else 2
     line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
@@ -505,6 +539,7 @@ def main(argv=None):
                        "l2": f"{head['weight_copies']} rotating weight copies (>= 2x L2 = {2 * L2_BYTES >> 20} MiB)",
                        "timing": "K steps in one CUDA graph, events on the launching stream"},
             "roofline": head["roofline"], "kernel_ms": head["kernel_ms"], "e2e": head["e2e"],
+            "step": head["step"], "two_call": head.get("two_call"),
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
     if others:
         line["other_workloads"] = others

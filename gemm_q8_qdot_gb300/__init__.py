@@ -7,9 +7,9 @@ seeded workload generators.
 from .binding import (EXPORTS, PATH_AUTO, PATH_SIMT, PATH_TC, PQ_ERR_ALIGN, PQ_ERR_CUDA,
                       PQ_ERR_INVALID_ARG, PQ_ERR_SHAPE, PQ_ERR_TIMEOUT, PQ_ERR_UNSUPPORTED, PQ_OK,
                       WS_KB_N, WS_N_KB, PQError, check_device, lib_path, load, qdot_q8_0,
-                      qdot_q8_0_blocksums, qdot_q8_0_ex, quantize_q8_0, strerror)
+                      qdot_q8_0_blocksums, qdot_q8_0_ex, quantize_q8_0, quantize_qdot_q8_0, strerror)
 
 __all__ = ["EXPORTS", "PATH_AUTO", "PATH_SIMT", "PATH_TC", "WS_N_KB", "WS_KB_N", "PQError",
            "PQ_OK", "PQ_ERR_INVALID_ARG", "PQ_ERR_SHAPE", "PQ_ERR_ALIGN", "PQ_ERR_CUDA",
            "PQ_ERR_TIMEOUT", "PQ_ERR_UNSUPPORTED", "load", "lib_path", "quantize_q8_0",
-           "qdot_q8_0", "qdot_q8_0_ex", "qdot_q8_0_blocksums", "check_device", "strerror"]
+           "qdot_q8_0", "qdot_q8_0_ex", "quantize_qdot_q8_0", "qdot_q8_0_blocksums", "check_device", "strerror"]

@@ -25,8 +25,8 @@ PQ_ERR_UNSUPPORTED = -6
 PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
 WS_N_KB, WS_KB_N = 0, 1
 
-EXPORTS = ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_qdot_q8_0_blocksums",
-           "pq_check_device", "pq_strerror", "pq_version")
+EXPORTS = ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
+           "pq_qdot_q8_0_blocksums", "pq_check_device", "pq_strerror", "pq_version")
 
 _lib: ctypes.CDLL | None = None
 
@@ -54,13 +54,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pq_quantize_q8_0.argtypes = [vp, vp, vp, i64, i64, vp]
     lib.pq_qdot_q8_0.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp]
     lib.pq_qdot_q8_0_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp]
+    lib.pq_quantize_qdot_q8_0.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_qdot_q8_0_blocksums.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_check_device.argtypes = [vp]
     lib.pq_strerror.argtypes = [i32]
     lib.pq_strerror.restype = ctypes.c_char_p
     lib.pq_version.argtypes = []
-    for fn in ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_qdot_q8_0_blocksums",
-               "pq_check_device", "pq_version"):
+    for fn in ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
+               "pq_qdot_q8_0_blocksums", "pq_check_device", "pq_version"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -130,6 +131,20 @@ def qdot_q8_0_ex(A, AS, W, WS, C=None, ws_layout: int = WS_N_KB, path: int = PAT
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     _check(load().pq_qdot_q8_0_ex(_ptr(A), _ptr(AS), _ptr(W), _ptr(WS), _ptr(C), M, N, K,
                                   int(ws_layout), int(path), _stream(stream)), "pq_qdot_q8_0_ex")
+    return C
+
+
+def quantize_qdot_q8_0(x, W, WS, C=None, A=None, AS=None, ws_layout: int = WS_N_KB, stream=None):
+    """One decode step via pq_quantize_qdot_q8_0: C = qdot_t(quantize(x), W); A/AS optionally
+    receive the quantized rows (required for M > 8)."""
+    if x.dtype != torch.float32:
+        raise TypeError("x must be float32")
+    M, K = x.shape
+    N = W.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(load().pq_quantize_qdot_q8_0(_ptr(x), _ptr(A), _ptr(AS), _ptr(W), _ptr(WS), _ptr(C), M, N, K,
+                                        int(ws_layout), _stream(stream)), "pq_quantize_qdot_q8_0")
     return C
 
 

@@ -5,11 +5,47 @@
 // entry on a bad extent, which leaves the CUDA context unusable ("Kernel ABI",
 // section "Entry checks"); a shared GPU must never see that.
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime_api.h>
 
 #include "pq.h"
 #include "pq_debug.h"
 #include "pq_internal.h"
+
+namespace pq {
+
+// Per-device workspace for the quantized rows of pq_quantize_qdot_q8_0 calls
+// that do not pass A / AS: allocated on the first such call on a device,
+// grown (cudaFree + cudaMalloc) when a larger one arrives, kept until exit.
+cudaError_t device_workspace(size_t bytes, void** out) {
+    static std::mutex mu;
+    static void* ptr[64] = {};
+    static size_t have[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (have[dev] < bytes) {
+        if (ptr[dev]) {
+            e = cudaFree(ptr[dev]);  // synchronizes the device: no earlier call still uses it
+            if (e != cudaSuccess) return e;
+            ptr[dev] = nullptr;
+            have[dev] = 0;
+        }
+        const size_t want = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
+        e = cudaMalloc(&ptr[dev], want);
+        if (e != cudaSuccess) {
+            ptr[dev] = nullptr;
+            return e;
+        }
+        have[dev] = want;
+    }
+    *out = ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace pq
 
 namespace {
 
@@ -86,6 +122,35 @@ int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const flo
     return qdot_impl(A, AS, W, WS, C, nullptr, M, N, K, ws_layout, path, stream);
 }
 
+int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W, const float* WS, float* C,
+                          int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream) {
+    if (ws_layout != PQ_WS_N_KB && ws_layout != PQ_WS_KB_N) return PQ_ERR_INVALID_ARG;
+    int st = check_qdot_shape(M, N, K);
+    if (st != PQ_OK) return st;
+    if (M == 0 || N == 0) return PQ_OK;
+    if (!x || !W || !WS || !C) return PQ_ERR_INVALID_ARG;
+    if ((A == nullptr) != (AS == nullptr)) return PQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(W, 16) || !aligned(WS, 4) || !aligned(C, 4)) return PQ_ERR_ALIGN;
+    if (A && (!aligned(A, 16) || !aligned(AS, 4))) return PQ_ERR_ALIGN;
+    // one kernel for a single row whose grid fits one wave
+    pq::FusedArgs f{x, A, AS, W, WS, C, M, N, K, ws_layout};
+    cudaError_t e = pq::launch_qdot_fused(f, stream);
+    if (e != cudaErrorNotSupported) return map_cuda(e);
+    // otherwise the quantizer, then qdot_t (the second launch overlaps the first);
+    // the quantized rows go to A / AS, or to this device's workspace
+    if (!A) {
+        void* ws = nullptr;
+        const size_t qbytes = (static_cast<size_t>(M * K) + 255) & ~size_t(255);
+        e = pq::device_workspace(qbytes + static_cast<size_t>(M * (K / 32)) * sizeof(float), &ws);
+        if (e != cudaSuccess) return map_cuda(e);
+        A = static_cast<int8_t*>(ws);
+        AS = reinterpret_cast<float*>(static_cast<char*>(ws) + qbytes);
+    }
+    st = pq_quantize_q8_0(x, A, AS, M, K, stream);
+    if (st != PQ_OK) return st;
+    return qdot_impl(A, AS, W, WS, C, nullptr, M, N, K, ws_layout, PQ_PATH_AUTO, stream);
+}
+
 int pq_qdot_q8_0_blocksums(const int8_t* A, const int8_t* W, int32_t* S, int64_t M, int64_t N,
                            int64_t K, int path, cudaStream_t stream) {
     int st = check_qdot_shape(M, N, K);
@@ -116,7 +181,7 @@ const char* pq_strerror(int code) {
     }
 }
 
-int pq_version(void) { return 100; }
+int pq_version(void) { return 101; }
 
 int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles) {
     if (skip_stage < -1) return PQ_ERR_INVALID_ARG;

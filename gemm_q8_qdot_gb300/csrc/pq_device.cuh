@@ -96,6 +96,44 @@ __device__ __forceinline__ int block_dot(const u32x8& a, const u32x8& w) {
     return s;
 }
 
+// ---------------------------------------------------------------- Q8_0 quantizer
+// Per block of 32: amax = max |x|, d = amax / 127 (IEEE division), q =
+// round(x / d) with ties to even, clamped to [-127, 127]; d == 0 gives q = 0.
+// Four consecutive lanes share a block, 8 floats each.
+
+__device__ __forceinline__ uint32_t q8_byte(float v, float d) {
+    if (d == 0.0f) return 0u;
+    int r = __float2int_rn(__fdiv_rn(v, d));  // IEEE x/d, round to nearest even
+    r = max(-127, min(127, r));
+    return static_cast<uint32_t>(r) & 0xffu;
+}
+
+// The block's scale: a width-4 xor butterfly of max over the 4 lanes.  Every
+// lane of the warp must call it (full-mask shuffles).
+__device__ __forceinline__ float q8_block_scale(const float4& v0, const float4& v1) {
+    float amax = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                       fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    return __fdiv_rn(amax, 127.0f);
+}
+
+// This lane's 8 quantized bytes, little-endian in two words.
+__device__ __forceinline__ uint2 q8_pack8(const float4& v0, const float4& v1, float d) {
+    uint2 r;
+    r.x = q8_byte(v0.x, d) | (q8_byte(v0.y, d) << 8) | (q8_byte(v0.z, d) << 16) | (q8_byte(v0.w, d) << 24);
+    r.y = q8_byte(v1.x, d) | (q8_byte(v1.y, d) << 8) | (q8_byte(v1.z, d) << 16) | (q8_byte(v1.w, d) << 24);
+    return r;
+}
+
+// x may be written by the preceding kernel: coherent, kept after pdl_wait.
+__device__ __forceinline__ float4 ld_stream_f4(const float* p) {
+    float4 r;
+    asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(p) : "memory");
+    return r;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);

@@ -17,6 +17,17 @@ struct QdotArgs {
     int ws_layout;   // 0: WS [N, K/32]; 1: WS [K/32, N]
 };
 
+struct FusedArgs {
+    const float* x;  // f32 [M, K] activations
+    int8_t* A;       // optional int8 [M, K] output of the quantizer (with AS), or null
+    float* AS;
+    const int8_t* W;
+    const float* WS;
+    float* C;
+    int64_t M, N, K;
+    int ws_layout;
+};
+
 // Launches `kernel` with programmatic stream serialization allowed: it may be
 // scheduled while the previous kernel on the stream is still running, and
 // orders itself with griddepcontrol.wait (pdl_wait) before touching data that
@@ -44,8 +55,17 @@ cudaError_t launch_quantize(const float* x, int8_t* q, float* s, int64_t rows, i
 // grid would exceed the device limits.
 cudaError_t launch_qdot_simt(const QdotArgs& a, cudaStream_t stream);
 
+// Fused quantize + dp4a contraction for one activation row (cudaErrorNotSupported
+// for M != 1, when the grid would need more than one wave, or when the
+// quantized row does not fit a CTA's shared memory).
+cudaError_t launch_qdot_fused(const FusedArgs& a, cudaStream_t stream);
+
 // tcgen05 tensor-core kernel.  cudaErrorNotSupported if the device is not sm_103.
 cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream);
+
+// The current device's workspace of at least `bytes` (allocated on first use,
+// grown on demand, never freed before exit).
+cudaError_t device_workspace(size_t bytes, void** out);
 
 // Reads and clears the device status word (set by a bounded wait that gave up).
 cudaError_t read_and_clear_status(unsigned* status);

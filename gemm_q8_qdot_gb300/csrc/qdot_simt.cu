@@ -38,6 +38,10 @@ namespace pq {
 namespace {
 
 constexpr int kWarps = 8;
+#ifndef PQ_FUSED_WARPS
+#define PQ_FUSED_WARPS 32
+#endif
+constexpr int kFusedWarps = PQ_FUSED_WARPS;  // warps (= output columns) per CTA of the fused step
 
 template <int MR, int COLS, int U, bool V8, bool SUMS, int WSL>
 __global__ void __launch_bounds__(kWarps * 32)
@@ -164,7 +168,142 @@ cudaError_t launch_by_m(const QdotArgs& a, bool v8, cudaStream_t stream) {
     return launch_tile<4, 2, 2, SUMS, WSL>(a, v8, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Fused decode step: quantize the activation rows x [M, K] (M <= MR) into this
+// CTA's shared memory with the quantizer's exact arithmetic, then contract
+// them with W like qdot_simt_kernel (one output column per warp).  One launch
+// per step instead of two: before griddepcontrol.wait the CTA asks L2 to
+// prefetch its weight rows; after it, each warp issues its first round of
+// weight loads, then the CTA quantizes x (from L2) while they are in flight.
+// CTA 0 also writes the quantized rows to A / AS when they are requested.
+template <int MR, int U, bool V8, int WSL, int NW>
+__global__ void __launch_bounds__(NW * 32)
+qdot_fused_kernel(FusedArgs p) {
+    extern __shared__ __align__(16) uint8_t fsm[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t N = p.N, M = p.M, K = p.K, KB = K >> 5;
+    int8_t* a_s = reinterpret_cast<int8_t*>(fsm);                    // [MR][K]
+    float* as_s = reinterpret_cast<float*>(fsm + MR * K);             // [MR][KB]
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * NW + warp;
+    const bool jv = j < N;
+    const int8_t* wrow = p.W + (jv ? j : 0) * K;
+
+    pdl_trigger();
+    if (lane == 0 && jv) {
+        prefetch_l2(wrow, static_cast<uint32_t>(K < (int64_t(1) << 30) ? K : (int64_t(1) << 30)));
+        if (WSL == 0 && (KB * 4) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.WS + j * KB) & 15) == 0)
+            prefetch_l2(p.WS + j * KB, static_cast<uint32_t>(KB * 4));
+    }
+    pdl_wait();
+
+    // weights of round `bb`: U blocks per lane
+    u32x8 wv[U];
+    float wsv[U];
+    auto load_round = [&](int64_t bb) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t b = bb + u * 32 + lane;
+            if (jv && b < KB) {
+                wv[u] = ld_block<V8, true>(wrow + b * 32);
+                wsv[u] = ld_f32(WSL == 0 ? p.WS + j * KB + b : p.WS + b * N + j);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) wv[u].v[t] = 0u;
+                wsv[u] = 0.0f;
+            }
+        }
+    };
+    load_round(0);
+
+    // quantize x while the first weight round is in flight: 4 lanes per Q8_0
+    // block, 8 blocks per warp per CTA round (warp-uniform loop for the shuffles)
+    const int64_t nq = M * KB;
+    const bool writer = blockIdx.x == 0 && p.A != nullptr;
+    for (int64_t base = 0; base < nq; base += NW * 8) {
+        const int64_t g = base + (threadIdx.x >> 2);
+        const int sub = threadIdx.x & 3;
+        const bool live = g < nq;
+        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+        if (live) {
+            const float* px = p.x + g * 32 + sub * 8;
+            v0 = ld_stream_f4(px);
+            v1 = ld_stream_f4(px + 4);
+        }
+        const float d = q8_block_scale(v0, v1);
+        if (live) {
+            const uint2 q = q8_pack8(v0, v1, d);
+            *reinterpret_cast<uint2*>(a_s + g * 32 + sub * 8) = q;
+            if (sub == 0) as_s[g] = d;
+            if (writer) {
+                *reinterpret_cast<uint2*>(p.A + g * 32 + sub * 8) = q;
+                if (sub == 0) p.AS[g] = d;
+            }
+        }
+    }
+    __syncthreads();
+    if (!jv) return;
+
+    float acc[MR];
+#pragma unroll
+    for (int r = 0; r < MR; ++r) acc[r] = 0.0f;
+    for (int64_t bb = 0; bb < KB; bb += 32 * U) {
+        if (bb > 0) load_round(bb);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t b = bb + u * 32 + lane;
+            if (b >= KB) continue;
+#pragma unroll
+            for (int r = 0; r < MR; ++r) {
+                if (r >= M) break;
+                const uint4* pa = reinterpret_cast<const uint4*>(a_s + r * K + b * 32);
+                const uint4 a0 = pa[0], a1 = pa[1];
+                u32x8 av;
+                av.v[0] = a0.x; av.v[1] = a0.y; av.v[2] = a0.z; av.v[3] = a0.w;
+                av.v[4] = a1.x; av.v[5] = a1.y; av.v[6] = a1.z; av.v[7] = a1.w;
+                const int sdot = block_dot(av, wv[u]);
+                acc[r] = fmaf(as_s[r * KB + b] * wsv[u], static_cast<float>(sdot), acc[r]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < MR; ++r) {
+        if (r >= M) break;
+        const float v = warp_sum(acc[r]);
+        if (lane == 0) p.C[r * N + j] = v;
+    }
+}
+
+template <int MR, int U, int WSL>
+cudaError_t launch_fused_mr(const FusedArgs& a, bool v8, int sms, cudaStream_t stream) {
+    const size_t smem = static_cast<size_t>(MR) * a.K + static_cast<size_t>(MR) * (a.K / 32) * 4;
+    if (smem > 200 * 1024) return cudaErrorNotSupported;
+    // one output column per warp; NW warps per CTA quantize x once for NW columns
+    constexpr int NW = kFusedWarps;
+    const int64_t grid = (a.N + NW - 1) / NW;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    (void)sms;
+    auto k8 = qdot_fused_kernel<MR, U, true, WSL, NW>;
+    auto k4 = qdot_fused_kernel<MR, U, false, WSL, NW>;
+    auto kern = v8 ? k8 : k4;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NW * 32), smem, stream, a);
+}
+
 }  // namespace
+
+cudaError_t launch_qdot_fused(const FusedArgs& a, cudaStream_t stream) {
+    // one row (the decode step); the grid must fit one wave of two 1024-thread CTAs per SM
+    if (a.M != 1) return cudaErrorNotSupported;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNotSupported;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return cudaErrorNotSupported;
+    if ((a.N + kFusedWarps - 1) / kFusedWarps > 2 * static_cast<int64_t>(sms)) return cudaErrorNotSupported;
+    const bool v8 = (reinterpret_cast<uintptr_t>(a.W) & 31u) == 0;
+    return a.ws_layout == 0 ? launch_fused_mr<1, 4, 0>(a, v8, sms, stream) : launch_fused_mr<1, 4, 1>(a, v8, sms, stream);
+}
 
 cudaError_t launch_qdot_simt(const QdotArgs& a, cudaStream_t stream) {
     // 256-bit loads need 32-byte aligned blocks: every row starts at a multiple

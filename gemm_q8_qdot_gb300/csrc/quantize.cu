@@ -23,25 +23,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBlocksPerCta = kThreads / 4;
 
-__device__ __forceinline__ uint32_t q_byte(float v, float d) {
-    if (d == 0.0f) return 0u;
-    int r = __float2int_rn(__fdiv_rn(v, d));  // IEEE x/d, round to nearest even
-    r = max(-127, min(127, r));
-    return static_cast<uint32_t>(r) & 0xffu;
-}
-
-__device__ __forceinline__ uint32_t pack4(float a, float b, float c, float e, float d) {
-    return q_byte(a, d) | (q_byte(b, d) << 8) | (q_byte(c, d) << 16) | (q_byte(e, d) << 24);
-}
-
-// x may be written by the preceding kernel: coherent load, kept after pdl_wait.
-__device__ __forceinline__ float4 ld_stream_f4(const float* p) {
-    float4 r;
-    asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(p) : "memory");
-    return r;
-}
-
 __global__ void __launch_bounds__(kThreads)
 quantize_q8_0_kernel(const float* __restrict__ x, int8_t* __restrict__ q, float* __restrict__ s,
                      int64_t nblocks) {
@@ -59,17 +40,9 @@ quantize_q8_0_kernel(const float* __restrict__ x, int8_t* __restrict__ q, float*
         v0 = ld_stream_f4(p);
         v1 = ld_stream_f4(p + 4);
     }
-    float amax = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
-                       fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
-    // every lane of the warp takes part, so the full mask is exact
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const float d = __fdiv_rn(amax, 127.0f);
+    const float d = q8_block_scale(v0, v1);  // every lane of the warp takes part
     if (live) {
-        uint2 packed;
-        packed.x = pack4(v0.x, v0.y, v0.z, v0.w, d);
-        packed.y = pack4(v1.x, v1.y, v1.z, v1.w, d);
-        *reinterpret_cast<uint2*>(q + g * 32 + sub * 8) = packed;
+        *reinterpret_cast<uint2*>(q + g * 32 + sub * 8) = q8_pack8(v0, v1, d);
         if (sub == 0) s[g] = d;
     }
 }

@@ -115,6 +115,28 @@ int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const flo
                     int ws_layout, int path, cudaStream_t stream);
 
 /*
+ * One decode step in one call: quantize the activation rows x [M, K] f32 to
+ * Q8_0 (exactly as pq_quantize_q8_0) and contract them with W (as
+ * pq_qdot_q8_0_ex with the given weight-scale layout, automatic path) -- the
+ * quantizer feeding qdot_t that "Quantized built-ins and formats", section
+ * "Q8_0", describes ("the activations are quantized the same way").  For one
+ * row (M == 1) and N up to 64 x the SM count this is one kernel, in which
+ * every CTA quantizes x into its shared memory while its weight stream is in
+ * flight; otherwise it is the quantizer followed by qdot_t, launched so that
+ * the second overlaps the first.  A [M, K] int8 and AS [M, K/32] f32
+ * optionally receive the quantized rows (both null, or both non-null).  When
+ * they are null and the two-kernel route is taken, the rows go to a
+ * per-device workspace that the library allocates on the first such call and
+ * grows when a larger one arrives (that call must not be inside a stream
+ * capture); the workspace is shared by all calls on the device, so calls of
+ * this kind must not overlap on different streams.  x: 16-byte aligned f32
+ * [M, K]; A 16-byte aligned; AS, WS, C 4-byte aligned.  C must not overlap
+ * any input.
+ */
+int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W, const float* WS,
+                          float* C, int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);
+
+/*
  * The integer stage alone, for verification: S[i, j, b] = sum over k in
  * block b of A[i, k] * W[j, k] ("Quantized built-ins and formats": "the
  * inner sum in integers"), computed by the engine of `path` (PQ_PATH_SIMT:
@@ -136,7 +158,7 @@ int pq_check_device(cudaStream_t stream);
 /* A static, human-readable name for a pq_status code. */
 const char* pq_strerror(int code);
 
-/* ABI version of this header: major * 100 + minor. */
+/* ABI version of this header: major * 100 + minor (1.01: pq_quantize_qdot_q8_0). */
 int pq_version(void);
 
 #ifdef __cplusplus

@@ -30,8 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_abi():
     names = declared_functions()
-    for n in ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_qdot_q8_0_blocksums",
-              "pq_check_device", "pq_strerror", "pq_version"):
+    for n in ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
+              "pq_qdot_q8_0_blocksums", "pq_check_device", "pq_strerror", "pq_version"):
         assert n in names, n
 
 
@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert lib.pq_version() == 100
+    assert lib.pq_version() == 101
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert lib.pq_strerror(code).decode()
     assert "unknown" in lib.pq_strerror(99).decode()
@@ -111,3 +111,17 @@ def test_unknown_codes(lib):
     assert qdot(lib, path=7) == binding.PQ_ERR_INVALID_ARG
     assert qdot(lib, layout=3) == binding.PQ_ERR_INVALID_ARG
     assert lib.pq_qdot_q8_0_blocksums(P16, P16, P16, 1, 1, 32, 9, None) == binding.PQ_ERR_INVALID_ARG
+
+
+def fused(lib, x=P16, A=None, AS=None, W=P16, WS=P16, C=P16, M=1, N=1, K=32, layout=0):
+    return lib.pq_quantize_qdot_q8_0(x, A, AS, W, WS, C, M, N, K, layout, None)
+
+
+def test_fused_entry_checks(lib):
+    assert fused(lib, K=48) == binding.PQ_ERR_SHAPE
+    assert fused(lib, M=0, x=None, W=None, WS=None, C=None) == binding.PQ_OK
+    assert fused(lib, x=None) == binding.PQ_ERR_INVALID_ARG
+    assert fused(lib, A=P16, AS=None) == binding.PQ_ERR_INVALID_ARG     # A and AS come together
+    assert fused(lib, x=P8) == binding.PQ_ERR_ALIGN
+    assert fused(lib, A=P8, AS=P16) == binding.PQ_ERR_ALIGN
+    assert fused(lib, layout=5) == binding.PQ_ERR_INVALID_ARG

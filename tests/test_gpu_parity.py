@@ -300,3 +300,65 @@ def test_qdot_workload_full_tc(pq, name):
     sampled_check(C, qa, sa, qw, sw, rows, np.unique(cols), name)
     # a property at full size: every row of C is finite
     assert torch.isfinite(C).all()
+
+
+# ------------------------------------------------------------------ fused quantize + qdot
+
+FUSED_SHAPES = [(1, 64, 256), (1, 300, 1056), (2, 17, 128), (3, 129, 512), (4, 64, 4096), (7, 33, 96),
+                (8, 257, 256), (1, 40, 14336)]
+
+
+@pytest.mark.parametrize("M,N,K", FUSED_SHAPES)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_quantize_qdot_fused(pq, M, N, K, layout):
+    rng = np.random.default_rng(M * 101 + N + K + layout)
+    x = (rng.standard_normal((M, K)) * np.exp(rng.uniform(-3, 3, size=(M, 1)))).astype(np.float32)
+    _, _, w, w_s = rand_operands(N + K, 1, N, K)
+    qa, sa = oracle.quantize_q8_0(x)
+    out, bound = oracle.qdot(qa, sa, w, w_s)
+    ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+    A = torch.full((M, K), 77, dtype=torch.int8, device=DEV)
+    AS = torch.full((M, K // 32), -1.0, dtype=torch.float32, device=DEV)
+    C = pq.quantize_qdot_q8_0(dev(x), dev(w), dev(ws), A=A, AS=AS, ws_layout=layout)
+    pq.check_device()
+    assert_bytes_equal(A, AS, qa, sa)
+    assert_within_bound(C, out, bound, f"fused M={M} N={N} K={K} layout={layout}")
+    # without the optional outputs: same result
+    C2 = pq.quantize_qdot_q8_0(dev(x), dev(w), dev(ws), ws_layout=layout)
+    pq.check_device()
+    assert_within_bound(C2, out, bound, "fused, no A/AS")
+
+
+def test_quantize_qdot_large_m(pq):
+    """M > 1 runs the quantizer and qdot_t as two kernels, into A / AS or the workspace."""
+    M, N, K = 40, 96, 256
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    _, _, w, w_s = rand_operands(3, 1, N, K)
+    qa, sa = oracle.quantize_q8_0(x)
+    out, bound = oracle.qdot(qa, sa, w, w_s)
+    C0 = pq.quantize_qdot_q8_0(dev(x), dev(w), dev(w_s))          # workspace route
+    pq.check_device()
+    assert_within_bound(C0, out, bound, "two-kernel route, workspace")
+    A = torch.empty((M, K), dtype=torch.int8, device=DEV)
+    AS = torch.empty((M, K // 32), dtype=torch.float32, device=DEV)
+    C = pq.quantize_qdot_q8_0(dev(x), dev(w), dev(w_s), A=A, AS=AS)
+    pq.check_device()
+    assert_bytes_equal(A, AS, qa, sa)
+    assert_within_bound(C, out, bound, "two-kernel route")
+
+
+@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if workloads.WORKLOADS[n].M <= 8])
+def test_quantize_qdot_workload_full(pq, name):
+    """Decode / small-batch workloads at full size through the one-call step."""
+    x, w, qa, sa, qw, sw = quantized_workload(name)
+    M, N = qa.shape[0], qw.shape[0]
+    W, WS = pq.quantize_q8_0(dev(w))
+    A = torch.empty(qa.shape, dtype=torch.int8, device=DEV)
+    AS = torch.empty(sa.shape, dtype=torch.float32, device=DEV)
+    C = pq.quantize_qdot_q8_0(dev(x), W, WS, A=A, AS=AS)
+    pq.check_device()
+    assert_bytes_equal(A, AS, qa, sa)
+    rng = np.random.default_rng(2)
+    cols = np.sort(rng.choice(N, min(N, 1024), replace=False))
+    sampled_check(C, qa, sa, qw, sw, np.arange(M), cols, name)
