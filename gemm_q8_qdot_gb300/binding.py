@@ -21,12 +21,14 @@ PQ_ERR_ALIGN = -3
 PQ_ERR_CUDA = -4
 PQ_ERR_TIMEOUT = -5
 PQ_ERR_UNSUPPORTED = -6
+PQ_ERR_SCRATCH = -7
 
 PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
 WS_N_KB, WS_KB_N = 0, 1
 
 EXPORTS = ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
-           "pq_qdot_q8_0_blocksums", "pq_check_device", "pq_strerror", "pq_version")
+           "pq_quantize_qdot_q8_0_noalloc", "pq_qdot_q8_0_blocksums", "pq_check_device", "pq_strerror",
+           "pq_version")
 
 _lib: ctypes.CDLL | None = None
 
@@ -55,13 +57,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pq_qdot_q8_0.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp]
     lib.pq_qdot_q8_0_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp]
     lib.pq_quantize_qdot_q8_0.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
+    lib.pq_quantize_qdot_q8_0_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_qdot_q8_0_blocksums.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_check_device.argtypes = [vp]
     lib.pq_strerror.argtypes = [i32]
     lib.pq_strerror.restype = ctypes.c_char_p
     lib.pq_version.argtypes = []
     for fn in ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
-               "pq_qdot_q8_0_blocksums", "pq_check_device", "pq_version"):
+               "pq_quantize_qdot_q8_0_noalloc", "pq_qdot_q8_0_blocksums", "pq_check_device", "pq_version"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -145,6 +148,20 @@ def quantize_qdot_q8_0(x, W, WS, C=None, A=None, AS=None, ws_layout: int = WS_N_
         C = torch.empty((M, N), dtype=torch.float32, device=x.device)
     _check(load().pq_quantize_qdot_q8_0(_ptr(x), _ptr(A), _ptr(AS), _ptr(W), _ptr(WS), _ptr(C), M, N, K,
                                         int(ws_layout), _stream(stream)), "pq_quantize_qdot_q8_0")
+    return C
+
+
+def quantize_qdot_q8_0_noalloc(x, W, WS, C=None, ws_layout: int = WS_N_KB, stream=None):
+    """pq_quantize_qdot_q8_0_noalloc: the one-call step with the quantized rows in the library's
+    fixed device array instead of an allocated workspace (for callers that cannot allocate)."""
+    if x.dtype != torch.float32:
+        raise TypeError("x must be float32")
+    M, K = x.shape
+    N = W.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(load().pq_quantize_qdot_q8_0_noalloc(_ptr(x), _ptr(W), _ptr(WS), _ptr(C), M, N, K, int(ws_layout),
+                                                _stream(stream)), "pq_quantize_qdot_q8_0_noalloc")
     return C
 
 

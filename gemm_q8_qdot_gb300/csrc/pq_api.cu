@@ -177,6 +177,7 @@ const char* pq_strerror(int code) {
         case PQ_ERR_CUDA: return "CUDA runtime error";
         case PQ_ERR_TIMEOUT: return "a bounded on-device wait gave up";
         case PQ_ERR_UNSUPPORTED: return "unsupported device or shape for this path";
+        case PQ_ERR_SCRATCH: return "problem larger than the fixed scratch of the allocation-free entry point";
         default: return "unknown pq_status";
     }
 }

@@ -64,8 +64,12 @@ typedef enum {
     PQ_ERR_ALIGN = -3,       /* a base pointer below the alignment stated above */
     PQ_ERR_CUDA = -4,        /* the CUDA runtime refused a launch or a query */
     PQ_ERR_TIMEOUT = -5,     /* a bounded on-device wait gave up (reported by pq_check_device) */
-    PQ_ERR_UNSUPPORTED = -6  /* the device is not sm_103 / the path cannot take this shape */
+    PQ_ERR_UNSUPPORTED = -6, /* the device is not sm_103 / the path cannot take this shape */
+    PQ_ERR_SCRATCH = -7      /* the problem does not fit the fixed scratch of pq_quantize_qdot_q8_0_noalloc */
 } pq_status;
+
+/* Bytes of device memory that pq_quantize_qdot_q8_0_noalloc keeps for itself on every GPU. */
+#define PQ_NOALLOC_SCRATCH_BYTES (1u << 20)
 
 /* Kernel path selector for pq_qdot_q8_0_ex / pq_qdot_q8_0_blocksums. */
 enum {
@@ -135,6 +139,38 @@ int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const flo
  */
 int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W, const float* WS,
                           float* C, int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);
+
+/*
+ * pq_quantize_qdot_q8_0 without any device allocation.  (The Phobos pages
+ * have no counterpart: this is a property of the library, not of the method.)
+ *
+ * For callers that cannot have the library allocate device memory -- code
+ * whose work is recorded into a CUDA graph (no allocation while a stream is
+ * being captured), serving loops that must never stall on cudaMalloc or
+ * cudaFree (both may synchronize the device), hosts that give a plugin a
+ * fixed memory budget and make every allocation themselves.  Same result as
+ * pq_quantize_qdot_q8_0 with A = AS = NULL (the quantizer, then qdot_t on the
+ * automatic path), but the quantized rows and their scales are kept in a
+ * fixed array of PQ_NOALLOC_SCRATCH_BYTES (1 MiB) that is part of the library
+ * and that every GPU which loads the library holds until the process exits.
+ * The caller still passes x, W, WS and C (same layouts and alignment as
+ * pq_quantize_qdot_q8_0); nothing else is allocated, by this call or by the
+ * kernels it starts.
+ *
+ * Limits: M * K bytes (rounded up to 256) plus M * K / 8 bytes of scales must
+ * fit PQ_NOALLOC_SCRATCH_BYTES -- e.g. M <= 227 for K = 4096, M <= 65 for
+ * K = 14336 -- else PQ_ERR_SCRATCH and nothing is launched.
+ *
+ * The first call on a device resolves the array's device address there (a
+ * runtime query, no allocation); make that first call before any stream
+ * capture on that device.  Every call on a device uses the same array, and
+ * each call overwrites all of it that it reads, so nothing carries over from
+ * an earlier call; but calls that can run at the same time on the GPU (on
+ * different streams, without an ordering between them) race on the array and
+ * give wrong results.
+ */
+int pq_quantize_qdot_q8_0_noalloc(const float* x, const int8_t* W, const float* WS, float* C,
+                                  int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);
 
 /*
  * The integer stage alone, for verification: S[i, j, b] = sum over k in
