@@ -99,31 +99,58 @@ __device__ __forceinline__ int block_dot(const u32x8& a, const u32x8& w) {
 // ---------------------------------------------------------------- Q8_0 quantizer
 // Per block of 32: amax = max |x|, d = amax / 127 (IEEE division), q =
 // round(x / d) with ties to even, clamped to [-127, 127]; d == 0 gives q = 0.
-// Four consecutive lanes share a block, 8 floats each.
-
-__device__ __forceinline__ uint32_t q8_byte(float v, float d) {
-    if (d == 0.0f) return 0u;
-    int r = __float2int_rn(__fdiv_rn(v, d));  // IEEE x/d, round to nearest even
-    r = max(-127, min(127, r));
-    return static_cast<uint32_t>(r) & 0xffu;
+//
+// round(fl(x / d)) without a division per element.  With r = fl(1 / d) (one
+// correctly rounded reciprocal per block) and y = fl(x * r), both roundings
+// are relative errors of at most 2^-24, and fl(x / d) is one more, so
+//   |y - fl(x / d)| <= |x / d| * 3 * 2^-24 <= 1.5 * 2^-16   (|x / d| <= 128,
+// which holds for every element of the block since d = fl(amax / 127)).
+// Hence if y is more than 2^-14 away from a half-integer, the nearest integer
+// to y is the nearest integer to fl(x / d), with no tie to break.  Otherwise
+// (a near-tie, about one element in 10^4 for continuous data, or an r that
+// is not finite because d is subnormal) the quotient is formed with the IEEE
+// division itself.  The result is bit-identical to round(__fdiv_rn(x, d)).
+__device__ __forceinline__ int q8_round(float v, float d, float r) {
+    const float y = v * r;
+    const float n = rintf(y);
+    if (fabsf(y - n) < 0.5f - 6.103515625e-05f) return static_cast<int>(n);  // 0.5 - 2^-14
+    return __float2int_rn(__fdiv_rn(v, d));
 }
 
-// The block's scale: a width-4 xor butterfly of max over the 4 lanes.  Every
-// lane of the warp must call it (full-mask shuffles).
-__device__ __forceinline__ float q8_block_scale(const float4& v0, const float4& v1) {
-    float amax = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
-                       fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+__device__ __forceinline__ uint32_t q8_byte(float v, float d, float r) {
+    if (d == 0.0f) return 0u;
+    const int q = max(-127, min(127, q8_round(v, d, r)));
+    return static_cast<uint32_t>(q) & 0xffu;
+}
+
+// The block's scale when LANES consecutive lanes share a block: an xor
+// butterfly of max over them.  Every lane of the warp must call it
+// (full-mask shuffles).
+template <int LANES>
+__device__ __forceinline__ float q8_scale_of(float amax) {
+#pragma unroll
+    for (int m = 1; m < LANES; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
     return __fdiv_rn(amax, 127.0f);
 }
 
-// This lane's 8 quantized bytes, little-endian in two words.
+__device__ __forceinline__ float amax4(const float4& v) {
+    return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+}
+
+// Four quantized bytes, little-endian in one word.
+__device__ __forceinline__ uint32_t q8_pack4(const float4& v, float d, float r) {
+    return q8_byte(v.x, d, r) | (q8_byte(v.y, d, r) << 8) | (q8_byte(v.z, d, r) << 16) | (q8_byte(v.w, d, r) << 24);
+}
+
+// Four lanes per block, 8 floats each: the block's scale ...
+__device__ __forceinline__ float q8_block_scale(const float4& v0, const float4& v1) {
+    return q8_scale_of<4>(fmaxf(amax4(v0), amax4(v1)));
+}
+
+// ... and this lane's 8 quantized bytes in two words.
 __device__ __forceinline__ uint2 q8_pack8(const float4& v0, const float4& v1, float d) {
-    uint2 r;
-    r.x = q8_byte(v0.x, d) | (q8_byte(v0.y, d) << 8) | (q8_byte(v0.z, d) << 16) | (q8_byte(v0.w, d) << 24);
-    r.y = q8_byte(v1.x, d) | (q8_byte(v1.y, d) << 8) | (q8_byte(v1.z, d) << 16) | (q8_byte(v1.w, d) << 24);
-    return r;
+    const float r = __frcp_rn(d);
+    return make_uint2(q8_pack4(v0, d, r), q8_pack4(v1, d, r));
 }
 
 // x may be written by the preceding kernel: coherent, kept after pdl_wait.

@@ -216,30 +216,29 @@ qdot_fused_kernel(FusedArgs p) {
     };
     load_round(0);
 
-    // quantize x while the first weight round is in flight: 4 lanes per Q8_0
-    // block, 8 blocks per warp per CTA round (warp-uniform loop for the shuffles)
-    const int64_t nq = M * KB;
+    // quantize x while the first weight round is in flight: 8 lanes per Q8_0
+    // block, 4 floats each, so every thread of the CTA works; the next round's
+    // x load is issued before the current round is quantized
+    const int64_t nthr = M * KB * 8;    // one float4 of x per thread and round
     const bool writer = blockIdx.x == 0 && p.A != nullptr;
-    for (int64_t base = 0; base < nq; base += NW * 8) {
-        const int64_t g = base + (threadIdx.x >> 2);
-        const int sub = threadIdx.x & 3;
-        const bool live = g < nq;
-        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
-        if (live) {
-            const float* px = p.x + g * 32 + sub * 8;
-            v0 = ld_stream_f4(px);
-            v1 = ld_stream_f4(px + 4);
-        }
-        const float d = q8_block_scale(v0, v1);
-        if (live) {
-            const uint2 q = q8_pack8(v0, v1, d);
-            *reinterpret_cast<uint2*>(a_s + g * 32 + sub * 8) = q;
-            if (sub == 0) as_s[g] = d;
+    constexpr int64_t kRound = NW * 32;
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 xv = threadIdx.x < nthr ? ld_stream_f4(p.x + threadIdx.x * 4) : zero4;
+    for (int64_t base = 0; base < nthr; base += kRound) {  // CTA-uniform
+        const int64_t t = base + threadIdx.x;
+        const int64_t tn = t + kRound;
+        const float4 xn = tn < nthr ? ld_stream_f4(p.x + tn * 4) : zero4;
+        const float d = q8_scale_of<8>(amax4(xv));  // every lane of the warp takes part
+        if (t < nthr) {
+            const uint32_t q = q8_pack4(xv, d, __frcp_rn(d));
+            *reinterpret_cast<uint32_t*>(a_s + t * 4) = q;
+            if ((threadIdx.x & 7) == 0) as_s[t >> 3] = d;
             if (writer) {
-                *reinterpret_cast<uint2*>(p.A + g * 32 + sub * 8) = q;
-                if (sub == 0) p.AS[g] = d;
+                *reinterpret_cast<uint32_t*>(p.A + t * 4) = q;
+                if ((threadIdx.x & 7) == 0) p.AS[t >> 3] = d;
             }
         }
+        xv = xn;
     }
     __syncthreads();
     if (!jv) return;

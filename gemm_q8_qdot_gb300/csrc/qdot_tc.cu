@@ -10,29 +10,45 @@
 // every partial sum of one 32-element block (|S| <= 524288 < 2^24) is exact in
 // an f32 accumulator, so a kind::f16 MMA with f32 accumulation gives the
 // integer block sums S exactly, whatever order the tensor core adds in.  Each
-// Q8_0 block is two K = 16 MMAs into a fresh TMEM accumulator; the epilogue
-// warps read S back (tcgen05.ld) and apply acc += (xs * ys) * S in f32
-// registers.  (GB300's dense int8 tensor rate is far below its f16 rate, so
-// the integer MMA kind is not used.)
+// Q8_0 block is two K = 16 MMAs into a fresh TMEM accumulator.  (GB300's
+// dense int8 tensor rate is far below its f16 rate, and ptxas does not take
+// the integer MMA kind for sm_103a.)
+//
+// Scale products on the tensor core.  The per-block factor xs[p, b] * ys[q, b]
+// is itself a rank-1 product, so a third MMA per block (bf16, K = 16) writes
+// the 128 x BN tile of factors P next to S in TMEM: each f32 scale is split
+// exactly into three bf16 (hi + mid + lo, each the rounded remainder of the
+// previous), and the K = 16 operand rows [h h h m m m l l l 0 ..] of X and
+// [h m l h m l h m l 0 ..] of Y multiply out to all nine cross terms, whose
+// f32 sum is xs * ys up to f32 rounding.  The epilogue is then one tcgen05.ld
+// of S, one of P and one FFMA per output per block: acc += P * S.
 //
 // Tile.  The "P" operand X (128 rows per tile, the MMA M and the TMEM lanes)
 // and the "Q" operand Y (BN rows, the MMA N) are both K-major int8 [rows, K].
-// For M > 64, X = A and Y = W (output C[p * N + q]); for M <= 64, X = W and
-// Y = A with BN = M rounded up to 16 (output C[q * N + p]), so that the large
-// weight matrix fills the 128-row side.  Optional split-K over gridDim.z adds
-// the partial sums into a zeroed C with atomics.
+// For M > 64, X = A and Y = W (output C[p * N + q], BN = 128); for M <= 64,
+// X = W and Y = A with BN = M rounded up to 16, 32 or 64 (output C[q * N + p]),
+// so that the large weight matrix fills the 128-row side.
 //
-// Pipeline (one CTA per tile, warp-specialised):
-//   warp 0      TMA: int8 tiles of X and Y, 64 K per stage, 64-byte swizzle
-//               -> int8 ring (full8 / empty8 mbarriers);
-//   warps 2..   converters: int8 -> f16 (magic-number trick: the byte b is
-//               biased to b + 128, placed under the f16 exponent of 1024 and
-//               1152 is subtracted, all exact) into the UMMA K-major layout
-//               with the 128-byte swizzle -> f16 ring (full16 / empty16);
-//   warp 1      MMA issuer: 2 x tcgen05.mma per block into one of NBUF TMEM
-//               buffers, tcgen05.commit -> tfull; commits free f16 stages;
-//   epilogue    tcgen05.ld of S, f32 scale-and-accumulate in registers,
-//   warps       scales prefetched one group of 4 blocks ahead (tempty).
+// Work.  Persistent CTAs (at most one per SM) take (P tile, Q tile, K split)
+// units round-robin, the P tile varying fastest.  K is split only when the
+// tiles are too few to spread evenly over the SMs; split units add their
+// partial sums into a zeroed C with atomics.
+//
+// Pipeline (warp-specialised, all hand-offs through mbarriers):
+//   warp 0      TMA producer: per int8 stage (one scale group of 4 blocks,
+//               128 K) a 128-byte-swizzled int8 box of X and of Y and the
+//               two f32 scale boxes, on one barrier (int8 ring, S8 deep);
+//   warps 2..5  converters: int8 -> f16 (the byte b is biased to b + 128,
+//               placed under the f16 exponent of 1024 and 1152 subtracted,
+//               all exact) into the UMMA K-major 128-byte-swizzle layout, two
+//               f16 stages of 64 K per int8 stage, plus the bf16 split
+//               operands of the stage's scale products (f16 ring, S16 deep);
+//   warp 1      MMA issuer (one thread): 2 S-MMAs + 1 P-MMA per block into
+//               one of NBUF TMEM buffer pairs, tcgen05.commit -> tfull;
+//               commits also free the f16 stages;
+//   warps 6..13 epilogue: four TMEM lane quadrants x two column halves;
+//               acc += P * S in registers; the unit's last block stores C
+//               (float4 when the rows are 16-byte aligned).
 //
 // Safety.  Every mbarrier wait is bounded (a clock64 limit).  A wait that
 // gives up sets the library's device status word and a CTA-wide abort flag;

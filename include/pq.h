@@ -112,7 +112,11 @@ int pq_qdot_q8_0(const int8_t* A, const float* AS, const int8_t* W, const float*
  * As pq_qdot_q8_0, with the weight-scale layout (PQ_WS_N_KB for qdot_t,
  * PQ_WS_KB_N for qmma_t, spec section 10) and the kernel path chosen by the
  * caller (PQ_PATH_*).  PQ_ERR_UNSUPPORTED if the chosen path cannot take
- * the shape.
+ * the shape.  PQ_PATH_TC works on groups of four Q8_0 blocks and loads the
+ * scale planes with TMA, so it needs K a multiple of 128, AS and WS 16-byte
+ * aligned, and N a multiple of 4 for PQ_WS_KB_N (TMA row strides are
+ * multiples of 16 bytes); otherwise it returns PQ_ERR_UNSUPPORTED, and
+ * PQ_PATH_AUTO takes the dp4a kernel instead.
  */
 int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const float* WS,
                     float* C, int64_t M, int64_t N, int64_t K,

@@ -92,6 +92,54 @@ def test_quantize_random(pq, rows, K):
     assert_bytes_equal(qg, sg, q_ref, s_ref)
 
 
+def near_tie_rows(rows, K, seed):
+    """Blocks built to land x / d on or next to half-integers, at many scales.
+
+    Per block: element 0 is 127 * sc (so amax / 127 is sc up to rounding);
+    the others are (n + 0.5) * sc for random n, or that value's float
+    neighbour on either side.  Every fourth block is plain random data; two
+    blocks have subnormal scales (d subnormal) and one is near FLT_MAX.
+    """
+    rng = np.random.default_rng(seed)
+    x = np.empty((rows, K), dtype=np.float32)
+    blocks = x.reshape(-1, 32)
+    for b in range(blocks.shape[0]):
+        sc = np.float32(1.0) if b % 4 == 0 else np.float32(np.ldexp(1.0 + rng.uniform(0, 1), int(rng.integers(-30, 30))))
+        if b % 4 == 3:
+            v = (rng.uniform(-127, 127, 32) * sc).astype(np.float32)
+        else:
+            n = (rng.integers(-127, 127, 32) + 0.5).astype(np.float32)
+            v = (n * sc).astype(np.float32)
+            side = rng.integers(0, 3, 32)
+            v = np.where(side == 1, np.nextafter(v, np.float32(np.inf)), v)
+            v = np.where(side == 2, np.nextafter(v, np.float32(-np.inf)), v)
+        v[0] = np.float32(127.0) * sc
+        v = np.clip(v, -np.float32(127.0) * sc, np.float32(127.0) * sc)
+        blocks[b] = v
+    blocks[1] = (rng.integers(-127, 128, 32) * np.float32(1e-45)).astype(np.float32)   # subnormal x and d
+    blocks[2] = (rng.uniform(-1, 1, 32) * np.float32(3e-41)).astype(np.float32)
+    blocks[5] = (rng.uniform(-1, 1, 32) * np.float32(3.0e38)).astype(np.float32)       # near FLT_MAX
+    return x
+
+
+@pytest.mark.parametrize("rows,K", [(1, 4096), (1, 14336), (3, 1024), (64, 256)])
+def test_quantize_near_ties(pq, rows, K):
+    """The quantizer's rounding against the oracle's IEEE division on near-tie quotients:
+    the standalone quantizer and the fused step's quantized rows, bit for bit."""
+    x = near_tie_rows(rows, K, rows * 31 + K)
+    q_ref, s_ref = oracle.quantize_q8_0(x)
+    qg, sg = pq.quantize_q8_0(dev(x))
+    torch.cuda.synchronize()
+    assert_bytes_equal(qg, sg, q_ref, s_ref)
+    w = np.ones((8, K), dtype=np.int8)
+    w_s = np.ones((8, K // 32), dtype=np.float32)
+    A = torch.empty((rows, K), dtype=torch.int8, device=DEV)
+    AS = torch.empty((rows, K // 32), dtype=torch.float32, device=DEV)
+    pq.quantize_qdot_q8_0(dev(x), dev(w), dev(w_s), A=A, AS=AS)
+    pq.check_device()
+    assert_bytes_equal(A, AS, q_ref, s_ref)
+
+
 @pytest.mark.parametrize("name", list(workloads.WORKLOADS))
 def test_quantize_workload_full(pq, name):
     x, w, qa, sa, qw, sw = quantized_workload(name)
