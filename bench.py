@@ -385,7 +385,7 @@ def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str, one_kernel
             wl.weight_bytes + wl.M * wl.K + 4 * wl.M * (wl.K // 32) + 4 * wl.M * wl.N)
         achieved = nbytes / (qdot_ms * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])
-        kernel = ("qdot_fused" if one_kernel else "qdot_simt") if wl.M <= 8 else "qdot_tc"
+        kernel = ("qdot_fused" if one_kernel else "qdot_simt") if wl.M <= 16 else "qdot_tc"
         traffic = recorded_traffic(kernel, wl.name)
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,

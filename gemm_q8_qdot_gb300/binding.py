@@ -139,7 +139,8 @@ def qdot_q8_0_ex(A, AS, W, WS, C=None, ws_layout: int = WS_N_KB, path: int = PAT
 
 def quantize_qdot_q8_0(x, W, WS, C=None, A=None, AS=None, ws_layout: int = WS_N_KB, stream=None):
     """One decode step via pq_quantize_qdot_q8_0: C = qdot_t(quantize(x), W); A/AS optionally
-    receive the quantized rows (required for M > 8)."""
+    receive the quantized rows (both or neither; without them the library keeps the rows in
+    its own workspace)."""
     if x.dtype != torch.float32:
         raise TypeError("x must be float32")
     M, K = x.shape

@@ -89,10 +89,12 @@ int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS
     pq::QdotArgs a{A, AS, W, WS, C, S, M, N, K, ws_layout};
     if (path == PQ_PATH_SIMT) return map_cuda(pq::launch_qdot_simt(a, stream));
     if (path == PQ_PATH_TC) return map_cuda(pq::launch_qdot_tc(a, stream));
-    // automatic: the dp4a streaming kernel while it keeps up with HBM (M <= 8),
-    // the tensor cores above; shapes the tensor-core kernel cannot take
-    // (K % 128 != 0) go to the dp4a kernel, which takes every shape
-    if (M > 8) {
+    // automatic: the dp4a streaming kernel up to 16 rows (measured on GB300 at
+    // K = 4096, N = 11008: 36 us at M = 16 against 44 us for the tensor-core
+    // kernel, which is flat at 44-47 us up to M = 32), the tensor cores above;
+    // shapes the tensor-core kernel cannot take (K % 128 != 0) go to the dp4a
+    // kernel, which takes every shape
+    if (M > 16) {
         cudaError_t e = pq::launch_qdot_tc(a, stream);
         if (e != cudaErrorNotSupported) return map_cuda(e);
     }

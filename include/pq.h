@@ -73,7 +73,7 @@ typedef enum {
 
 /* Kernel path selector for pq_qdot_q8_0_ex / pq_qdot_q8_0_blocksums. */
 enum {
-    PQ_PATH_AUTO = 0,  /* by M: the dp4a streaming kernels for small M, tensor cores above */
+    PQ_PATH_AUTO = 0,  /* by M: the dp4a streaming kernels up to M = 16, tensor cores above */
     PQ_PATH_SIMT = 1,  /* dp4a (CUDA-core) streaming kernel, any M */
     PQ_PATH_TC = 2     /* tcgen05 tensor-core kernel (f16 operands, exact integer block sums) */
 };
