@@ -14,11 +14,14 @@ pages it follows, are stated in the C file:
   qdot_t formula with the inner sum in integers;
 * "Phobos Language Spec", section 10 "Quantized built-ins" -- operand shapes,
   the qmma_t scale layout [K/32, N];
-* same spec, section 9, Elementwise table -- round() ties to even.
+* same spec, section 9, Elementwise table -- round() ties to even;
+* same spec, section 10, Q5_0 row (q50_qdot_t) -- Q5_0 weight blocks (qh word,
+  16 nibble bytes, elements q - 16) against Q8_0 activations.
 
 Pins: every function here is checked against values fixed by the pages and by
 mathematics (brute force in exact rationals, closed forms, invariants, a
-float64 library matmul on dequantized values) in ``tests/test_oracle_pins.py``.
+float64 library matmul on dequantized values) in ``tests/test_oracle_pins.py``
+and, for Q5_0, ``tests/test_oracle_q50_pins.py``.
 The exact f32 bit pattern of qdot_t's output is not fixed by the pages (the
 summation order and FMA contraction are free), so that is held to a tolerance,
 not pinned.
@@ -73,8 +76,14 @@ def _lib(mutant: int = 0) -> ctypes.CDLL:
             lib.oracle_qdot_q8_0.argtypes = [_I8P, _F32P, _I8P, _F32P, _F64P, _F64P, _I64, _I64, _I64]
             lib.oracle_qdot_q8_0_ex.argtypes = [_I8P, _F32P, _I8P, _F32P, _F64P, _F64P,
                                                 _I64, _I64, _I64, ctypes.c_int]
+            _U8P = ctypes.POINTER(ctypes.c_uint8)
+            lib.oracle_decode_q5_0.argtypes = [_U8P, _I8P, _I64, _I64]
+            lib.oracle_blocksums_q5_0.argtypes = [_I8P, _U8P, _I64P, _I64, _I64, _I64]
+            lib.oracle_qdot_q5_0.argtypes = [_I8P, _F32P, _U8P, _F32P, _F64P, _F64P,
+                                             _I64, _I64, _I64, ctypes.c_int]
             for fn in ("oracle_quantize_q8_0", "oracle_blocksums_q8_0", "oracle_qdot_q8_0",
-                       "oracle_qdot_q8_0_ex"):
+                       "oracle_qdot_q8_0_ex", "oracle_decode_q5_0", "oracle_blocksums_q5_0",
+                       "oracle_qdot_q5_0"):
                 getattr(lib, fn).restype = None
             lib.oracle_mutant.restype = ctypes.c_int
             assert lib.oracle_mutant() == mutant
@@ -145,4 +154,56 @@ def qdot(a, a_scales, w, w_scales, ws_layout: int = 0, mutant: int = 0):
         lib.oracle_qdot_q8_0(*args)
     else:
         lib.oracle_qdot_q8_0_ex(*args, int(ws_layout))
+    return out, bound
+
+
+# ---------------------------------------------------------------- Q5_0 weights
+
+Q50_BYTES = 20  # bytes per 32-element Q5_0 block without its scale
+
+
+def decode_q5_0(w5, K: int, mutant: int = 0) -> np.ndarray:
+    """Q5_0 blocks uint8 [R, K/32 * 20] -> int8 [R, K] (q - 16)."""
+    w5 = _c(w5, np.uint8)
+    R = w5.shape[0]
+    if K % QK or w5.shape[1] != K // QK * Q50_BYTES:
+        raise ValueError("shape mismatch")
+    w = np.empty((R, K), np.int8)
+    _lib(mutant).oracle_decode_q5_0(_p(w5, ctypes.c_uint8), _p(w, ctypes.c_int8), R, K)
+    return w
+
+
+def blocksums_q5_0(a, w5, mutant: int = 0) -> np.ndarray:
+    """a int8 [M, K], Q5_0 blocks [N, K/32 * 20] -> S int64 [M, N, K/32]."""
+    a = _c(a, np.int8)
+    w5 = _c(w5, np.uint8)
+    M, K = a.shape
+    N = w5.shape[0]
+    if K % QK or w5.shape[1] != K // QK * Q50_BYTES:
+        raise ValueError("shape mismatch")
+    S = np.empty((M, N, K // QK), np.int64)
+    _lib(mutant).oracle_blocksums_q5_0(_p(a, ctypes.c_int8), _p(w5, ctypes.c_uint8),
+                                       _p(S, ctypes.c_int64), M, N, K)
+    return S
+
+
+def qdot_q5_0(a, a_scales, w5, w_scales, ws_layout: int = 0, mutant: int = 0):
+    """q50_qdot_t (ws_layout 0) / q50_qmma_t scale layout (1) in double: (out, bound)."""
+    a = _c(a, np.int8)
+    w5 = _c(w5, np.uint8)
+    a_scales = _c(a_scales, np.float32)
+    w_scales = _c(w_scales, np.float32)
+    M, K = a.shape
+    N = w5.shape[0]
+    KB = K // QK
+    if K % QK or w5.shape[1] != KB * Q50_BYTES or a_scales.shape != (M, KB):
+        raise ValueError("shape mismatch")
+    if w_scales.shape != ((N, KB) if ws_layout == 0 else (KB, N)):
+        raise ValueError("w_scales shape mismatch")
+    out = np.empty((M, N), np.float64)
+    bound = np.empty((M, N), np.float64)
+    _lib(mutant).oracle_qdot_q5_0(_p(a, ctypes.c_int8), _p(a_scales, ctypes.c_float),
+                                  _p(w5, ctypes.c_uint8), _p(w_scales, ctypes.c_float),
+                                  _p(out, ctypes.c_double), _p(bound, ctypes.c_double),
+                                  M, N, K, int(ws_layout))
     return out, bound

@@ -177,3 +177,88 @@ void oracle_qdot_q8_0(const int8_t* a, const float* as, const int8_t* w, const f
     oracle_qdot_q8_0_ex(a, as, w, ws, out, bound, M, N, K, 0);
 #endif
 }
+
+/* ------------------------------------------------------------------ Q5_0 weights
+ *
+ * q50_qdot_t ("Phobos Language Spec" section 10, Q5_0 row; "Quantized built-ins
+ * and formats", built-in table): qdot_t against a Q5_0 weight held as its
+ * blocks without their f16 scale.  Per 32 elements a block is 20 bytes: the qh
+ * word, then 16 bytes whose byte e holds element e in its low nibble and
+ * element e + 16 in its high nibble; each element is q - 16, widened as it is
+ * loaded; the scales are as for qdot_t (w_scales [N, K/32] f32, or [K/32, N]
+ * for q50_qmma_t).
+ *
+ * Reading (the pages do not spell out the qh bit order): qh is a little-endian
+ * 32-bit word and its bit e is the fifth bit (value 16) of element e, so
+ * q = nibble(e) | (((qh >> e) & 1) << 4).
+ *
+ * w5 [N, K/32 * 20] bytes, row-major, block b of row j at byte j*(K/32)*20 + 20*b.
+ */
+#define Q50_BYTES 20
+
+static int q50_value(const uint8_t* blk, int e) {
+    const uint32_t qh = (uint32_t)blk[0] | ((uint32_t)blk[1] << 8) | ((uint32_t)blk[2] << 16) |
+                        ((uint32_t)blk[3] << 24);
+    const uint8_t byte = blk[4 + (e & 15)];
+#if ORACLE_MUTANT == 10
+    const int nib = e < 16 ? (byte >> 4) : (byte & 15); /* mutant: nibble halves swapped */
+#else
+    const int nib = e < 16 ? (byte & 15) : (byte >> 4);
+#endif
+#if ORACLE_MUTANT == 9
+    const int hb = (int)((qh >> (31 - e)) & 1u); /* mutant: qh bit order reversed */
+#else
+    const int hb = (int)((qh >> e) & 1u);
+#endif
+    const int q = nib | (hb << 4);
+#if ORACLE_MUTANT == 11
+    return q; /* mutant: the -16 offset dropped */
+#else
+    return q - 16;
+#endif
+}
+
+/* Decoded Q5_0 weights as int8: w [rows, K] = q - 16 in [-16, 15]. */
+void oracle_decode_q5_0(const uint8_t* w5, int8_t* w, int64_t rows, int64_t K) {
+    const int64_t KB = K / QK;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < KB; ++b) {
+            const uint8_t* blk = w5 + (r * KB + b) * Q50_BYTES;
+            for (int e = 0; e < QK; ++e) w[r * K + b * QK + e] = (int8_t)q50_value(blk, e);
+        }
+}
+
+/* Integer block sums S[i, j, b] = sum_{e < 32} a[i, 32b + e] * (q[j, 32b + e] - 16), int64. */
+void oracle_blocksums_q5_0(const int8_t* a, const uint8_t* w5, int64_t* S, int64_t M, int64_t N, int64_t K) {
+    const int64_t KB = K / QK;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j)
+            for (int64_t b = 0; b < KB; ++b) {
+                const uint8_t* blk = w5 + (j * KB + b) * Q50_BYTES;
+                int64_t acc = 0;
+                for (int e = 0; e < QK; ++e) acc += (int64_t)a[i * K + b * QK + e] * (int64_t)q50_value(blk, e);
+                S[(i * N + j) * KB + b] = acc;
+            }
+}
+
+/* q50_qdot_t in double, with the same tolerance as qdot_t: out[i, j] =
+ * sum_b as[i, b] * ws(j, b) * S[i, j, b]; bound = 1e-5 * sum_b |t_b| + 1e-6. */
+void oracle_qdot_q5_0(const int8_t* a, const float* as, const uint8_t* w5, const float* ws,
+                      double* out, double* bound, int64_t M, int64_t N, int64_t K, int ws_layout) {
+    const int64_t KB = K / QK;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double T = 0.0, U = 0.0;
+            for (int64_t b = 0; b < KB; ++b) {
+                const uint8_t* blk = w5 + (j * KB + b) * Q50_BYTES;
+                int64_t S = 0;
+                for (int e = 0; e < QK; ++e) S += (int64_t)a[i * K + b * QK + e] * (int64_t)q50_value(blk, e);
+                const double wsb = ws_layout ? (double)ws[b * N + j] : (double)ws[j * KB + b];
+                const double t = (double)as[i * KB + b] * wsb * (double)S;
+                T += t;
+                U += fabs(t);
+            }
+            out[i * N + j] = T;
+            if (bound) bound[i * N + j] = 1e-5 * U + 1e-6;
+        }
+}

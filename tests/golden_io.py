@@ -59,3 +59,25 @@ def qdot_cases():
             elif key == "out":
                 cur["out"][(int(vals[0]), int(vals[1]))] = float(vals[2])
     return cases
+
+
+def q5_0_blocks():
+    """Yields (name, bytes uint8[20], values int8[32]) from q5_0_blocks.txt."""
+    out = []
+    cur = None
+    with open(os.path.join(GOLDEN, "q5_0_blocks.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "block":
+                cur = {"name": vals[0]}
+                out.append(cur)
+            elif key == "bytes":
+                assert len(vals) == 20
+                cur["bytes"] = np.array([int(v, 16) for v in vals], np.uint8)
+            elif key == "values":
+                assert len(vals) == 32
+                cur["values"] = np.array([int(v) for v in vals], np.int8)
+    return [(b["name"], b["bytes"], b["values"]) for b in out]
