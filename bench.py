@@ -73,6 +73,7 @@ KERNEL_SOURCES = {
                 "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
     "quantize": ["gemm_q8_qdot_gb300/csrc/quantize.cu"],
     "qdot_fused": ["gemm_q8_qdot_gb300/csrc/qdot_simt.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
+    "qdot_q50": ["gemm_q8_qdot_gb300/csrc/qdot_q50.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
 }
 
 
@@ -244,13 +245,18 @@ class Problem:
         import torch
         self.wl = wl
         self.pq = pq
-        self.fused = fused and wl.M <= 8
+        self.q50 = wl.w_format == "q5_0"
+        self.fused = fused and wl.M <= 8 and not self.q50
         x = workloads.activations(wl)
         self.x_host = torch.from_numpy(x).pin_memory()
         self.x = self.x_host.to(device)
-        w = torch.from_numpy(workloads.weights(wl)).to(device)
-        W, WS = pq.quantize_q8_0(w)
-        del w
+        if self.q50:
+            w5, ws = workloads.q50_weights(wl)
+            W, WS = torch.from_numpy(w5).to(device), torch.from_numpy(ws).to(device)
+        else:
+            w = torch.from_numpy(workloads.weights(wl)).to(device)
+            W, WS = pq.quantize_q8_0(w)
+            del w
         wbytes = W.numel() + WS.numel() * 4
         self.copies = max(2, -(-2 * L2_BYTES // wbytes))
         self.W = [W] + [W.clone() for _ in range(self.copies - 1)]
@@ -276,9 +282,15 @@ class Problem:
         self.pq.quantize_q8_0(self.x, self.A, self.AS)
         if events is not None:
             events[1].record()
-        self.pq.qdot_q8_0(self.A, self.AS, self.W[c], self.WS[c], self.C)
+        self.qdot(c)
         if events is not None:
             events[2].record()
+
+    def qdot(self, c: int):
+        if self.q50:
+            self.pq.q50_qdot(self.A, self.AS, self.W[c], self.WS[c], self.C)
+        else:
+            self.pq.qdot_q8_0(self.A, self.AS, self.W[c], self.WS[c], self.C)
 
     @property
     def algorithmic_bytes(self) -> int:
@@ -296,8 +308,7 @@ def _capture(prob: Problem, first: int, steps: int, stream, events=None, only_qd
     with torch.cuda.graph(g, stream=stream):
         for t in range(steps):
             if only_qdot:
-                c = (first + t) % prob.copies
-                prob.pq.qdot_q8_0(prob.A, prob.AS, prob.W[c], prob.WS[c], prob.C)
+                prob.qdot((first + t) % prob.copies)
             else:
                 prob.step(first + t, events[t] if events else None)
     return g
@@ -385,7 +396,8 @@ def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str, one_kernel
             wl.weight_bytes + wl.M * wl.K + 4 * wl.M * (wl.K // 32) + 4 * wl.M * wl.N)
         achieved = nbytes / (qdot_ms * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])
-        kernel = ("qdot_fused" if one_kernel else "qdot_simt") if wl.M <= 16 else "qdot_tc"
+        kernel = "qdot_q50" if prob.q50 else \
+            ("qdot_fused" if one_kernel else "qdot_simt") if wl.M <= 16 else "qdot_tc"
         traffic = recorded_traffic(kernel, wl.name)
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
@@ -425,7 +437,7 @@ def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sample
     kernel_ms["dominant"] = round(dom_ms, 5)
     res = {"value": round(value / scale, 3), "unit": unit, "ms_per_step": round(t_max * 1e3 / steps, 5),
            "step": ("pq_quantize_qdot_q8_0 (one kernel)" if one_kernel else "pq_quantize_qdot_q8_0 (two kernels)")
-           if prob.fused else "pq_quantize_q8_0 + pq_qdot_q8_0",
+           if prob.fused else ("pq_quantize_q8_0 + pq_q50_qdot" if prob.q50 else "pq_quantize_q8_0 + pq_qdot_q8_0"),
            "kernel_ms": kernel_ms,
            "roofline": roofline_for(prob, dom_ms, peaks, peak_src, one_kernel), "weight_copies": prob.copies,
            "window": window}
@@ -535,7 +547,8 @@ def main(argv=None):
     others = {}
     if not args.no_others:
         for name in (PROMPT, "ffn_up_m1_k4096_n14336", "ffn_down_m1_k14336_n4096",
-                     "smallm_m4_k4096_n11008", "smallm_m16_k4096_n11008", "smallm_m64_k4096_n11008"):
+                     "smallm_m4_k4096_n11008", "smallm_m16_k4096_n11008", "smallm_m64_k4096_n11008",
+                     "q50_decode_m1_k4096_n4096"):
             if name == args.workload:
                 continue
             try:

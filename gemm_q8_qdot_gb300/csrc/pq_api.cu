@@ -163,6 +163,32 @@ int pq_qdot_q8_0_blocksums(const int8_t* A, const int8_t* W, int32_t* S, int64_t
     return qdot_impl(A, nullptr, W, nullptr, nullptr, S, M, N, K, PQ_WS_N_KB, path, stream);
 }
 
+int pq_q50_qdot(const int8_t* A, const float* AS, const uint8_t* W5, const float* WS, float* C,
+                int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream) {
+    if (ws_layout != PQ_WS_N_KB && ws_layout != PQ_WS_KB_N) return PQ_ERR_INVALID_ARG;
+    int st = check_qdot_shape(M, N, K);
+    if (st != PQ_OK) return st;
+    if ((__int128)N * (K / 32) * 20 > (__int128)INT64_MAX) return PQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return PQ_OK;
+    if (!A || !AS || !W5 || !WS || !C) return PQ_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(W5, 4) || !aligned(AS, 4) || !aligned(WS, 4) || !aligned(C, 4))
+        return PQ_ERR_ALIGN;
+    pq::QdotArgs a{A, AS, reinterpret_cast<const int8_t*>(W5), WS, C, nullptr, M, N, K, ws_layout};
+    return map_cuda(pq::launch_qdot_q50(a, stream));
+}
+
+int pq_q50_blocksums(const int8_t* A, const uint8_t* W5, int32_t* S, int64_t M, int64_t N, int64_t K,
+                     cudaStream_t stream) {
+    int st = check_qdot_shape(M, N, K);
+    if (st != PQ_OK) return st;
+    if ((__int128)N * (K / 32) * 20 > (__int128)INT64_MAX) return PQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return PQ_OK;
+    if (!A || !W5 || !S) return PQ_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(W5, 4) || !aligned(S, 4)) return PQ_ERR_ALIGN;
+    pq::QdotArgs a{A, nullptr, reinterpret_cast<const int8_t*>(W5), nullptr, nullptr, S, M, N, K, PQ_WS_N_KB};
+    return map_cuda(pq::launch_qdot_q50(a, stream));
+}
+
 int pq_check_device(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return PQ_ERR_CUDA;
     unsigned status = 0;
@@ -184,7 +210,7 @@ const char* pq_strerror(int code) {
     }
 }
 
-int pq_version(void) { return 101; }
+int pq_version(void) { return 102; }
 
 int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles) {
     if (skip_stage < -1) return PQ_ERR_INVALID_ARG;

@@ -60,6 +60,10 @@ cudaError_t launch_qdot_simt(const QdotArgs& a, cudaStream_t stream);
 // quantized row does not fit a CTA's shared memory).
 cudaError_t launch_qdot_fused(const FusedArgs& a, cudaStream_t stream);
 
+// dp4a kernel for Q5_0 weights (q50_qdot_t): a.W points at the 20-byte Q5_0
+// blocks, [N, K/32 * 20] bytes; any M.
+cudaError_t launch_qdot_q50(const QdotArgs& a, cudaStream_t stream);
+
 // tcgen05 tensor-core kernel.  cudaErrorNotSupported if the device is not sm_103.
 cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream);
 

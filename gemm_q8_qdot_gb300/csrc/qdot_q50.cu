@@ -1,0 +1,200 @@
+// q50_qdot_t on CUDA cores with dp4a: Q8_0 activations against Q5_0 weights.
+//
+// "Phobos Language Spec", section 10 (Quantized built-ins), Q5_0 row, and
+// "Quantized built-ins and formats", built-in table: qdot_t against a Q5_0
+// weight held as its blocks without their f16 scale.  A weight block is 20
+// bytes per 32 elements: the qh word, then 16 bytes whose byte e holds element
+// e in its low nibble and element e + 16 in its high nibble; each element is
+// q - 16.  qh is read as a little-endian word whose bit e is the fifth bit of
+// element e.  The scales are as for qdot_t: w_scales [N, K/32] f32, or
+// [K/32, N] (q50_qmma_t's layout).
+//
+//   out[i, j] = sum_b a_scales[i, b] * w_scales[j, b] * sum_{e<32} a[i, 32b+e] * (q[j, 32b+e] - 16)
+//
+// Work layout as the Q8_0 streaming kernel: a warp owns COLS output columns
+// and MR activation rows; lane l takes blocks l, l + 32, ... of K.  A weight
+// row is K/32 * 20 bytes, so the 32 blocks a warp reads at once are 640
+// contiguous bytes: each lane loads its block as five 32-bit words, the first
+// of which brings every line of the 640 bytes into L1, so the other four hit.
+// The weights cross HBM at their stored size: 0.625 bytes per weight plus
+// 0.125 of scale.
+//
+// Decode in registers: the low and high nibbles of the four data words give
+// elements 0..15 and 16..31 in dp4a word order; the matching four qh bits are
+// spread to bit 4 of each byte ((x * 0x00204081) & 0x01010101 puts bit i of x
+// at bit 8i, no carries); q - 16 per byte without borrows is
+// ((q | 0x80) - 0x10) ^ 0x80 on all four bytes at once, a signed byte in
+// [-16, 15].  Then 8 dp4a against the activation block, exact in int32.
+#include "pq_internal.h"
+#include "pq_device.cuh"
+
+namespace pq {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kQ50Bytes = 20;
+
+// 32-bit global load, kept in L1 (the neighbouring lanes' loads hit the same
+// lines); volatile and coherent like every load after griddepcontrol.wait.
+__device__ __forceinline__ uint32_t ld_u32(const void* p) {
+    uint32_t r;
+    asm volatile("ld.global.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+struct Q50Block {
+    uint32_t w[5];  // qh, then the 16 nibble bytes as four words
+};
+
+__device__ __forceinline__ Q50Block ld_q50(const uint8_t* p) {
+    Q50Block b;
+#pragma unroll
+    for (int t = 0; t < 5; ++t) b.w[t] = ld_u32(p + 4 * t);
+    return b;
+}
+
+__device__ __forceinline__ uint32_t spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
+
+__device__ __forceinline__ uint32_t minus16(uint32_t q) {
+    return ((q | 0x80808080u) - 0x10101010u) ^ 0x80808080u;
+}
+
+// The block's 32 elements as signed bytes, word t = elements 4t .. 4t+3.
+__device__ __forceinline__ u32x8 q50_unpack(const Q50Block& b) {
+    u32x8 r;
+    const uint32_t qh = b.w[0];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint32_t w = b.w[1 + t];
+        const uint32_t lo = (w & 0x0F0F0F0Fu) | (spread4((qh >> (4 * t)) & 0xFu) << 4);
+        const uint32_t hi = ((w >> 4) & 0x0F0F0F0Fu) | (spread4((qh >> (16 + 4 * t)) & 0xFu) << 4);
+        r.v[t] = minus16(lo);
+        r.v[4 + t] = minus16(hi);
+    }
+    return r;
+}
+
+template <int MR, int COLS, int U, bool V8, bool SUMS, int WSL>
+__global__ void __launch_bounds__(kWarps * 32)
+qdot_q50_kernel(QdotArgs p) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t N = p.N, M = p.M, K = p.K, KB = K >> 5;
+    const int64_t row_bytes = KB * kQ50Bytes;
+    const uint8_t* W5 = reinterpret_cast<const uint8_t*>(p.W);
+    const int64_t j0 = (static_cast<int64_t>(blockIdx.x) * kWarps + warp) * COLS;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.y) * MR;
+    pdl_trigger();
+    if (j0 >= N) return;  // warp-uniform; no CTA-wide synchronisation below
+    if (lane < COLS && j0 + lane < N) {
+        // bulk L2 prefetch of the weight row when it is 16-byte aligned and sized
+        const uint8_t* row = W5 + (j0 + lane) * row_bytes;
+        if ((row_bytes % 16) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0 && row_bytes < (int64_t(1) << 30))
+            prefetch_l2(row, static_cast<uint32_t>(row_bytes));
+    }
+    pdl_wait();
+
+    bool jv[COLS];
+    const uint8_t* wrow[COLS];
+#pragma unroll
+    for (int c = 0; c < COLS; ++c) {
+        jv[c] = (j0 + c) < N;
+        wrow[c] = W5 + (jv[c] ? (j0 + c) : j0) * row_bytes;
+    }
+    bool iv[MR];
+    const int8_t* arow[MR];
+#pragma unroll
+    for (int r = 0; r < MR; ++r) {
+        iv[r] = (i0 + r) < M;
+        arow[r] = p.A + (iv[r] ? (i0 + r) : i0) * K;
+    }
+
+    float acc[MR][COLS];
+#pragma unroll
+    for (int r = 0; r < MR; ++r)
+#pragma unroll
+        for (int c = 0; c < COLS; ++c) acc[r][c] = 0.0f;
+
+    for (int64_t bb = 0; bb < KB; bb += 32 * U) {
+        Q50Block wb[U][COLS];
+        float wsv[U][COLS];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t b = bb + u * 32 + lane;
+#pragma unroll
+            for (int c = 0; c < COLS; ++c) {
+                if (b < KB && jv[c]) {
+                    wb[u][c] = ld_q50(wrow[c] + b * kQ50Bytes);
+                    if constexpr (!SUMS)
+                        wsv[u][c] = ld_f32(WSL == 0 ? p.WS + (j0 + c) * KB + b : p.WS + b * N + (j0 + c));
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 5; ++t) wb[u][c].w[t] = 0u;
+                    wsv[u][c] = 0.0f;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t b = bb + u * 32 + lane;
+            if (b >= KB) continue;
+            u32x8 wq[COLS];
+#pragma unroll
+            for (int c = 0; c < COLS; ++c) wq[c] = q50_unpack(wb[u][c]);
+#pragma unroll
+            for (int r = 0; r < MR; ++r) {
+                if (!iv[r]) continue;
+                const u32x8 av = ld_block<V8, false>(arow[r] + b * 32);
+                float as = 0.0f;
+                if constexpr (!SUMS) as = ld_f32(p.AS + (i0 + r) * KB + b);
+#pragma unroll
+                for (int c = 0; c < COLS; ++c) {
+                    const int s = block_dot(av, wq[c]);
+                    if constexpr (SUMS) {
+                        if (jv[c]) p.S[((i0 + r) * N + (j0 + c)) * KB + b] = s;
+                    } else {
+                        acc[r][c] = fmaf(as * wsv[u][c], static_cast<float>(s), acc[r][c]);
+                    }
+                }
+            }
+        }
+    }
+    if constexpr (!SUMS) {
+#pragma unroll
+        for (int r = 0; r < MR; ++r)
+#pragma unroll
+            for (int c = 0; c < COLS; ++c) {
+                const float v = warp_sum(acc[r][c]);
+                if (lane == 0 && iv[r] && jv[c]) p.C[(i0 + r) * N + (j0 + c)] = v;
+            }
+    }
+}
+
+template <int MR, int COLS, int U, bool SUMS, int WSL>
+cudaError_t launch_tile(const QdotArgs& a, bool v8, cudaStream_t stream) {
+    const int64_t gx = (a.N + kWarps * COLS - 1) / (kWarps * COLS);
+    const int64_t gy = (a.M + MR - 1) / MR;
+    if (gx > 0x7fffffffLL || gy > 65535) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+    if (v8) return launch_pdl(qdot_q50_kernel<MR, COLS, U, true, SUMS, WSL>, grid, dim3(kWarps * 32), 0, stream, a);
+    return launch_pdl(qdot_q50_kernel<MR, COLS, U, false, SUMS, WSL>, grid, dim3(kWarps * 32), 0, stream, a);
+}
+
+template <bool SUMS, int WSL>
+cudaError_t launch_by_m(const QdotArgs& a, bool v8, cudaStream_t stream) {
+    if (a.M == 1) return launch_tile<1, 1, 4, SUMS, WSL>(a, v8, stream);
+    if (a.M == 2) return launch_tile<2, 2, 2, SUMS, WSL>(a, v8, stream);
+    return launch_tile<4, 2, 2, SUMS, WSL>(a, v8, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_qdot_q50(const QdotArgs& a, cudaStream_t stream) {
+    // the activation blocks take 256-bit loads when A is 32-byte aligned
+    const bool v8 = (reinterpret_cast<uintptr_t>(a.A) & 31u) == 0;
+    if (a.S != nullptr) return launch_by_m<true, 0>(a, v8, stream);
+    if (a.ws_layout == 0) return launch_by_m<false, 0>(a, v8, stream);
+    return launch_by_m<false, 1>(a, v8, stream);
+}
+
+}  // namespace pq

@@ -12,7 +12,11 @@ Shapes are decode and prompt projections of a model with hidden size 4096
   channels (a seeded choice of columns) are multiplied by 50;
 * weights ~ N(0, 0.02); for the decode FFN shapes 1% of the entries (a
   seeded Bernoulli mask) are multiplied by 20;
-* the smallest (parity) case uses N(0, 1) for both.
+* the smallest (parity) case uses N(0, 1) for both;
+* the Q5_0 decode case (q50_qdot_t) draws its weight blocks directly: every
+  byte uniform in [0, 255] (so every element q - 16 is uniform in [-16, 15])
+  and the f32 block scales log-uniform in [1e-3, 1e-2], the range a Q5_0
+  encoding of N(0, 0.02) weights has (the pages define no Q5_0 encoder).
 
 Every workload is seeded with 20261202 + its index, drawn with numpy's PCG64.
 """
@@ -35,6 +39,7 @@ class Workload:
     x_dist: str = "normal"        # normal | row_loguniform | outlier_channels
     w_std: float = 0.02
     w_outliers: bool = False
+    w_format: str = "q8_0"        # q8_0 | q5_0 (q50_qdot_t)
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
     @property
@@ -43,8 +48,10 @@ class Workload:
 
     @property
     def weight_bytes(self) -> int:
-        """Stored bytes of W in Q8_0: N*K int8 values plus N*K/32 f32 scales."""
-        return self.N * self.K + 4 * self.N * (self.K // 32)
+        """Stored bytes of W: Q8_0 N*K int8 values, or Q5_0 20 bytes per 32 elements,
+        plus N*K/32 f32 scales."""
+        data = self.N * (self.K // 32) * 20 if self.w_format == "q5_0" else self.N * self.K
+        return data + 4 * self.N * (self.K // 32)
 
     @property
     def ops(self) -> int:
@@ -61,7 +68,11 @@ WORKLOADS = {
     "smallm_m16_k4096_n11008": Workload("smallm_m16_k4096_n11008", 16, 11008, 4096, 3, x_dist="row_loguniform"),
     "smallm_m64_k4096_n11008": Workload("smallm_m64_k4096_n11008", 64, 11008, 4096, 3, x_dist="row_loguniform"),
     "prompt_m512_k4096_n14336": Workload("prompt_m512_k4096_n14336", 512, 14336, 4096, 4, x_dist="outlier_channels"),
+    "q50_decode_m1_k4096_n4096": Workload("q50_decode_m1_k4096_n4096", 1, 4096, 4096, 5, w_format="q5_0"),
 }
+
+# the workloads whose weights are Q8_0 (qdot_t proper)
+Q8_WORKLOADS = {n: w for n, w in WORKLOADS.items() if w.w_format == "q8_0"}
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -105,3 +116,13 @@ def random_int8(rng: np.random.Generator, shape, lo: int = -128, hi: int = 127) 
 def random_scales(rng: np.random.Generator, shape, lo: float = 1e-4, hi: float = 1.0) -> np.ndarray:
     """Positive f32 scales, log-uniform in [lo, hi]."""
     return np.exp(rng.uniform(np.log(lo), np.log(hi), size=shape)).astype(np.float32)
+
+
+def q50_weights(wl: Workload, N: int | None = None, K: int | None = None):
+    """Q5_0 weight blocks uint8 [N, K/32 * 20] and f32 scales [N, K/32] of a workload."""
+    N = wl.N if N is None else N
+    K = wl.K if K is None else K
+    rng = _rng(wl.seed, 4)
+    w5 = rng.integers(0, 256, size=(N, K // 32 * 20), dtype=np.uint8)
+    ws = random_scales(rng, (N, K // 32), 1e-3, 1e-2)
+    return w5, ws

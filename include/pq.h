@@ -188,6 +188,35 @@ int pq_qdot_q8_0_blocksums(const int8_t* A, const int8_t* W, int32_t* S,
                            int64_t M, int64_t N, int64_t K, int path, cudaStream_t stream);
 
 /*
+ * q50_qdot_t: C[M, N] = the Q8_0 contraction of A [M, K] with a Q5_0 weight
+ * ("Phobos Language Spec", section 10, Q5_0 row; "Quantized built-ins and
+ * formats", built-in table):
+ *
+ *   C[i, j] = sum over blocks b of AS[i, b] * WS[j, b]
+ *               * sum over e < 32 of A[i, 32b + e] * (q[j, 32b + e] - 16)
+ *
+ * W5 holds the weight's Q5_0 blocks without their scale, row-major
+ * [N, K/32 * 20] bytes: per 32 elements a 4-byte qh word, then 16 bytes whose
+ * byte e holds element e in its low nibble and element e + 16 in its high
+ * nibble.  qh is read as a little-endian 32-bit word whose bit e is the fifth
+ * bit (value 16) of element e (the pages do not state the bit order; this is
+ * the reading taken).  WS is f32 [N, K/32] (PQ_WS_N_KB) or [K/32, N]
+ * (PQ_WS_KB_N, q50_qmma_t's layout); A and AS as for pq_qdot_q8_0.  C is
+ * overwritten.  Alignment: A 16 bytes; W5, AS, WS, C 4 bytes.  Every M runs
+ * the dp4a kernel.
+ */
+int pq_q50_qdot(const int8_t* A, const float* AS, const uint8_t* W5, const float* WS, float* C,
+                int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);
+
+/*
+ * The integer stage of pq_q50_qdot alone, for verification: S[i, j, b] =
+ * sum over e < 32 of A[i, 32b + e] * (q[j, 32b + e] - 16), int32 [M, N, K/32],
+ * 4-byte aligned, overwritten.
+ */
+int pq_q50_blocksums(const int8_t* A, const uint8_t* W5, int32_t* S, int64_t M, int64_t N, int64_t K,
+                     cudaStream_t stream);
+
+/*
  * Synchronizes `stream`, then reads and clears this library's device status
  * word for the current device.  Returns PQ_OK, PQ_ERR_TIMEOUT if a kernel's
  * bounded wait gave up since the last check (its output is then invalid), or
@@ -198,7 +227,7 @@ int pq_check_device(cudaStream_t stream);
 /* A static, human-readable name for a pq_status code. */
 const char* pq_strerror(int code);
 
-/* ABI version of this header: major * 100 + minor (1.01: pq_quantize_qdot_q8_0). */
+/* ABI version of this header: major * 100 + minor (1.01: pq_quantize_qdot_q8_0; 1.02: Q5_0 weights). */
 int pq_version(void);
 
 #ifdef __cplusplus

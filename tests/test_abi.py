@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     for n in ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
-              "pq_qdot_q8_0_blocksums", "pq_check_device", "pq_strerror", "pq_version"):
+              "pq_qdot_q8_0_blocksums", "pq_q50_qdot", "pq_q50_blocksums", "pq_check_device", "pq_strerror",
+              "pq_version"):
         assert n in names, n
 
 
@@ -42,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert lib.pq_version() == 101
+    assert lib.pq_version() == 102
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert lib.pq_strerror(code).decode()
     assert "unknown" in lib.pq_strerror(99).decode()
@@ -125,3 +126,20 @@ def test_fused_entry_checks(lib):
     assert fused(lib, x=P8) == binding.PQ_ERR_ALIGN
     assert fused(lib, A=P8, AS=P16) == binding.PQ_ERR_ALIGN
     assert fused(lib, layout=5) == binding.PQ_ERR_INVALID_ARG
+
+
+def q50(lib, A=P16, AS=P16, W5=P16, WS=P16, C=P16, M=1, N=1, K=32, layout=0):
+    return lib.pq_q50_qdot(A, AS, W5, WS, C, M, N, K, layout, None)
+
+
+def test_q50_entry_checks(lib):
+    assert q50(lib, K=48) == binding.PQ_ERR_SHAPE
+    assert q50(lib, M=-1) == binding.PQ_ERR_SHAPE
+    assert q50(lib, M=0, A=None, AS=None, W5=None, WS=None, C=None) == binding.PQ_OK
+    assert q50(lib, W5=None) == binding.PQ_ERR_INVALID_ARG
+    assert q50(lib, layout=2) == binding.PQ_ERR_INVALID_ARG
+    assert q50(lib, A=P8) == binding.PQ_ERR_ALIGN
+    assert q50(lib, W5=P2) == binding.PQ_ERR_ALIGN
+    assert lib.pq_q50_blocksums(P16, P16, None, 1, 1, 32, None) == binding.PQ_ERR_INVALID_ARG
+    assert lib.pq_q50_blocksums(P16, P16, P2, 1, 1, 32, None) == binding.PQ_ERR_ALIGN
+    assert lib.pq_q50_blocksums(P16, P16, P16, 1, 1, 33, None) == binding.PQ_ERR_SHAPE

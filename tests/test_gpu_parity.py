@@ -140,7 +140,7 @@ def test_quantize_near_ties(pq, rows, K):
     assert_bytes_equal(A, AS, q_ref, s_ref)
 
 
-@pytest.mark.parametrize("name", list(workloads.WORKLOADS))
+@pytest.mark.parametrize("name", list(workloads.Q8_WORKLOADS))
 def test_quantize_workload_full(pq, name):
     x, w, qa, sa, qw, sw = quantized_workload(name)
     qg, sg = pq.quantize_q8_0(dev(x))
@@ -249,7 +249,7 @@ def sampled_check(C, qa, sa, qw, sw, rows, cols, what):
     assert_within_bound(host(C)[np.ix_(rows, cols)], out, bound, what)
 
 
-@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if workloads.WORKLOADS[n].M <= 8])
+@pytest.mark.parametrize("name", [n for n in workloads.Q8_WORKLOADS if workloads.Q8_WORKLOADS[n].M <= 8])
 def test_qdot_workload_full_simt(pq, name):
     """The decode / small-batch workloads at full size, the launch the benchmark times."""
     x, w, qa, sa, qw, sw = quantized_workload(name)
@@ -333,7 +333,7 @@ def test_qdot_tc_unsupported_k(pq):
     assert_within_bound(C, out, bound, "auto fallback")
 
 
-@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if workloads.WORKLOADS[n].M > 8])
+@pytest.mark.parametrize("name", [n for n in workloads.Q8_WORKLOADS if workloads.Q8_WORKLOADS[n].M > 8])
 def test_qdot_workload_full_tc(pq, name):
     """Small-batch (M = 16, 64) and prompt (M = 512) workloads at full size, as benchmarked."""
     x, w, qa, sa, qw, sw = quantized_workload(name)
@@ -396,7 +396,7 @@ def test_quantize_qdot_large_m(pq):
     assert_within_bound(C, out, bound, "two-kernel route")
 
 
-@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if workloads.WORKLOADS[n].M <= 8])
+@pytest.mark.parametrize("name", [n for n in workloads.Q8_WORKLOADS if workloads.Q8_WORKLOADS[n].M <= 8])
 def test_quantize_qdot_workload_full(pq, name):
     """Decode / small-batch workloads at full size through the one-call step."""
     x, w, qa, sa, qw, sw = quantized_workload(name)

@@ -1,0 +1,101 @@
+"""GPU parity for Q5_0 weights (q50_qdot_t) against the CPU oracle.
+
+Bars as for Q8_0: integer block sums identical; outputs within
+1e-5 * sum_b |t_b| + 1e-6 of the oracle's double result, element by element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_q8_qdot_gb300 import workloads
+from tests import golden_io
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def operands(seed, M, N, K):
+    rng = np.random.default_rng(seed)
+    a = workloads.random_int8(rng, (M, K), -128, 127)
+    w5 = rng.integers(0, 256, size=(N, K // 32 * 20), dtype=np.uint8)
+    a_s = workloads.random_scales(rng, (M, K // 32), 1e-3, 10.0)
+    w_s = workloads.random_scales(rng, (N, K // 32), 1e-4, 1.0)
+    return a, a_s, w5, w_s
+
+
+def within(C, out, bound, what):
+    C = C.cpu().numpy().astype(np.float64)
+    err = np.abs(C - out)
+    assert np.all(err <= bound), f"{what}: {int((err > bound).sum())} outside, worst {np.max(err / bound):.3g}x"
+
+
+SHAPES = [(1, 1, 32), (1, 7, 64), (1, 300, 1056), (2, 9, 96), (3, 17, 128), (5, 33, 256), (13, 70, 160),
+          (1, 2, 14336), (64, 40, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_q50_blocksums_exact(pq, M, N, K):
+    a, _, w5, _ = operands(M * 3 + N + K, M, N, K)
+    S = pq.q50_blocksums(dev(a), dev(w5))
+    pq.check_device()
+    assert np.array_equal(S.cpu().numpy().astype(np.int64), oracle.blocksums_q5_0(a, w5))
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_q50_qdot(pq, M, N, K, layout):
+    a, a_s, w5, w_s = operands(M * 5 + N * 7 + K + layout, M, N, K)
+    ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+    out, bound = oracle.qdot_q5_0(a, a_s, w5, ws, ws_layout=layout)
+    C = pq.q50_qdot(dev(a), dev(a_s), dev(w5), dev(ws), ws_layout=layout)
+    pq.check_device()
+    within(C, out, bound, f"q50 M={M} N={N} K={K} layout={layout}")
+
+
+def test_q50_golden_blocks_on_gpu(pq):
+    """The hand-derived blocks as one weight row; a one-hot activation reads each element back."""
+    blocks = golden_io.q5_0_blocks()
+    K = 32 * len(blocks)
+    w5 = np.concatenate([b for _, b, _ in blocks])[None, :]
+    values = np.concatenate([v for _, _, v in blocks]).astype(np.int64)
+    # activation row e picks element e (a one-hot row per element of the first 64)
+    M = 64
+    a = np.zeros((M, K), np.int8)
+    a[np.arange(M), np.arange(M)] = 1
+    S = pq.q50_blocksums(dev(a), dev(w5))
+    pq.check_device()
+    got = S.cpu().numpy()[:, 0, :].sum(axis=1)
+    assert got.tolist() == values[:M].tolist()
+
+
+def test_q50_weight_base_4_byte_aligned(pq):
+    """W5 needs only 4-byte alignment (20-byte blocks): an offset view gives the same result."""
+    M, N, K = 2, 37, 256
+    a, a_s, w5, w_s = operands(99, M, N, K)
+    out, bound = oracle.qdot_q5_0(a, a_s, w5, w_s)
+    buf = torch.zeros(w5.size + 64, dtype=torch.uint8, device=DEV)
+    view = buf[4:4 + w5.size].view(N, K // 32 * 20)
+    view.copy_(dev(w5))
+    C = pq.q50_qdot(dev(a), dev(a_s), view, dev(w_s))
+    pq.check_device()
+    within(C, out, bound, "offset W5")
+
+
+def test_q50_workload_full(pq):
+    """The Q5_0 decode workload at full size: Q8_0-quantized activations, sampled columns."""
+    wl = workloads.WORKLOADS["q50_decode_m1_k4096_n4096"]
+    x = workloads.activations(wl)
+    qa, sa = oracle.quantize_q8_0(x)
+    w5, ws = workloads.q50_weights(wl)
+    C = pq.q50_qdot(dev(qa), dev(sa), dev(w5), dev(ws))
+    pq.check_device()
+    cols = np.sort(np.random.default_rng(3).choice(wl.N, 512, replace=False))
+    out, bound = oracle.qdot_q5_0(qa, sa, w5[cols], ws[cols])
+    within(C[:, torch.from_numpy(cols).to(DEV)], out, bound, "q50 decode full size")
+    assert torch.isfinite(C).all()
