@@ -56,6 +56,56 @@ __device__ __forceinline__ u32x8 ld_cached_2v4(const void* p) {
     return r;
 }
 
+// L2 eviction policy of a weight stream.  A launch that reads each weight byte
+// once can mark those lines evict_first, so that the stream (many times larger
+// than L2 across a model's layers) does not push the small, hot activation rows
+// out of L2.  Measured on GB300 (graphs of back-to-back steps, rotating weight
+// copies): the fused decode step at K = 4096, N = 4096 goes from 5.2 to 4.8 us
+// with it, the Q5_0 decode kernel from 3.91 to 3.82 us; the dp4a qdot_t kernel
+// with pre-quantized activations gets slower (4.23 to 4.62 us at M = 1, 31.8 to
+// 33.6 us at M = 16), so it does not use it.  A launch whose CTAs read the same
+// weights again (several row groups) keeps the normal priority.
+__device__ __forceinline__ uint64_t l2_weight_policy(bool read_once) {
+    uint64_t pol;
+    if (read_once) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    else asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// A weight block (32 B) with an L2 policy, not kept in L1.
+template <bool kV8>
+__device__ __forceinline__ u32x8 ld_wblock(const void* p, uint64_t pol) {
+    u32x8 r;
+    if constexpr (kV8) {
+        asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+                     : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]),
+                       "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
+                     : "l"(p), "l"(pol));
+    } else {
+        asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.b32 {%0,%1,%2,%3}, [%4], %5;"
+                     : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]) : "l"(p), "l"(pol));
+        asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.b32 {%0,%1,%2,%3}, [%4], %5;"
+                     : "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
+                     : "l"(static_cast<const char*>(p) + 16), "l"(pol));
+    }
+    return r;
+}
+
+// A weight scale with an L2 policy.
+__device__ __forceinline__ float ld_wscale(const float* p, uint64_t pol) {
+    float r;
+    asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(r) : "l"(p), "l"(pol));
+    return r;
+}
+
+// A 32-bit word of a weight block with an L2 policy (kept in L1: the Q5_0
+// kernel reads a 20-byte block as five words, the first brings the line in).
+__device__ __forceinline__ uint32_t ld_wword(const void* p, uint64_t pol) {
+    uint32_t r;
+    asm volatile("ld.global.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(r) : "l"(p), "l"(pol));
+    return r;
+}
+
 template <bool kV8, bool kStream>
 __device__ __forceinline__ u32x8 ld_block(const void* p) {
     if constexpr (kV8) {

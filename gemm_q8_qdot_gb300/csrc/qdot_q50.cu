@@ -34,22 +34,14 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kQ50Bytes = 20;
 
-// 32-bit global load, kept in L1 (the neighbouring lanes' loads hit the same
-// lines); volatile and coherent like every load after griddepcontrol.wait.
-__device__ __forceinline__ uint32_t ld_u32(const void* p) {
-    uint32_t r;
-    asm volatile("ld.global.u32 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
-}
-
 struct Q50Block {
     uint32_t w[5];  // qh, then the 16 nibble bytes as four words
 };
 
-__device__ __forceinline__ Q50Block ld_q50(const uint8_t* p) {
+__device__ __forceinline__ Q50Block ld_q50(const uint8_t* p, uint64_t pol) {
     Q50Block b;
 #pragma unroll
-    for (int t = 0; t < 5; ++t) b.w[t] = ld_u32(p + 4 * t);
+    for (int t = 0; t < 5; ++t) b.w[t] = ld_wword(p + 4 * t, pol);
     return b;
 }
 
@@ -94,6 +86,7 @@ qdot_q50_kernel(QdotArgs p) {
     }
     pdl_wait();
 
+    const uint64_t wpol = l2_weight_policy(gridDim.y == 1);
     bool jv[COLS];
     const uint8_t* wrow[COLS];
 #pragma unroll
@@ -124,9 +117,9 @@ qdot_q50_kernel(QdotArgs p) {
 #pragma unroll
             for (int c = 0; c < COLS; ++c) {
                 if (b < KB && jv[c]) {
-                    wb[u][c] = ld_q50(wrow[c] + b * kQ50Bytes);
+                    wb[u][c] = ld_q50(wrow[c] + b * kQ50Bytes, wpol);
                     if constexpr (!SUMS)
-                        wsv[u][c] = ld_f32(WSL == 0 ? p.WS + (j0 + c) * KB + b : p.WS + b * N + (j0 + c));
+                        wsv[u][c] = ld_wscale(WSL == 0 ? p.WS + (j0 + c) * KB + b : p.WS + b * N + (j0 + c), wpol);
                 } else {
 #pragma unroll
                     for (int t = 0; t < 5; ++t) wb[u][c].w[t] = 0u;
