@@ -468,6 +468,34 @@ def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sample
     return res
 
 
+def int8_library_rate():
+    """The GPU's practical dense int8 tensor rate: cuBLASLt's int8 GEMM (torch._int_mm) at 8192^3.
+
+    A context figure for the prompt GEMM, which computes int8 x int8 block sums on the f16
+    tensor path (the int8 MMA kind is not available on sm_103a); not part of any step."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randint(-127, 128, (n, n), dtype=torch.int8, device="cuda")
+        b = torch.randint(-127, 128, (n, n), dtype=torch.int8, device="cuda").t()
+        for _ in range(2):
+            torch._int_mm(a, b)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(3):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            torch._int_mm(a, b)
+            e.record()
+            torch.cuda.synchronize()
+            ts.append(s.elapsed_time(e))
+        del a, b
+        torch.cuda.empty_cache()
+        return round(2 * n ** 3 / (sorted(ts)[1] * 1e-3) / 1e12, 1)
+    except Exception:  # torch without _int_mm, or no int8 GEMM for this device
+        return None
+
+
 def cpu_baseline(name: str, budget_s: float = 10.0):
     """The oracle, as it stands, on a bounded sample of the workload (rank 0, host cores)."""
     import oracle
@@ -566,6 +594,13 @@ def main(argv=None):
                 others[name] = r
             except pq.PQError as e:
                 others[name] = {"error": str(e)}
+    prompt_res = head if args.workload == PROMPT else others.get(PROMPT, {})
+    if "roofline" in prompt_res:
+        rate = int8_library_rate()
+        if rate:
+            rl = prompt_res["roofline"]
+            rl["int8_library_tops"] = rate
+            rl["frac_of_int8_library"] = round(rl["achieved"] / rate, 3)
     launches_per_step = 1 if head["step"].endswith("(one kernel)") else 2
     line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
