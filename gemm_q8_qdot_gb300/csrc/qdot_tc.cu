@@ -101,6 +101,7 @@ struct TcParams {
     int ys_sr, ys_sb;
     int inject_skip_stage;    // test hook: the producer skips this stage (-1: off)
     unsigned long long timeout_cycles;
+    int regsplit;             // 1: move registers from the producer / converter warps to the epilogue
 };
 
 // MMA-A ("X", 128 rows per tile) and MMA-B ("Y", BN rows) both arrive as int8
@@ -284,6 +285,18 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     __syncthreads();
     tc::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Register split between the roles.  The launch gives each of the 512 threads
+    // 128 registers; the warpgroups of the producer, the MMA issuer and the
+    // converters (warps 0-7) give 16 each to the epilogue warpgroups (warps 8-15),
+    // whose 64 accumulators and TMEM chunks then fit without spilling:
+    // 256 x 112 + 256 x 144 = 65,536 = the launch's total.  The host sets regsplit
+    // only after checking that the kernel was built with exactly 128 registers.
+    if constexpr (CF::kThreads == 512 && CF::kE0 == 8) {
+        if (prm.regsplit) {
+            if (warp < CF::kE0) asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
+            else asm volatile("setmaxnreg.inc.sync.aligned.u32 144;" ::: "memory");
+        }
+    }
     // everything below reads global memory the preceding kernel may have written
     pdl_wait();
 
@@ -644,8 +657,15 @@ cudaError_t launch_cfg(const CUtensorMap* maps, const TcParams& prm, int64_t gri
     auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SUMS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::kSmem);
     if (e != cudaSuccess) return e;
+    // the register split adds up only if every thread was launched with 128 registers
+    static const int regs = [&] {
+        cudaFuncAttributes fa{};
+        return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : 0;
+    }();
+    TcParams p = prm;
+    p.regsplit = (CF::kThreads == 512 && CF::kE0 == 8 && regs == 128) ? 1 : 0;
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(CF::kThreads), static_cast<size_t>(CF::kSmem),
-                      stream, maps[0], maps[1], maps[2], maps[3], prm);
+                      stream, maps[0], maps[1], maps[2], maps[3], p);
 }
 
 template <bool SUMS>
