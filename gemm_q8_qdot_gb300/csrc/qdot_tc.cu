@@ -198,6 +198,19 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
+// Packed f32 pairs (low word first) and the sm_100+ paired FMA, each element
+// rounded as its scalar counterpart: one instruction for two accumulators.
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // Exact split of an f32 into three bf16 whose sum is the value (normal range).
 __device__ __forceinline__ void split3_bf16(float x, uint32_t& h, uint32_t& m, uint32_t& l) {
     const __nv_bfloat16 bh = __float2bfloat16_rn(x);
@@ -483,9 +496,9 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int prow = quad * 32 + lane;
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
 
-        float acc[CF::kCW];
+        uint64_t acc[CF::kCW / 2];  // f32 pairs: columns cb + 2t, cb + 2t + 1
 #pragma unroll
-        for (int t = 0; t < CF::kCW; ++t) acc[t] = 0.0f;
+        for (int t = 0; t < CF::kCW / 2; ++t) acc[t] = 0ull;
 
         int g = 0;  // block counter over all units of this CTA
         for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
@@ -526,9 +539,10 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         tc::TmemLd<CF::kCH>::wait(sv);
                         tc::TmemLd<CF::kCH>::wait(pvv);
 #pragma unroll
-                        for (int t = 0; t < CF::kCH; ++t)
-                            acc[c * CF::kCH + t] =
-                                fmaf(__uint_as_float(pvv[t]), __uint_as_float(sv[t]), acc[c * CF::kCH + t]);
+                        for (int t = 0; t < CF::kCH; t += 2) {
+                            const int a = (c * CF::kCH + t) / 2;
+                            acc[a] = f2_fma(f2_pack(pvv[t], pvv[t + 1]), f2_pack(sv[t], sv[t + 1]), acc[a]);
+                        }
                     }
                 }
                 tc::tc_fence_before_sync();
@@ -538,13 +552,19 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             if constexpr (!SUMS) {
                 // the unit's last block: write its tile and start the next from zero
                 if (*abort_flag == 0 && pv) {
+                    float accf[CF::kCW];
+#pragma unroll
+                    for (int t = 0; t < CF::kCW / 2; ++t) {
+                        accf[2 * t] = __uint_as_float(static_cast<uint32_t>(acc[t]));
+                        accf[2 * t + 1] = __uint_as_float(static_cast<uint32_t>(acc[t] >> 32));
+                    }
                     if (prm.vec_store) {
 #pragma unroll
                         for (int t = 0; t < CF::kCW; t += 4) {
                             const int64_t q = cu.q0 + cb + t;
                             if (q < prm.Q)
                                 *reinterpret_cast<float4*>(prm.C + p * prm.ldp + q) =
-                                    make_float4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]);
+                                    make_float4(accf[t], accf[t + 1], accf[t + 2], accf[t + 3]);
                         }
                     } else {
 #pragma unroll
@@ -553,15 +573,15 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                             if (q < prm.Q) {
                                 float* dst = prm.C + p * prm.ldp + q * prm.ldq;
                                 if (prm.atomic)
-                                    atomicAdd(dst, acc[t]);
+                                    atomicAdd(dst, accf[t]);
                                 else
-                                    *dst = acc[t];
+                                    *dst = accf[t];
                             }
                         }
                     }
                 }
 #pragma unroll
-                for (int t = 0; t < CF::kCW; ++t) acc[t] = 0.0f;
+                for (int t = 0; t < CF::kCW / 2; ++t) acc[t] = 0ull;
             }
         }
     }
