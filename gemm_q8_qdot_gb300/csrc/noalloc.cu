@@ -20,6 +20,7 @@
 #include <cuda_runtime_api.h>
 
 #include "pq.h"
+#include "pq_internal.h"
 
 namespace {
 
@@ -76,5 +77,7 @@ extern "C" int pq_quantize_qdot_q8_0_noalloc(const float* x, const int8_t* W, co
     float* AS = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + qbytes);
     const int st = pq_quantize_q8_0(x, A, AS, M, K, stream);
     if (st != PQ_OK) return st;
-    return pq_qdot_q8_0_ex(A, AS, W, WS, C, M, N, K, ws_layout, PQ_PATH_AUTO, stream);
+    // qdot_t on the path that allocates nothing (the tensor-core kernel then
+    // converts the activations itself instead of pre-tiling them in a workspace)
+    return pq::qdot_noalloc(A, AS, W, WS, C, M, N, K, ws_layout, stream);
 }

@@ -45,6 +45,61 @@ cudaError_t device_workspace(size_t bytes, void** out) {
     return cudaSuccess;
 }
 
+// Per-(device, stream) workspaces (the tensor-core path's pre-tiled
+// activations): at most 64 pairs; allocated on the first call on a stream,
+// grown (cudaFree + cudaMalloc) when a larger one arrives, kept until exit.
+cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out) {
+    struct Slot {
+        int dev;
+        cudaStream_t stream;
+        void* ptr;
+        size_t size;
+    };
+    static std::mutex mu;
+    static Slot slots[64];
+    static int nslots = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    Slot* sl = nullptr;
+    for (int i = 0; i < nslots; ++i)
+        if (slots[i].dev == dev && slots[i].stream == stream) sl = &slots[i];
+    if (sl && sl->size >= bytes) {
+        *out = sl->ptr;
+        return cudaSuccess;
+    }
+    // allocating (or freeing) is not allowed while the stream is being captured
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // leave no sticky error behind for the caller's next check
+        return e;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return cudaErrorNotPermitted;
+    if (!sl) {
+        if (nslots == 64) return cudaErrorMemoryAllocation;
+        sl = &slots[nslots++];
+        *sl = Slot{dev, stream, nullptr, 0};
+    }
+    if (sl->ptr) {
+        e = cudaFree(sl->ptr);  // synchronizes the device: no earlier call still uses it
+        if (e != cudaSuccess) return e;
+        sl->ptr = nullptr;
+        sl->size = 0;
+    }
+    const size_t want = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
+    e = cudaMalloc(&sl->ptr, want);
+    if (e != cudaSuccess) {
+        sl->ptr = nullptr;
+        cudaGetLastError();
+        return e;
+    }
+    sl->size = want;
+    *out = sl->ptr;
+    return cudaSuccess;
+}
+
 }  // namespace pq
 
 namespace {
@@ -73,7 +128,7 @@ int check_qdot_shape(int64_t M, int64_t N, int64_t K) {
 
 int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C,
               int32_t* S, int64_t M, int64_t N, int64_t K, int ws_layout, int path,
-              cudaStream_t stream) {
+              cudaStream_t stream, int no_alloc = 0) {
     if (path != PQ_PATH_AUTO && path != PQ_PATH_SIMT && path != PQ_PATH_TC) return PQ_ERR_INVALID_ARG;
     if (ws_layout != PQ_WS_N_KB && ws_layout != PQ_WS_KB_N) return PQ_ERR_INVALID_ARG;
     int st = check_qdot_shape(M, N, K);
@@ -86,7 +141,7 @@ int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS
     if (sums && !aligned(S, 4)) return PQ_ERR_ALIGN;
     if (!sums && (!aligned(AS, 4) || !aligned(WS, 4) || !aligned(C, 4))) return PQ_ERR_ALIGN;
 
-    pq::QdotArgs a{A, AS, W, WS, C, S, M, N, K, ws_layout};
+    pq::QdotArgs a{A, AS, W, WS, C, S, M, N, K, ws_layout, no_alloc};
     if (path == PQ_PATH_SIMT) return map_cuda(pq::launch_qdot_simt(a, stream));
     if (path == PQ_PATH_TC) return map_cuda(pq::launch_qdot_tc(a, stream));
     // automatic: the dp4a streaming kernel up to 16 rows (measured on GB300 at
@@ -102,6 +157,11 @@ int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS
 }
 
 }  // namespace
+
+int pq::qdot_noalloc(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C, int64_t M,
+                     int64_t N, int64_t K, int ws_layout, cudaStream_t stream) {
+    return qdot_impl(A, AS, W, WS, C, nullptr, M, N, K, ws_layout, PQ_PATH_AUTO, stream, 1);
+}
 
 extern "C" {
 

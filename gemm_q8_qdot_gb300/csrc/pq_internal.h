@@ -15,6 +15,7 @@ struct QdotArgs {
     int32_t* S;      // int32 [M, N, K/32] block sums, or null
     int64_t M, N, K;
     int ws_layout;   // 0: WS [N, K/32]; 1: WS [K/32, N]
+    int no_alloc = 0;  // 1: the call must not allocate device memory (no workspace)
 };
 
 struct FusedArgs {
@@ -70,6 +71,17 @@ cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream);
 // The current device's workspace of at least `bytes` (allocated on first use,
 // grown on demand, never freed before exit).
 cudaError_t device_workspace(size_t bytes, void** out);
+
+// A workspace of at least `bytes` for work enqueued on `stream` of the current
+// device (one per device and stream, so calls on different streams never share
+// it; allocated or grown on demand).  Fails without allocating while `stream`
+// is being captured and the workspace is too small, or when the table of
+// streams is full; callers then take a path that needs no workspace.
+cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out);
+
+// qdot_t (automatic kernel path) without any device allocation; returns a pq_status.
+int qdot_noalloc(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C, int64_t M, int64_t N,
+                 int64_t K, int ws_layout, cudaStream_t stream);
 
 // Reads and clears the device status word (set by a bounded wait that gave up).
 cudaError_t read_and_clear_status(unsigned* status);

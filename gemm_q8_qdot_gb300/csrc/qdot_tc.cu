@@ -79,6 +79,11 @@ constexpr int BM = 128;      // rows of the MMA's A operand per tile (MMA M, TME
 constexpr int KS = 64;       // K elements per f16 stage (two Q8_0 blocks)
 constexpr int KS8 = 128;     // K elements per int8 stage (one scale group): 128-byte TMA rows
 constexpr int GROUP = 4;     // Q8_0 blocks per scale group (128 K, two stages)
+// One f16 stage of the pre-tiled X operand (PREX): the 128 x 64 f16 tile in
+// the UMMA K-major 128-byte-swizzle layout, then the scale-product operands of
+// its two Q8_0 blocks (128 rows x 16 bf16 each, K-major without swizzle).
+constexpr int kXtF16 = BM * KS * 2;
+constexpr int kXtStage = kXtF16 + 2 * BM * 32;
 
 struct TcParams {
     const float* xs;          // scale of MMA-A row p, block b: xs[p * xs_r + b * xs_b]
@@ -102,6 +107,8 @@ struct TcParams {
     int inject_skip_stage;    // test hook: the producer skips this stage (-1: off)
     unsigned long long timeout_cycles;
     int regsplit;             // 1: move registers from the producer / converter warps to the epilogue
+    const uint8_t* xt;        // pre-tiled X (PREX kernels): kXtStage bytes per (P tile, f16 stage)
+    int64_t xt_tile_stride;   // bytes per P tile of xt
 };
 
 // MMA-A ("X", 128 rows per tile) and MMA-B ("Y", BN rows) both arrive as int8
@@ -223,7 +230,7 @@ __device__ __forceinline__ void split3_bf16(float x, uint32_t& h, uint32_t& m, u
     l = __bfloat16_as_ushort(bl);
 }
 
-template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS>
+template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS, bool PREX>
 __global__ void __launch_bounds__(Cfg<BN, NCONV, NEPI, S8, S16>::kThreads, MINB)
 qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
                const __grid_constant__ CUtensorMap tmXS, const __grid_constant__ CUtensorMap tmYS,
@@ -273,7 +280,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             tc::mbar_init(&empty8[i], NCONV);
         }
         for (int i = 0; i < S16; ++i) {
-            tc::mbar_init(&full16[i], NCONV);
+            tc::mbar_init(&full16[i], NCONV + (PREX ? 1 : 0));  // + the producer's copy of pre-tiled X
             tc::mbar_init(&empty16[i], 1);
         }
         for (int i = 0; i < CF::kNbuf; ++i) {
@@ -317,9 +324,13 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         // ------------------------------------------------------------ producer
         // One int8 stage = one scale group = 128 K = two f16 stages: the int8
         // tiles of X and Y and their f32 scales, four TMA boxes on one barrier.
+        // With pre-tiled X (PREX) the int8 stage holds Y and its scales only, and
+        // each f16 stage's X tile and X scale-product operands arrive by one bulk
+        // copy straight into the f16 ring (the converters then handle Y alone).
         if (lane == 0) {
-            const uint32_t tx = CF::kX8 + CF::kY8 + (prm.has_scales ? CF::kXS + CF::kYS : 0);
-            int issued8 = 0;
+            const uint32_t tx = (PREX ? 0 : CF::kX8) + CF::kY8 +
+                                (prm.has_scales ? (PREX ? 0 : CF::kXS) + CF::kYS : 0);
+            int issued8 = 0, issued16 = 0;
             int gi = 0;  // int8-stage counter over all units of this CTA
             for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
                 const Unit un = unit(u);
@@ -329,25 +340,46 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     const int g = un.g_begin + i;  // scale group = int8 stage along K
                     if (!bounded_wait(&empty8[s8], ((gi / S8) & 1) ^ 1, abort_flag, limit)) continue;
                     issued8 = gi + 1;
-                    if (gi == prm.inject_skip_stage) continue;  // test hook: never arrives
-                    tc::mbar_arrive_expect_tx(&full8[s8], tx);
-                    tc::tma_load_2d(smem + CF::kOffX8 + s8 * CF::kX8, &tmX, &full8[s8], g * KS8, static_cast<int>(un.p0));
-                    tc::tma_load_2d(smem + CF::kOffY8 + s8 * CF::kY8, &tmY, &full8[s8], g * KS8, static_cast<int>(un.q0));
-                    if (prm.has_scales) {
-                        // row-major planes: box {4 blocks, rows}; block-major: box {rows, 4 blocks}
-                        const int b0 = g * GROUP;
-                        tc::tma_load_2d(smem + CF::kOffXS + s8 * CF::kXS, &tmXS, &full8[s8],
-                                        prm.xs_sb == 1 ? b0 : static_cast<int>(un.p0),
-                                        prm.xs_sb == 1 ? static_cast<int>(un.p0) : b0);
-                        tc::tma_load_2d(smem + CF::kOffYS + s8 * CF::kYS, &tmYS, &full8[s8],
-                                        prm.ys_sb == 1 ? b0 : static_cast<int>(un.q0),
-                                        prm.ys_sb == 1 ? static_cast<int>(un.q0) : b0);
+                    if (gi != prm.inject_skip_stage) {  // test hook: the skipped stage never arrives
+                        tc::mbar_arrive_expect_tx(&full8[s8], tx);
+                        if (!PREX)
+                            tc::tma_load_2d(smem + CF::kOffX8 + s8 * CF::kX8, &tmX, &full8[s8], g * KS8,
+                                            static_cast<int>(un.p0));
+                        tc::tma_load_2d(smem + CF::kOffY8 + s8 * CF::kY8, &tmY, &full8[s8], g * KS8, static_cast<int>(un.q0));
+                        if (prm.has_scales) {
+                            // row-major planes: box {4 blocks, rows}; block-major: box {rows, 4 blocks}
+                            const int b0 = g * GROUP;
+                            if (!PREX)
+                                tc::tma_load_2d(smem + CF::kOffXS + s8 * CF::kXS, &tmXS, &full8[s8],
+                                                prm.xs_sb == 1 ? b0 : static_cast<int>(un.p0),
+                                                prm.xs_sb == 1 ? static_cast<int>(un.p0) : b0);
+                            tc::tma_load_2d(smem + CF::kOffYS + s8 * CF::kYS, &tmYS, &full8[s8],
+                                            prm.ys_sb == 1 ? b0 : static_cast<int>(un.q0),
+                                            prm.ys_sb == 1 ? static_cast<int>(un.q0) : b0);
+                        }
+                    }
+                    if constexpr (PREX) {
+#pragma unroll 1
+                        for (int h = 0; h < 2; ++h) {
+                            const int gi16 = gi * 2 + h;
+                            const int s16 = gi16 % S16;
+                            if (!bounded_wait(&empty16[s16], ((gi16 / S16) & 1) ^ 1, abort_flag, limit)) continue;
+                            issued16 = gi16 + 1;
+                            const uint8_t* src = prm.xt + (un.p0 / BM) * prm.xt_tile_stride +
+                                                 static_cast<int64_t>(g * 2 + h) * kXtStage;
+                            tc::mbar_arrive_expect_tx(&full16[s16], kXtStage);
+                            tc::bulk_copy_g2s(smem + CF::kOffX16 + s16 * CF::kX16, src, kXtF16, &full16[s16]);
+                            tc::bulk_copy_g2s(smem + CF::kOffXP + s16 * 2 * CF::kXP, src + kXtF16, 2 * CF::kXP,
+                                              &full16[s16]);
+                        }
                     }
                 }
             }
             // copies in flight land before the CTA may exit
             for (int i = max(0, issued8 - S8); i < issued8; ++i)
                 if (i != prm.inject_skip_stage) drain_wait(&full8[i % S8], (i / S8) & 1, limit);
+            if constexpr (PREX)
+                for (int i = max(0, issued16 - S16); i < issued16; ++i) drain_wait(&full16[i % S16], (i / S16) & 1, limit);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -420,10 +452,12 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         const uint32_t x16 = sbase + CF::kOffX16 + s16 * CF::kX16;
                         const uint32_t y16 = sbase + CF::kOffY16 + s16 * CF::kY16;
                         const int c8 = h * 4 + c4;  // 16-byte chunk of the 128-byte int8 row
-                        uint4 v[CF::kOctPerWarp];
+                        // octets of rows converted per warp (Y rows only with pre-tiled X)
+                        constexpr int kOw = PREX ? (BN / 8 + NCONV - 1) / NCONV : CF::kOctPerWarp;
+                        uint4 v[kOw];
 #pragma unroll
-                        for (int t = 0; t < CF::kOctPerWarp; ++t) {  // all loads first
-                            const int o = cw + t * NCONV;
+                        for (int t = 0; t < kOw; ++t) {  // all loads first
+                            const int o = (PREX ? BM / 8 : 0) + cw + t * NCONV;
                             if (o < CF::kOct) {
                                 const bool isx = o < BM / 8;
                                 const int row = (isx ? o : o - BM / 8) * 8 + r_in;
@@ -431,8 +465,8 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                             }
                         }
 #pragma unroll
-                        for (int t = 0; t < CF::kOctPerWarp; ++t) {
-                            const int o = cw + t * NCONV;
+                        for (int t = 0; t < kOw; ++t) {
+                            const int o = (PREX ? BM / 8 : 0) + cw + t * NCONV;
                             if (o < CF::kOct) {
                                 const bool isx = o < BM / 8;
                                 const int row = (isx ? o : o - BM / 8) * 8 + r_in;
@@ -450,12 +484,14 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         // 16 bf16 [h h h m m m l l l 0..] (X) or [h m l h m l h m l 0..] (Y),
                         // K-major without swizzle: 8-row x 16-byte core matrices, the two
                         // K halves 128 B apart, 8-row groups 256 B apart
+                        constexpr int kSp = PREX ? (BN * 2 + NCONV * 32 - 1) / (NCONV * 32) : CF::kSplitPerThread;
 #pragma unroll
-                        for (int t = 0; t < CF::kSplitPerThread; ++t) {
+                        for (int t = 0; t < kSp; ++t) {
                             const int w = ct + t * NCONV * 32;
-                            if (w < (BM + BN) * 2) {
-                                const int bb = w / (BM + BN);
-                                const int r = w - bb * (BM + BN);
+                            constexpr int kRows = PREX ? BN : BM + BN;  // rows whose scales are split here
+                            if (w < kRows * 2) {
+                                const int bb = w / kRows;
+                                const int r = (PREX ? BM : 0) + w - bb * kRows;
                                 const int blk = h * 2 + bb;  // block within the scale group
                                 const bool isx = r < BM;
                                 const int row = isx ? r : r - BM;
@@ -593,6 +629,47 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
 }
 
+// Pre-tiles the activation operand X = A [P, K] (with its scales AS [P, K/32])
+// for the PREX kernels: one CTA per (128-row tile, 64-K f16 stage) writes the
+// stage's f16 tile in the UMMA K-major 128-byte-swizzle layout (row r at r * 128
+// bytes, its 16-byte chunk j at ((j ^ (r & 7)) << 4)) and the scale-product
+// operands of the stage's two Q8_0 blocks (row r's 16 bf16 [h h h m m m l l l
+// 0 ..] at (r >> 3) * 256 + (r & 7) * 16, the second K half 128 bytes on), i.e.
+// exactly what the converter warps would write into the f16 ring.  Rows past P
+// are zero.  Every 128-row tile is then converted once per call instead of once
+// per output-column tile.
+__global__ void __launch_bounds__(256)
+tile_x_kernel(const int8_t* __restrict__ A, const float* __restrict__ AS, uint8_t* __restrict__ T, int64_t P,
+              int64_t K) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t ns = K / KS;
+    const int64_t KB = K / 32;
+    const int64_t tile = blockIdx.x / ns, st = blockIdx.x % ns;
+    uint8_t* out = T + static_cast<int64_t>(blockIdx.x) * kXtStage;
+    for (int i = threadIdx.x; i < BM * 8; i += blockDim.x) {
+        const int r = i >> 3, j = i & 7;
+        const int64_t p = tile * BM + r;
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (p < P) {
+            const uint2 b = *reinterpret_cast<const uint2*>(A + p * K + st * KS + j * 8);
+            i8x4_to_f16x4(b.x, o.x, o.y);
+            i8x4_to_f16x4(b.y, o.z, o.w);
+        }
+        *reinterpret_cast<uint4*>(out + r * (KS * 2) + ((j ^ (r & 7)) << 4)) = o;
+    }
+    for (int i = threadIdx.x; i < BM * 2; i += blockDim.x) {
+        const int r = i % BM, bb = i / BM;
+        const int64_t p = tile * BM + r;
+        const float sc = p < P ? AS[p * KB + st * 2 + bb] : 0.0f;
+        uint32_t sh, sm, sl3;
+        split3_bf16(sc, sh, sm, sl3);
+        uint8_t* dst = out + kXtF16 + bb * (BM * 32) + (r >> 3) * 256 + (r & 7) * 16;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(sh | (sh << 16), sh | (sm << 16), sm | (sm << 16), sl3 | (sl3 << 16));
+        *reinterpret_cast<uint4*>(dst + 128) = make_uint4(sl3, 0u, 0u, 0u);
+    }
+}
+
 // ---------------------------------------------------------------------- host
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -671,10 +748,10 @@ DeviceInfo device_info(int dev) {
 int g_inject_skip_stage = -1;
 unsigned long long g_timeout_cycles = 4000000000ull;  // ~2 s at 2 GHz
 
-template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS>
+template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS, bool PREX = false>
 cudaError_t launch_cfg(const CUtensorMap* maps, const TcParams& prm, int64_t grid, cudaStream_t stream) {
     using CF = Cfg<BN, NCONV, NEPI, S8, S16>;
-    auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SUMS>;
+    auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SUMS, PREX>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::kSmem);
     if (e != cudaSuccess) return e;
     // the register split adds up only if every thread was launched with 128 registers
@@ -783,6 +860,25 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
         maps[2] = maps[0];
         maps[3] = maps[1];
     }
+    // Pre-tiled X for the prompt shapes (X = A): converted once per call into a
+    // per-(device, stream) workspace, unless the caller allocates nothing or the
+    // workspace cannot be had now (stream capture); then the converter warps
+    // convert X in the kernel as for every other shape.
+    bool prex = false;
+    if (!SUMS && !swap && a.no_alloc == 0) {
+        const int64_t ns = a.K / KS;
+        const int64_t tp = (P + BM - 1) / BM;
+        void* xt = nullptr;
+        if (tp * ns <= 0x7fffffffLL &&
+            stream_workspace(stream, static_cast<size_t>(tp * ns) * kXtStage, &xt) == cudaSuccess) {
+            cudaError_t e0 = launch_pdl(tile_x_kernel, dim3(static_cast<unsigned>(tp * ns)), dim3(256), 0, stream,
+                                        a.A, a.AS, static_cast<uint8_t*>(xt), P, a.K);
+            if (e0 != cudaSuccess) return e0;
+            prm.xt = static_cast<const uint8_t*>(xt);
+            prm.xt_tile_stride = ns * kXtStage;
+            prex = true;
+        }
+    }
     cudaError_t e = cudaSuccess;
     if (prm.atomic) {
         e = cudaMemsetAsync(a.C, 0, static_cast<size_t>(a.M * a.N) * sizeof(float), stream);
@@ -793,7 +889,11 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
     // shared memory: three f16 stages measured ~11 % faster than two at every
     // shape (the converters run ahead of the MMA issuer), at the cost of int8
     // depth
-    if (!swap) return launch_cfg<128, 6, 8, 2, 3, 1, SUMS>(maps, prm, grid, stream);
+    if (!swap) {
+        if constexpr (!SUMS)
+            if (prex) return launch_cfg<128, 6, 8, 2, 3, 1, SUMS, true>(maps, prm, grid, stream);
+        return launch_cfg<128, 6, 8, 2, 3, 1, SUMS>(maps, prm, grid, stream);
+    }
     if (BN == 16) return launch_cfg<16, 6, 8, 5, 3, 1, SUMS>(maps, prm, grid, stream);
     if (BN == 32) return launch_cfg<32, 6, 8, 5, 3, 1, SUMS>(maps, prm, grid, stream);
     return launch_cfg<64, 6, 8, 4, 3, 1, SUMS>(maps, prm, grid, stream);
