@@ -20,7 +20,10 @@
  *
  *   Memory.  All tensors are row-major and dense (the innermost index is
  *   contiguous, no padding).  Every pointer is a DEVICE pointer owned by the
- *   caller; the library never frees it, keeps it, or allocates per call.
+ *   caller; the library never frees it or keeps it.  The only device memory
+ *   the library allocates is the workspace some entry points keep per device
+ *   or per stream (documented with each); it is allocated on first use and
+ *   grown on demand, never per call.
  *   Base alignment: int8 tensors (A, W, q) and f32 inputs read as vectors
  *   (x) start on a 16-byte boundary; the f32 scale planes and C on a 4-byte
  *   boundary.  (The pages ask 16 bytes of every tensor base, "Kernel ABI",
@@ -104,6 +107,16 @@ int pq_quantize_q8_0(const float* x, int8_t* q, float* s,
  * the example kernel's argument order A, AS, W, WS, C).  C is overwritten
  * (the pages' example assigns the result).  The kernel is chosen by M.
  * C must not overlap any input.
+ *
+ * Workspace (tensor-core path, M > 64): the activations are converted once
+ * per call, by a small kernel enqueued before the contraction, into a
+ * workspace that belongs to the (device, stream) pair.  It is allocated on
+ * the first such call on that stream and grown when a larger one arrives
+ * (cudaMalloc / cudaFree, which synchronize the device), and kept until
+ * exit.  A call made while its stream is being captured, whose workspace does
+ * not exist yet or is too small, allocates nothing and lets the kernel convert
+ * the activations itself (same results); so does
+ * pq_quantize_qdot_q8_0_noalloc, and so does every stream past the 64th.
  */
 int pq_qdot_q8_0(const int8_t* A, const float* AS, const int8_t* W, const float* WS,
                  float* C, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
@@ -129,9 +142,9 @@ int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const flo
  * quantizer feeding qdot_t that "Quantized built-ins and formats", section
  * "Q8_0", describes ("the activations are quantized the same way").  For one
  * row (M == 1) and N up to 64 x the SM count this is one kernel, in which
- * every CTA quantizes x into its shared memory while its weight stream is in
- * flight; otherwise it is the quantizer followed by qdot_t, launched so that
- * the second overlaps the first.  A [M, K] int8 and AS [M, K/32] f32
+ * every CTA quantizes x into its shared memory while L2 prefetches its weight
+ * rows, then streams them; otherwise it is the quantizer followed by qdot_t,
+ * launched so that the second overlaps the first.  A [M, K] int8 and AS [M, K/32] f32
  * optionally receive the quantized rows (both null, or both non-null).  When
  * they are null and the two-kernel route is taken, the rows go to a
  * per-device workspace that the library allocates on the first such call and
