@@ -585,7 +585,7 @@ def main(argv=None):
     if not args.no_others:
         for name in (PROMPT, "ffn_up_m1_k4096_n14336", "ffn_down_m1_k14336_n4096",
                      "smallm_m4_k4096_n11008", "smallm_m16_k4096_n11008", "smallm_m64_k4096_n11008",
-                     "q50_decode_m1_k4096_n4096"):
+                     "q50_decode_m1_k4096_n4096", "q50_prompt_m512_k4096_n14336"):
             if name == args.workload:
                 continue
             try:

@@ -234,6 +234,13 @@ int pq_q50_qdot(const int8_t* A, const float* AS, const uint8_t* W5, const float
     if (!aligned(A, 16) || !aligned(W5, 4) || !aligned(AS, 4) || !aligned(WS, 4) || !aligned(C, 4))
         return PQ_ERR_ALIGN;
     pq::QdotArgs a{A, AS, reinterpret_cast<const int8_t*>(W5), WS, C, nullptr, M, N, K, ws_layout};
+    // prompt shapes on the tensor cores (Q5_0 blocks decoded to f16 in the
+    // kernel); every other shape, and whatever that kernel declines (K not a
+    // multiple of 128, bases not 16-byte aligned), on the dp4a kernel
+    if (M > 64) {
+        cudaError_t e = pq::launch_qdot_tc_q50(a, stream);
+        if (e != cudaErrorNotSupported) return map_cuda(e);
+    }
     return map_cuda(pq::launch_qdot_q50(a, stream));
 }
 

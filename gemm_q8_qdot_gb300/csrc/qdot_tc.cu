@@ -84,6 +84,12 @@ constexpr int GROUP = 4;     // Q8_0 blocks per scale group (128 K, two stages)
 // its two Q8_0 blocks (128 rows x 16 bf16 each, K-major without swizzle).
 constexpr int kXtF16 = BM * KS * 2;
 constexpr int kXtStage = kXtF16 + 2 * BM * 32;
+// Q5_0 weight blocks ("Phobos Language Spec" section 10, Q5_0 row): 20 bytes per
+// 32 elements, the qh word then 16 bytes whose byte e holds element e in its low
+// nibble and element e + 16 in its high nibble, each element q - 16.  One scale
+// group (4 blocks, 128 K) of a row is 80 bytes.
+constexpr int kQ5Block = 20;
+constexpr int kQ5Row = GROUP * kQ5Block;
 
 struct TcParams {
     const float* xs;          // scale of MMA-A row p, block b: xs[p * xs_r + b * xs_b]
@@ -116,7 +122,7 @@ struct TcParams {
 // The f32 scales of the stage's 4 blocks arrive by TMA with the int8 tiles;
 // the converters turn them into the scale-product MMA's operands (exact 3-way
 // bf16 splits) in the f16 stage.
-template <int BN, int NCONV, int NEPI, int S8, int S16>
+template <int BN, int NCONV, int NEPI, int S8, int S16, bool Q5 = false>
 struct Cfg {
     static constexpr int kThreads = 32 * (2 + NCONV + NEPI);
     static constexpr int kE0 = 2 + NCONV;                 // first epilogue warp
@@ -126,7 +132,7 @@ struct Cfg {
     static constexpr int kCW = BN / (NEPI / 4);          // columns per epilogue warp
     static constexpr int kCH = kCW < 16 ? kCW : 16;       // columns per tcgen05.ld
     static constexpr int kX8 = BM * KS8;                  // int8 X tile bytes (one TMA box)
-    static constexpr int kY8 = BN * KS8;
+    static constexpr int kY8 = BN * (Q5 ? kQ5Row : KS8);  // Y tile of one scale group (int8 or Q5_0 blocks)
     static constexpr int kXS = BM * GROUP * 4;            // f32 scales of the stage's 4 blocks
     static constexpr int kYS = BN * GROUP * 4;
     static constexpr int kX16 = BM * KS * 2;              // f16 X tile bytes
@@ -152,6 +158,7 @@ struct Cfg {
     static_assert(NEPI == 8, "epilogue warps: two column halves over the four TMEM lane quadrants");
     static_assert(kCW % kCH == 0 && kCH % 8 == 0, "epilogue column chunks");
     static_assert(kX8 % 1024 == 0 && kY8 % 1024 == 0 && kX16 % 1024 == 0 && kY16 % 1024 == 0, "1024-B tiles");
+    static_assert(!Q5 || BN % 8 == 0, "Q5_0 weights: whole row octets");
     static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
@@ -205,6 +212,22 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
+// Q5_0: the four bits of x spread to bit 0 of four bytes (x * 0x00204081 puts
+// bit i at bit 8i, no carries), and four biased elements q in [0, 31] (one per
+// byte) -> two f16x2 of q - 16, exact (placed under the f16 exponent of 1024,
+// 1040 = 1024 + 16 subtracted).
+__device__ __forceinline__ uint32_t q5_spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
+
+__device__ __forceinline__ void q5_to_f16x4(uint32_t q, uint32_t& lo, uint32_t& hi) {
+    const uint32_t a = __byte_perm(q, 0x64646464u, 0x4140u);
+    const uint32_t b = __byte_perm(q, 0x64646464u, 0x4342u);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6410u), __ushort_as_half(0x6410u));
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&ha);
+    hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
 // Packed f32 pairs (low word first) and the sm_100+ paired FMA, each element
 // rounded as its scalar counterpart: one instruction for two accumulators.
 __device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
@@ -230,12 +253,12 @@ __device__ __forceinline__ void split3_bf16(float x, uint32_t& h, uint32_t& m, u
     l = __bfloat16_as_ushort(bl);
 }
 
-template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS, bool PREX>
-__global__ void __launch_bounds__(Cfg<BN, NCONV, NEPI, S8, S16>::kThreads, MINB)
+template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS, bool PREX, bool Q5>
+__global__ void __launch_bounds__(Cfg<BN, NCONV, NEPI, S8, S16, Q5>::kThreads, MINB)
 qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
                const __grid_constant__ CUtensorMap tmXS, const __grid_constant__ CUtensorMap tmYS,
                const TcParams prm) {
-    using CF = Cfg<BN, NCONV, NEPI, S8, S16>;
+    using CF = Cfg<BN, NCONV, NEPI, S8, S16, Q5>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::kOffBar);
@@ -345,7 +368,8 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         if (!PREX)
                             tc::tma_load_2d(smem + CF::kOffX8 + s8 * CF::kX8, &tmX, &full8[s8], g * KS8,
                                             static_cast<int>(un.p0));
-                        tc::tma_load_2d(smem + CF::kOffY8 + s8 * CF::kY8, &tmY, &full8[s8], g * KS8, static_cast<int>(un.q0));
+                        tc::tma_load_2d(smem + CF::kOffY8 + s8 * CF::kY8, &tmY, &full8[s8], g * (Q5 ? kQ5Row : KS8),
+                                        static_cast<int>(un.q0));
                         if (prm.has_scales) {
                             // row-major planes: box {4 blocks, rows}; block-major: box {rows, 4 blocks}
                             const int b0 = g * GROUP;
@@ -452,13 +476,16 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         const uint32_t x16 = sbase + CF::kOffX16 + s16 * CF::kX16;
                         const uint32_t y16 = sbase + CF::kOffY16 + s16 * CF::kY16;
                         const int c8 = h * 4 + c4;  // 16-byte chunk of the 128-byte int8 row
-                        // octets of rows converted per warp (Y rows only with pre-tiled X)
-                        constexpr int kOw = PREX ? (BN / 8 + NCONV - 1) / NCONV : CF::kOctPerWarp;
-                        uint4 v[kOw];
+                        // octets of int8 rows converted per warp (Y rows only with pre-tiled X;
+                        // X rows only with Q5_0 weights, which are decoded below)
+                        constexpr int kOctEnd = Q5 ? BM / 8 : CF::kOct;
+                        constexpr int kOw = PREX ? (Q5 ? 0 : (BN / 8 + NCONV - 1) / NCONV)
+                                                 : (kOctEnd + NCONV - 1) / NCONV;
+                        uint4 v[kOw > 0 ? kOw : 1];
 #pragma unroll
                         for (int t = 0; t < kOw; ++t) {  // all loads first
                             const int o = (PREX ? BM / 8 : 0) + cw + t * NCONV;
-                            if (o < CF::kOct) {
+                            if (o < kOctEnd) {
                                 const bool isx = o < BM / 8;
                                 const int row = (isx ? o : o - BM / 8) * 8 + r_in;
                                 v[t] = tc::lds128((isx ? x8 : y8) + row * KS8 + ((c8 ^ (row & 7)) << 4));
@@ -467,7 +494,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 #pragma unroll
                         for (int t = 0; t < kOw; ++t) {
                             const int o = (PREX ? BM / 8 : 0) + cw + t * NCONV;
-                            if (o < CF::kOct) {
+                            if (o < kOctEnd) {
                                 const bool isx = o < BM / 8;
                                 const int row = (isx ? o : o - BM / 8) * 8 + r_in;
                                 uint4 o0, o1;
@@ -478,6 +505,40 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                                 const uint32_t dst = (isx ? x16 : y16) + row * (KS * 2);
                                 tc::sts128(dst + (((2 * c4) ^ (row & 7)) << 4), o0);
                                 tc::sts128(dst + (((2 * c4 + 1) ^ (row & 7)) << 4), o1);
+                            }
+                        }
+                        if constexpr (Q5) {
+                            // Y = the Q5_0 weight: one (row, block) of this f16 stage per task; the
+                            // 32 elements (q - 16) become four 16-byte f16 chunks of the row
+                            constexpr int kTasks = (BN * 2 + NCONV * 32 - 1) / (NCONV * 32);
+#pragma unroll
+                            for (int t = 0; t < kTasks; ++t) {
+                                const int w = ct + t * NCONV * 32;
+                                if (w < BN * 2) {
+                                    const int row = w >> 1, bb = w & 1;
+                                    const uint32_t src = y8 + row * kQ5Row + (h * 2 + bb) * kQ5Block;
+                                    const uint32_t qh = tc::lds32(src);
+                                    uint32_t d[4];
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) d[i] = tc::lds32(src + 4 + 4 * i);
+                                    const uint32_t dst = y16 + row * (KS * 2);
+#pragma unroll
+                                    for (int c = 0; c < 4; ++c) {
+                                        // chunk c: elements 8c .. 8c + 7 = two words of biased bytes q in [0, 31]
+                                        uint32_t u[2];
+#pragma unroll
+                                        for (int hw = 0; hw < 2; ++hw) {
+                                            const int e0 = 8 * c + 4 * hw;  // first element of the word
+                                            const int i = (e0 & 15) >> 2;   // data word holding it
+                                            const uint32_t nib = e0 < 16 ? (d[i] & 0x0f0f0f0fu) : ((d[i] >> 4) & 0x0f0f0f0fu);
+                                            u[hw] = nib | (q5_spread4((qh >> e0) & 0xfu) << 4);
+                                        }
+                                        uint4 o;
+                                        q5_to_f16x4(u[0], o.x, o.y);
+                                        q5_to_f16x4(u[1], o.z, o.w);
+                                        tc::sts128(dst + (((bb * 4 + c) ^ (row & 7)) << 4), o);
+                                    }
+                                }
                             }
                         }
                         // scale-product operands of this f16 stage's two blocks: row r, block bb ->
@@ -706,6 +767,20 @@ bool make_i8_map(CUtensorMap* map, const int8_t* base, int64_t rows, int64_t K, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q5_0 weight rows [rows, K/32 * 20] bytes, box {80 bytes = one scale group,
+// box_rows}, no swizzle, zero fill outside (ragged rows read as 0).
+bool make_q5_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t row_bytes, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kQ5Row), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // f32 plane [outer, inner] with the given row stride in bytes, box {box_inner,
 // box_outer}, no swizzle, zero fill outside.
 bool make_f32_map(CUtensorMap* map, const float* base, int64_t inner, int64_t outer, int64_t stride_bytes,
@@ -748,10 +823,10 @@ DeviceInfo device_info(int dev) {
 int g_inject_skip_stage = -1;
 unsigned long long g_timeout_cycles = 4000000000ull;  // ~2 s at 2 GHz
 
-template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS, bool PREX = false>
+template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS, bool PREX = false, bool Q5 = false>
 cudaError_t launch_cfg(const CUtensorMap* maps, const TcParams& prm, int64_t grid, cudaStream_t stream) {
-    using CF = Cfg<BN, NCONV, NEPI, S8, S16>;
-    auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SUMS, PREX>;
+    using CF = Cfg<BN, NCONV, NEPI, S8, S16, Q5>;
+    auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SUMS, PREX, Q5>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::kSmem);
     if (e != cudaSuccess) return e;
     // the register split adds up only if every thread was launched with 128 registers
@@ -765,7 +840,9 @@ cudaError_t launch_cfg(const CUtensorMap* maps, const TcParams& prm, int64_t gri
                       stream, maps[0], maps[1], maps[2], maps[3], p);
 }
 
-template <bool SUMS>
+// Q5 = true: a.W holds Q5_0 weight blocks [N, K/32 * 20] bytes (q50_qdot_t);
+// only the prompt layout (M > 64, X = A, Y = W) and not in block-sum mode.
+template <bool SUMS, bool Q5 = false>
 cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorNotSupported;
@@ -775,6 +852,7 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
     if (a.K > 0x7fffffffLL || a.M > 0x7fffffffLL || a.N > 0x7fffffffLL) return cudaErrorNotSupported;
     const int64_t KB = a.K / 32;
     const bool swap = a.M <= 64;
+    if (Q5 && (SUMS || swap || (reinterpret_cast<uintptr_t>(a.W) & 15u) != 0)) return cudaErrorNotSupported;
     TcParams prm{};
     const int64_t P = swap ? a.N : a.M;
     const int64_t Q = swap ? a.M : a.N;
@@ -833,7 +911,10 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
     CUtensorMap maps[4];
     const int8_t* X = swap ? a.W : a.A;
     const int8_t* Y = swap ? a.A : a.W;
-    if (!make_i8_map(&maps[0], X, P, a.K, BM) || !make_i8_map(&maps[1], Y, Q, a.K, BN)) return cudaErrorInvalidValue;
+    if (!make_i8_map(&maps[0], X, P, a.K, BM)) return cudaErrorInvalidValue;
+    if (Q5 ? !make_q5_map(&maps[1], reinterpret_cast<const uint8_t*>(Y), Q, KB * kQ5Block, BN)
+           : !make_i8_map(&maps[1], Y, Q, a.K, BN))
+        return cudaErrorInvalidValue;
     prm.has_scales = SUMS ? 0 : 1;
     if (!SUMS) {
         // scale planes by TMA: rows of 16-byte multiples from a 16-byte aligned base
@@ -889,6 +970,10 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
     // shared memory: three f16 stages measured ~11 % faster than two at every
     // shape (the converters run ahead of the MMA issuer), at the cost of int8
     // depth
+    if constexpr (Q5) {
+        if (prex) return launch_cfg<128, 6, 8, 2, 3, 1, false, true, true>(maps, prm, grid, stream);
+        return launch_cfg<128, 6, 8, 2, 3, 1, false, false, true>(maps, prm, grid, stream);
+    }
     if (!swap) {
         if constexpr (!SUMS)
             if (prex) return launch_cfg<128, 6, 8, 2, 3, 1, SUMS, true>(maps, prm, grid, stream);
@@ -903,6 +988,11 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream) {
     return a.S != nullptr ? launch_tc<true>(a, stream) : launch_tc<false>(a, stream);
+}
+
+cudaError_t launch_qdot_tc_q50(const QdotArgs& a, cudaStream_t stream) {
+    if (a.S != nullptr) return cudaErrorNotSupported;
+    return launch_tc<false, true>(a, stream);
 }
 
 cudaError_t read_and_clear_status(unsigned* status) {

@@ -69,6 +69,8 @@ WORKLOADS = {
     "smallm_m64_k4096_n11008": Workload("smallm_m64_k4096_n11008", 64, 11008, 4096, 3, x_dist="row_loguniform"),
     "prompt_m512_k4096_n14336": Workload("prompt_m512_k4096_n14336", 512, 14336, 4096, 4, x_dist="outlier_channels"),
     "q50_decode_m1_k4096_n4096": Workload("q50_decode_m1_k4096_n4096", 1, 4096, 4096, 5, w_format="q5_0"),
+    "q50_prompt_m512_k4096_n14336": Workload("q50_prompt_m512_k4096_n14336", 512, 14336, 4096, 6,
+                                             x_dist="outlier_channels", w_format="q5_0"),
 }
 
 # the workloads whose weights are Q8_0 (qdot_t proper)

@@ -99,3 +99,71 @@ def test_q50_workload_full(pq):
     out, bound = oracle.qdot_q5_0(qa, sa, w5[cols], ws[cols])
     within(C[:, torch.from_numpy(cols).to(DEV)], out, bound, "q50 decode full size")
     assert torch.isfinite(C).all()
+
+
+# ------------------------------------------------------------ tensor-core route (M > 64)
+
+TC_SHAPES = [(65, 64, 128), (130, 300, 512), (256, 129, 1024), (512, 256, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", TC_SHAPES)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_q50_qdot_tensor_cores(pq, M, N, K, layout):
+    """Prompt shapes take the tensor-core kernel, which decodes the Q5_0 blocks to f16 in
+    shared memory (ragged N, both scale layouts, split K at the small shapes)."""
+    a, a_s, w5, w_s = operands(M * 11 + N + K + layout, M, N, K)
+    ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+    out, bound = oracle.qdot_q5_0(a, a_s, w5, ws, ws_layout=layout)
+    C = pq.q50_qdot(dev(a), dev(a_s), dev(w5), dev(ws), ws_layout=layout)
+    pq.check_device()
+    within(C, out, bound, f"q50 tc M={M} N={N} K={K} layout={layout}")
+
+
+def test_q50_tensor_cores_under_capture(pq):
+    """Captured on a stream without a workspace yet: the kernel converts the activations
+    itself; the replay is within tolerance."""
+    M, N, K = 128, 192, 512
+    a, a_s, w5, w_s = operands(5, M, N, K)
+    out, bound = oracle.qdot_q5_0(a, a_s, w5, w_s)
+    A, AS, W5, WS = dev(a), dev(a_s), dev(w5), dev(w_s)
+    C = torch.full((M, N), float("nan"), device=DEV)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        pq.q50_qdot(A, AS, W5, WS, C)
+    g.replay()
+    torch.cuda.synchronize()
+    pq.check_device()
+    within(C, out, bound, "q50 tc captured")
+
+
+def test_q50_prompt_unaligned_weights_fall_back(pq):
+    """W5 only 4-byte aligned at a prompt shape: the tensor-core kernel declines (TMA wants 16
+    bytes) and the dp4a kernel gives the same result."""
+    M, N, K = 96, 40, 256
+    a, a_s, w5, w_s = operands(123, M, N, K)
+    out, bound = oracle.qdot_q5_0(a, a_s, w5, w_s)
+    buf = torch.zeros(w5.size + 64, dtype=torch.uint8, device=DEV)
+    view = buf[4:4 + w5.size].view(N, K // 32 * 20)
+    view.copy_(dev(w5))
+    C = pq.q50_qdot(dev(a), dev(a_s), view, dev(w_s))
+    pq.check_device()
+    within(C, out, bound, "q50 offset W5, prompt shape")
+
+
+def test_q50_prompt_workload_full(pq):
+    """The Q5_0 prompt workload at full size through the tensor cores: sampled rows and columns."""
+    wl = workloads.WORKLOADS["q50_prompt_m512_k4096_n14336"]
+    x = workloads.activations(wl)
+    qa, sa = oracle.quantize_q8_0(x)
+    w5, ws = workloads.q50_weights(wl)
+    C = pq.q50_qdot(dev(qa), dev(sa), dev(w5), dev(ws))
+    pq.check_device()
+    rng = np.random.default_rng(4)
+    rows = np.sort(rng.choice(wl.M, 96, replace=False))
+    cols = np.sort(rng.choice(wl.N, 256, replace=False))
+    out, bound = oracle.qdot_q5_0(qa[rows], sa[rows], w5[cols], ws[cols])
+    sub = C[torch.from_numpy(rows).to(DEV)][:, torch.from_numpy(cols).to(DEV)]
+    within(sub, out, bound, "q50 prompt full size")
+    assert torch.isfinite(C).all()
