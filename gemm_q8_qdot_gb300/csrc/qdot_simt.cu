@@ -38,6 +38,11 @@ namespace pq {
 namespace {
 
 constexpr int kWarps = 8;
+// bytes of each weight row a CTA asks L2 to prefetch before griddepcontrol.wait
+// (GB300, graphs of back-to-back steps: at K = 14336, 4 KB per row gives 14.0 us
+// per fused decode step against 15.1 us with whole rows, and 13.6 us against
+// 16.4 us for qdot_t alone; at K = 4096 it is the whole row either way)
+constexpr int64_t kPrefetchBytes = 4096;
 #ifndef PQ_FUSED_WARPS
 #define PQ_FUSED_WARPS 32
 #endif
@@ -54,12 +59,15 @@ qdot_simt_kernel(QdotArgs p) {
     pdl_trigger();
     if (j0 >= N) return;  // warp-uniform; no CTA-wide synchronisation below
     if (lane < COLS && j0 + lane < N) {
-        // one bulk L2 prefetch per weight row (K bytes) and scale row; rows of a
-        // 16-byte aligned base stay 16-byte aligned since K % 32 == 0
-        prefetch_l2(p.W + (j0 + lane) * K, static_cast<uint32_t>(K < (int64_t(1) << 30) ? K : (int64_t(1) << 30)));
-        if (WSL == 0 && !SUMS && (KB * 4) % 16 == 0 &&
+        // one bulk L2 prefetch per weight row and scale row, of the row's first
+        // kPrefetchBytes (whole rows up to K = 4096; prefetching whole long rows,
+        // K = 14336, measured slower); rows of a 16-byte aligned base stay 16-byte
+        // aligned since K % 32 == 0
+        const int64_t kb = K < kPrefetchBytes ? K : kPrefetchBytes;
+        prefetch_l2(p.W + (j0 + lane) * K, static_cast<uint32_t>(kb));
+        if (WSL == 0 && !SUMS && (kb / 32 * 4) % 16 == 0 &&
             (reinterpret_cast<uintptr_t>(p.WS + (j0 + lane) * KB) & 15) == 0)
-            prefetch_l2(p.WS + (j0 + lane) * KB, static_cast<uint32_t>(KB * 4));
+            prefetch_l2(p.WS + (j0 + lane) * KB, static_cast<uint32_t>(kb / 32 * 4));
     }
     pdl_wait();
 
@@ -181,8 +189,8 @@ cudaError_t launch_by_m(const QdotArgs& a, bool v8, cudaStream_t stream) {
 // Order of the memory traffic (measured on GB300 in a graph of back-to-back
 // steps at K = 4096, N = 4096: 4.7 us per step, against 5.6 us with the weight
 // loads issued before x):
-//   1. before griddepcontrol.wait the CTA asks L2 to prefetch its weight rows
-//      (a hint that cannot return stale data);
+//   1. before griddepcontrol.wait the CTA asks L2 to prefetch the first 4 KB
+//      of its weight rows (a hint that cannot return stale data);
 //   2. after it, the CTA loads x first: x is small and sits in L2, and its
 //      loads do not queue behind the CTA's own 128 KB of weight loads;
 //   3. the first round of weight loads is issued once the first round of x is
@@ -207,9 +215,12 @@ qdot_fused_kernel(FusedArgs p) {
     const int8_t* wrow = p.W + (jv ? j : 0) * K;
 
     if (lane == 0 && jv) {
-        prefetch_l2(wrow, static_cast<uint32_t>(K < (int64_t(1) << 30) ? K : (int64_t(1) << 30)));
-        if (WSL == 0 && (KB * 4) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.WS + j * KB) & 15) == 0)
-            prefetch_l2(p.WS + j * KB, static_cast<uint32_t>(KB * 4));
+        // the row's first kPrefetchBytes (the whole row up to K = 4096):
+        // prefetching whole long rows (K = 14336) measured slower than this
+        const int64_t kb = K < kPrefetchBytes ? K : kPrefetchBytes;
+        prefetch_l2(wrow, static_cast<uint32_t>(kb));
+        if (WSL == 0 && (reinterpret_cast<uintptr_t>(p.WS + j * KB) & 15) == 0 && (kb / 32 * 4) % 16 == 0)
+            prefetch_l2(p.WS + j * KB, static_cast<uint32_t>(kb / 32 * 4));
     }
     pdl_wait();
 
