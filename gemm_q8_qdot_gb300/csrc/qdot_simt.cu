@@ -31,6 +31,8 @@
 //
 // SUMS = true instead stores every block sum S[i, j, b] as int32 (the
 // verification entry point pq_qdot_q8_0_blocksums).
+#include <atomic>
+
 #include "pq_internal.h"
 #include "pq_device.cuh"
 
@@ -302,8 +304,20 @@ cudaError_t launch_fused(const FusedArgs& a, bool v8, cudaStream_t stream) {
     const int64_t grid = (a.N + NW - 1) / NW;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     auto kern = v8 ? qdot_fused_kernel<U, true, WSL, NW> : qdot_fused_kernel<U, false, WSL, NW>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
+    // beyond the default 48 KB of dynamic shared memory (K > 43690) the kernel's
+    // limit is raised once for the largest size met (it is per function, not per call)
+    if (smem > 48 * 1024) {
+        static std::atomic<int> raised[64][2];  // per device (the attribute is set in its context)
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorNotSupported;
+        std::atomic<int>& r = raised[dev][v8 ? 1 : 0];
+        if (static_cast<int>(smem) > r.load()) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+            r.store(static_cast<int>(smem));
+        }
+    }
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NW * 32), smem, stream, a);
 }
 
@@ -312,10 +326,16 @@ cudaError_t launch_fused(const FusedArgs& a, bool v8, cudaStream_t stream) {
 cudaError_t launch_qdot_fused(const FusedArgs& a, cudaStream_t stream) {
     // one row (the decode step), at most two waves of CTAs (one 1024-thread CTA per SM)
     if (a.M != 1) return cudaErrorNotSupported;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNotSupported;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        return cudaErrorNotSupported;
+    // the SM count of each device, queried once
+    static std::atomic<int> sm_count[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorNotSupported;
+    int sms = sm_count[dev].load(std::memory_order_relaxed);
+    if (sms <= 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            return cudaErrorNotSupported;
+        sm_count[dev].store(sms, std::memory_order_relaxed);
+    }
     if ((a.N + kFusedWarps - 1) / kFusedWarps > 2 * static_cast<int64_t>(sms)) return cudaErrorNotSupported;
     const bool v8 = (reinterpret_cast<uintptr_t>(a.W) & 31u) == 0;
     return a.ws_layout == 0 ? launch_fused<4, 0>(a, v8, stream) : launch_fused<4, 1>(a, v8, stream);
