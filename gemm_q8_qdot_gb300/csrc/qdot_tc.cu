@@ -122,23 +122,30 @@ struct TcParams {
 // The f32 scales of the stage's 4 blocks arrive by TMA with the int8 tiles;
 // the converters turn them into the scale-product MMA's operands (exact 3-way
 // bf16 splits) in the f16 stage.
-template <int BN, int NCONV, int NEPI, int S8, int S16, bool Q5 = false>
+//
+// ESC (narrow tiles): no scale-product MMA.  A TMEM buffer holds the block sums
+// of one scale group (4 blocks x BN columns) and the epilogue multiplies them by
+// the two f32 scales, read from the group's int8 stage, which it releases.
+template <int BN, int NCONV, int NEPI, int S8, int S16, bool Q5 = false, bool ESC = false>
 struct Cfg {
     static constexpr int kThreads = 32 * (2 + NCONV + NEPI);
     static constexpr int kE0 = 2 + NCONV;                 // first epilogue warp
-    static constexpr int kNbuf = (256 / BN) < 4 ? (256 / BN) : 4;  // TMEM buffers of S and P
-    static constexpr int kTmemCols = (2 * kNbuf * BN <= 32) ? 32 : (2 * kNbuf * BN <= 64) ? 64
-                                     : (2 * kNbuf * BN <= 128) ? 128 : (2 * kNbuf * BN <= 256) ? 256 : 512;
+    static constexpr int kBufCols = ESC ? GROUP * BN : 2 * BN;  // TMEM columns per buffer
+    static constexpr int kNbufMax = ESC ? 3 : 4;
+    static constexpr int kNbuf = (512 / kBufCols) < kNbufMax ? (512 / kBufCols) : kNbufMax;  // TMEM buffers
+    static constexpr int kTmemUsed = kNbuf * kBufCols;
+    static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+                                     : kTmemUsed <= 256 ? 256 : 512;
     static constexpr int kCW = BN / (NEPI / 4);          // columns per epilogue warp
-    static constexpr int kCH = kCW < 16 ? kCW : 16;       // columns per tcgen05.ld
+    static constexpr int kCH = kCW < (ESC ? 8 : 16) ? kCW : (ESC ? 8 : 16);  // columns per tcgen05.ld
     static constexpr int kX8 = BM * KS8;                  // int8 X tile bytes (one TMA box)
     static constexpr int kY8 = BN * (Q5 ? kQ5Row : KS8);  // Y tile of one scale group (int8 or Q5_0 blocks)
     static constexpr int kXS = BM * GROUP * 4;            // f32 scales of the stage's 4 blocks
     static constexpr int kYS = BN * GROUP * 4;
     static constexpr int kX16 = BM * KS * 2;              // f16 X tile bytes
     static constexpr int kY16 = BN * KS * 2;
-    static constexpr int kXP = BM * 32;                   // scale-product operand, one block: [rows][16] bf16
-    static constexpr int kYP = BN * 32;
+    static constexpr int kXP = ESC ? 0 : BM * 32;         // scale-product operand, one block: [rows][16] bf16
+    static constexpr int kYP = ESC ? 0 : BN * 32;
     static constexpr int kOffX8 = 0;
     static constexpr int kOffY8 = kOffX8 + S8 * kX8;
     static constexpr int kOffX16 = kOffY8 + S8 * kY8;
@@ -160,6 +167,7 @@ struct Cfg {
     static_assert(kX8 % 1024 == 0 && kY8 % 1024 == 0 && kX16 % 1024 == 0 && kY16 % 1024 == 0, "1024-B tiles");
     static_assert(!Q5 || BN % 8 == 0, "Q5_0 weights: whole row octets");
     static_assert(kSmem <= 227 * 1024, "shared memory");
+    static_assert(!ESC || !Q5, "scales in the epilogue: Q8_0 weights only");
 };
 
 __device__ __forceinline__ void set_abort(volatile int* abort_flag) {
@@ -241,6 +249,12 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
     return r;
 }
 
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // Exact split of an f32 into three bf16 whose sum is the value (normal range).
 __device__ __forceinline__ void split3_bf16(float x, uint32_t& h, uint32_t& m, uint32_t& l) {
     const __nv_bfloat16 bh = __float2bfloat16_rn(x);
@@ -253,12 +267,13 @@ __device__ __forceinline__ void split3_bf16(float x, uint32_t& h, uint32_t& m, u
     l = __bfloat16_as_ushort(bl);
 }
 
-template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS, bool PREX, bool Q5>
-__global__ void __launch_bounds__(Cfg<BN, NCONV, NEPI, S8, S16, Q5>::kThreads, MINB)
+template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS, bool PREX, bool Q5, bool ESC>
+__global__ void __launch_bounds__(Cfg<BN, NCONV, NEPI, S8, S16, Q5, ESC>::kThreads, MINB)
 qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
                const __grid_constant__ CUtensorMap tmXS, const __grid_constant__ CUtensorMap tmYS,
                const TcParams prm) {
-    using CF = Cfg<BN, NCONV, NEPI, S8, S16, Q5>;
+    using CF = Cfg<BN, NCONV, NEPI, S8, S16, Q5, ESC>;
+    static_assert(!ESC || (!SUMS && !PREX), "scales in the epilogue: scaled output, in-kernel X");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::kOffBar);
@@ -300,7 +315,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S8; ++i) {
             tc::mbar_init(&full8[i], 1);
-            tc::mbar_init(&empty8[i], NCONV);
+            tc::mbar_init(&empty8[i], NCONV + (ESC ? NEPI : 0));  // ESC: + the epilogue's reads of the scales
         }
         for (int i = 0; i < S16; ++i) {
             tc::mbar_init(&full16[i], NCONV + (PREX ? 1 : 0));  // + the producer's copy of pre-tiled X
@@ -410,7 +425,8 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_f16_f32(BM, BN);
             constexpr uint32_t idesc_p = tc::idesc_bf16_f32(BM, BN);
-            int g = 0, gi = 0;
+            int g = 0, gi = 0;  // g: TMEM hand-offs (blocks, or ESC scale groups)
+            bool gok = false;   // ESC: the group's buffer was free
             for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
                 const int nst = unit(u).nst;
                 for (int i = 0; i < nst; ++i, ++gi) {
@@ -419,25 +435,51 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     if (ok) tc::tc_fence_after_sync();
                     const uint32_t xa = sbase + CF::kOffX16 + s * CF::kX16;
                     const uint32_t ya = sbase + CF::kOffY16 + s * CF::kY16;
-#pragma unroll
-                    for (int bb = 0; bb < 2; ++bb, ++g) {
+                    if constexpr (ESC) {
+                        // this f16 stage holds blocks 2h and 2h + 1 of the group (units start
+                        // at group boundaries): their block sums go to columns (2h + bb) * BN
+                        // of the group's buffer, handed to the epilogue after the second half
+                        const int h = i & 1;
                         const int buf = g % CF::kNbuf;
-                        if (!ok || !bounded_wait(&tempty[buf], ((g / CF::kNbuf) & 1) ^ 1, abort_flag, limit))
-                            continue;
-                        tc::tc_fence_after_sync();
-                        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * 2 * BN);
+                        if (h == 0) gok = ok && bounded_wait(&tempty[buf], ((g / CF::kNbuf) & 1) ^ 1, abort_flag, limit);
+                        if (ok && gok) {
+                            tc::tc_fence_after_sync();
 #pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            const uint32_t koff = static_cast<uint32_t>((bb * 2 + kk) * 32);  // 16 f16 = 32 B
-                            tc::umma_f16(d, tc::sw128_kmajor_desc(xa + koff), tc::sw128_kmajor_desc(ya + koff),
-                                         idesc, kk);
+                            for (int bb = 0; bb < 2; ++bb) {
+                                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * CF::kBufCols + (h * 2 + bb) * BN);
+#pragma unroll
+                                for (int kk = 0; kk < 2; ++kk) {
+                                    const uint32_t koff = static_cast<uint32_t>((bb * 2 + kk) * 32);
+                                    tc::umma_f16(d, tc::sw128_kmajor_desc(xa + koff), tc::sw128_kmajor_desc(ya + koff),
+                                                 idesc, kk);
+                                }
+                            }
                         }
-                        // P = (split xs) . (split ys)^T: the scale products of this block
-                        const uint32_t xp = sbase + CF::kOffXP + (s * 2 + bb) * CF::kXP;
-                        const uint32_t yp = sbase + CF::kOffYP + (s * 2 + bb) * CF::kYP;
-                        tc::umma_f16(d + BN, tc::noswz_kmajor_desc(xp, 128, 256), tc::noswz_kmajor_desc(yp, 128, 256),
-                                     idesc_p, 0);
-                        tc::umma_commit(&tfull[buf]);
+                        if (h == 1) {
+                            if (gok) tc::umma_commit(&tfull[buf]);
+                            ++g;
+                        }
+                    } else {
+#pragma unroll
+                        for (int bb = 0; bb < 2; ++bb, ++g) {
+                            const int buf = g % CF::kNbuf;
+                            if (!ok || !bounded_wait(&tempty[buf], ((g / CF::kNbuf) & 1) ^ 1, abort_flag, limit))
+                                continue;
+                            tc::tc_fence_after_sync();
+                            const uint32_t d = tmem_base + static_cast<uint32_t>(buf * 2 * BN);
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                const uint32_t koff = static_cast<uint32_t>((bb * 2 + kk) * 32);  // 16 f16 = 32 B
+                                tc::umma_f16(d, tc::sw128_kmajor_desc(xa + koff), tc::sw128_kmajor_desc(ya + koff),
+                                             idesc, kk);
+                            }
+                            // P = (split xs) . (split ys)^T: the scale products of this block
+                            const uint32_t xp = sbase + CF::kOffXP + (s * 2 + bb) * CF::kXP;
+                            const uint32_t yp = sbase + CF::kOffYP + (s * 2 + bb) * CF::kYP;
+                            tc::umma_f16(d + BN, tc::noswz_kmajor_desc(xp, 128, 256), tc::noswz_kmajor_desc(yp, 128, 256),
+                                         idesc_p, 0);
+                            tc::umma_commit(&tfull[buf]);
+                        }
                     }
                     // release the f16 stage once its MMAs completed
                     tc::umma_commit(&empty16[s]);
@@ -545,7 +587,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         // 16 bf16 [h h h m m m l l l 0..] (X) or [h m l h m l h m l 0..] (Y),
                         // K-major without swizzle: 8-row x 16-byte core matrices, the two
                         // K halves 128 B apart, 8-row groups 256 B apart
-                        constexpr int kSp = PREX ? (BN * 2 + NCONV * 32 - 1) / (NCONV * 32) : CF::kSplitPerThread;
+                        constexpr int kSp = ESC ? 0 : PREX ? (BN * 2 + NCONV * 32 - 1) / (NCONV * 32) : CF::kSplitPerThread;
 #pragma unroll
                         for (int t = 0; t < kSp; ++t) {
                             const int w = ct + t * NCONV * 32;
@@ -603,48 +645,111 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             const int nblk = cu.nst * 2;
             const int64_t p = cu.p0 + prow;
             const bool pv = p < prm.P;
-            for (int k = 0; k < nblk; ++k, ++g) {
-                const int buf = g % CF::kNbuf;
-                int ok = 0;
-                if (lane == 0) ok = bounded_wait(&tfull[buf], (g / CF::kNbuf) & 1, abort_flag, limit);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) continue;
-                tc::tc_fence_after_sync();
-                const uint32_t ts = t_lane + static_cast<uint32_t>(buf * 2 * BN + cb);
-                if constexpr (SUMS) {
-                    const int64_t b = static_cast<int64_t>(cu.g_begin) * GROUP + k;
+            if constexpr (ESC) {
+                // one hand-off per scale group: block sums S_b (b = 0..3) in columns b * BN of the
+                // buffer; out += (xs[p, b] * ys[q, b]) * S_b[p, q] with both scales read from the
+                // group's int8 stage, released here once they are read
+                for (int k = 0; k < cu.nst / 2; ++k, ++g) {
+                    const int buf = g % CF::kNbuf;
+                    const int s8 = g % S8;
+                    int ok = 0;
+                    if (lane == 0) ok = bounded_wait(&tfull[buf], (g / CF::kNbuf) & 1, abort_flag, limit);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) continue;
+                    tc::tc_fence_after_sync();
+                    const uint32_t xs8 = sbase + CF::kOffXS + s8 * CF::kXS;
+                    const uint32_t ys8 = sbase + CF::kOffYS + s8 * CF::kYS;
+                    float4 xv;  // xs[p, b] for the group's four blocks
+                    if (prm.xs_sb == 1) {
+                        xv = tc::lds128f(xs8 + prow * (GROUP * 4));
+                    } else {
+                        xv.x = tc::lds32f(xs8 + (prow * prm.xs_sr + 0 * prm.xs_sb) * 4);
+                        xv.y = tc::lds32f(xs8 + (prow * prm.xs_sr + 1 * prm.xs_sb) * 4);
+                        xv.z = tc::lds32f(xs8 + (prow * prm.xs_sr + 2 * prm.xs_sb) * 4);
+                        xv.w = tc::lds32f(xs8 + (prow * prm.xs_sr + 3 * prm.xs_sb) * 4);
+                    }
+                    const uint64_t x0 = f2_pack(__float_as_uint(xv.x), __float_as_uint(xv.x));
+                    const uint64_t x1 = f2_pack(__float_as_uint(xv.y), __float_as_uint(xv.y));
+                    const uint64_t x2 = f2_pack(__float_as_uint(xv.z), __float_as_uint(xv.z));
+                    const uint64_t x3 = f2_pack(__float_as_uint(xv.w), __float_as_uint(xv.w));
+                    const uint32_t ts = t_lane + static_cast<uint32_t>(buf * CF::kBufCols + cb);
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) {
-                        uint32_t sv[CF::kCH];
-                        tc::TmemLd<CF::kCH>::load(ts + c * CF::kCH, sv);
-                        tc::TmemLd<CF::kCH>::wait(sv);
-                        if (pv) {
+                        uint32_t sv[GROUP][CF::kCH];
 #pragma unroll
-                            for (int t = 0; t < CF::kCH; ++t) {
-                                const int64_t q = cu.q0 + cb + c * CF::kCH + t;
-                                if (q < prm.Q)
-                                    prm.S[p * prm.sp + q * prm.sq + b] = static_cast<int32_t>(__uint_as_float(sv[t]));
+                        for (int b = 0; b < GROUP; ++b) tc::TmemLd<CF::kCH>::load(ts + b * BN + c * CF::kCH, sv[b]);
+#pragma unroll
+                        for (int b = 0; b < GROUP; ++b) tc::TmemLd<CF::kCH>::wait(sv[b]);
+#pragma unroll
+                        for (int t = 0; t < CF::kCH; t += 2) {
+                            // ys[q, 0..3] of columns q, q + 1: one row of the [BN][4] scale tile each
+                            const int q = cb + c * CF::kCH + t;
+                            const float4 y0 = tc::lds128f(ys8 + q * (GROUP * 4));
+                            const float4 y1 = tc::lds128f(ys8 + (q + 1) * (GROUP * 4));
+                            const int a = (c * CF::kCH + t) / 2;
+                            uint64_t r = acc[a];
+                            r = f2_fma(f2_mul(x0, f2_pack(__float_as_uint(y0.x), __float_as_uint(y1.x))),
+                                       f2_pack(sv[0][t], sv[0][t + 1]), r);
+                            r = f2_fma(f2_mul(x1, f2_pack(__float_as_uint(y0.y), __float_as_uint(y1.y))),
+                                       f2_pack(sv[1][t], sv[1][t + 1]), r);
+                            r = f2_fma(f2_mul(x2, f2_pack(__float_as_uint(y0.z), __float_as_uint(y1.z))),
+                                       f2_pack(sv[2][t], sv[2][t + 1]), r);
+                            r = f2_fma(f2_mul(x3, f2_pack(__float_as_uint(y0.w), __float_as_uint(y1.w))),
+                                       f2_pack(sv[3][t], sv[3][t + 1]), r);
+                            acc[a] = r;
+                        }
+                    }
+                    tc::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tc::mbar_arrive(&tempty[buf]);
+                        tc::mbar_arrive(&empty8[s8]);
+                    }
+                }
+            } else {
+                for (int k = 0; k < nblk; ++k, ++g) {
+                    const int buf = g % CF::kNbuf;
+                    int ok = 0;
+                    if (lane == 0) ok = bounded_wait(&tfull[buf], (g / CF::kNbuf) & 1, abort_flag, limit);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) continue;
+                    tc::tc_fence_after_sync();
+                    const uint32_t ts = t_lane + static_cast<uint32_t>(buf * 2 * BN + cb);
+                    if constexpr (SUMS) {
+                        const int64_t b = static_cast<int64_t>(cu.g_begin) * GROUP + k;
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) {
+                            uint32_t sv[CF::kCH];
+                            tc::TmemLd<CF::kCH>::load(ts + c * CF::kCH, sv);
+                            tc::TmemLd<CF::kCH>::wait(sv);
+                            if (pv) {
+#pragma unroll
+                                for (int t = 0; t < CF::kCH; ++t) {
+                                    const int64_t q = cu.q0 + cb + c * CF::kCH + t;
+                                    if (q < prm.Q)
+                                        prm.S[p * prm.sp + q * prm.sq + b] = static_cast<int32_t>(__uint_as_float(sv[t]));
+                                }
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) {
+                            uint32_t sv[CF::kCH], pvv[CF::kCH];
+                            tc::TmemLd<CF::kCH>::load(ts + c * CF::kCH, sv);
+                            tc::TmemLd<CF::kCH>::load(ts + BN + c * CF::kCH, pvv);
+                            tc::TmemLd<CF::kCH>::wait(sv);
+                            tc::TmemLd<CF::kCH>::wait(pvv);
+#pragma unroll
+                            for (int t = 0; t < CF::kCH; t += 2) {
+                                const int a = (c * CF::kCH + t) / 2;
+                                acc[a] = f2_fma(f2_pack(pvv[t], pvv[t + 1]), f2_pack(sv[t], sv[t + 1]), acc[a]);
                             }
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        uint32_t sv[CF::kCH], pvv[CF::kCH];
-                        tc::TmemLd<CF::kCH>::load(ts + c * CF::kCH, sv);
-                        tc::TmemLd<CF::kCH>::load(ts + BN + c * CF::kCH, pvv);
-                        tc::TmemLd<CF::kCH>::wait(sv);
-                        tc::TmemLd<CF::kCH>::wait(pvv);
-#pragma unroll
-                        for (int t = 0; t < CF::kCH; t += 2) {
-                            const int a = (c * CF::kCH + t) / 2;
-                            acc[a] = f2_fma(f2_pack(pvv[t], pvv[t + 1]), f2_pack(sv[t], sv[t + 1]), acc[a]);
-                        }
-                    }
+                    tc::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&tempty[buf]);
                 }
-                tc::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&tempty[buf]);
             }
             if constexpr (!SUMS) {
                 // the unit's last block: write its tile and start the next from zero
@@ -823,10 +928,11 @@ DeviceInfo device_info(int dev) {
 int g_inject_skip_stage = -1;
 unsigned long long g_timeout_cycles = 4000000000ull;  // ~2 s at 2 GHz
 
-template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS, bool PREX = false, bool Q5 = false>
+template <int BN, int NCONV, int NEPI, int S8, int S16, int MINB, bool SUMS, bool PREX = false, bool Q5 = false,
+          bool ESC = false>
 cudaError_t launch_cfg(const CUtensorMap* maps, const TcParams& prm, int64_t grid, cudaStream_t stream) {
-    using CF = Cfg<BN, NCONV, NEPI, S8, S16, Q5>;
-    auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SUMS, PREX, Q5>;
+    using CF = Cfg<BN, NCONV, NEPI, S8, S16, Q5, ESC>;
+    auto kern = qdot_tc_kernel<BN, NCONV, NEPI, S8, S16, MINB, SUMS, PREX, Q5, ESC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::kSmem);
     if (e != cudaSuccess) return e;
     // the register split adds up only if every thread was launched with 128 registers
@@ -979,9 +1085,19 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
             if (prex) return launch_cfg<128, 6, 8, 2, 3, 1, SUMS, true>(maps, prm, grid, stream);
         return launch_cfg<128, 6, 8, 2, 3, 1, SUMS>(maps, prm, grid, stream);
     }
-    if (BN == 16) return launch_cfg<16, 6, 8, 5, 3, 1, SUMS>(maps, prm, grid, stream);
-    if (BN == 32) return launch_cfg<32, 6, 8, 5, 3, 1, SUMS>(maps, prm, grid, stream);
-    return launch_cfg<64, 6, 8, 4, 3, 1, SUMS>(maps, prm, grid, stream);
+    if constexpr (SUMS) {
+        if (BN == 16) return launch_cfg<16, 6, 8, 5, 3, 1, SUMS>(maps, prm, grid, stream);
+        if (BN == 32) return launch_cfg<32, 6, 8, 5, 3, 1, SUMS>(maps, prm, grid, stream);
+        return launch_cfg<64, 6, 8, 4, 3, 1, SUMS>(maps, prm, grid, stream);
+    } else {
+        // narrow tiles take the scales in the epilogue (the activation scale tile is
+        // [BN][4] in shared memory here: AS is row-major); the int8 ring is then
+        // deeper, as each stage lives until the epilogue has read its scales
+        if (prm.ys_sr != GROUP || prm.ys_sb != 1) return cudaErrorNotSupported;
+        if (BN == 16) return launch_cfg<16, 6, 8, 8, 3, 1, false, false, false, true>(maps, prm, grid, stream);
+        if (BN == 32) return launch_cfg<32, 6, 8, 7, 3, 1, false, false, false, true>(maps, prm, grid, stream);
+        return launch_cfg<64, 6, 8, 5, 3, 1, false, false, false, true>(maps, prm, grid, stream);
+    }
 }
 
 }  // namespace

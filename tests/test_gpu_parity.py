@@ -270,7 +270,9 @@ def test_qdot_workload_full_simt(pq, name):
 # ------------------------------------------------------------------ tensor-core path
 
 TC_SHAPES = [(1, 16, 128), (9, 100, 256), (16, 128, 128), (17, 300, 384), (33, 130, 128), (64, 257, 512),
-             (65, 64, 256), (130, 200, 128), (256, 384, 1024), (300, 129, 256)]
+             (65, 64, 256), (130, 200, 128), (256, 384, 1024), (300, 129, 256),
+             # narrow tiles over many scale groups, split along K into units of unequal length
+             (5, 2000, 2048), (24, 700, 3072), (48, 1100, 4096)]
 
 
 @pytest.mark.parametrize("M,N,K", TC_SHAPES)
