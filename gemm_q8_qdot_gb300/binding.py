@@ -23,7 +23,7 @@ PQ_ERR_TIMEOUT = -5
 PQ_ERR_UNSUPPORTED = -6
 PQ_ERR_SCRATCH = -7
 
-PATH_AUTO, PATH_SIMT, PATH_TC = 0, 1, 2
+PATH_AUTO, PATH_SIMT, PATH_TC, PATH_MMA = 0, 1, 2, 3
 WS_N_KB, WS_KB_N = 0, 1
 
 EXPORTS = ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",

@@ -129,7 +129,8 @@ int check_qdot_shape(int64_t M, int64_t N, int64_t K) {
 int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C,
               int32_t* S, int64_t M, int64_t N, int64_t K, int ws_layout, int path,
               cudaStream_t stream, int no_alloc = 0) {
-    if (path != PQ_PATH_AUTO && path != PQ_PATH_SIMT && path != PQ_PATH_TC) return PQ_ERR_INVALID_ARG;
+    if (path != PQ_PATH_AUTO && path != PQ_PATH_SIMT && path != PQ_PATH_TC && path != PQ_PATH_MMA)
+        return PQ_ERR_INVALID_ARG;
     if (ws_layout != PQ_WS_N_KB && ws_layout != PQ_WS_KB_N) return PQ_ERR_INVALID_ARG;
     int st = check_qdot_shape(M, N, K);
     if (st != PQ_OK) return st;
@@ -144,15 +145,18 @@ int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS
     pq::QdotArgs a{A, AS, W, WS, C, S, M, N, K, ws_layout, no_alloc};
     if (path == PQ_PATH_SIMT) return map_cuda(pq::launch_qdot_simt(a, stream));
     if (path == PQ_PATH_TC) return map_cuda(pq::launch_qdot_tc(a, stream));
-    // automatic: the dp4a streaming kernel up to 16 rows (measured on GB300 at
-    // K = 4096, N = 11008: 36 us at M = 16 against 44 us for the tensor-core
-    // kernel, which is flat at 44-47 us up to M = 32), the tensor cores above;
-    // shapes the tensor-core kernel cannot take (K % 128 != 0) go to the dp4a
-    // kernel, which takes every shape
-    if (M > 16) {
-        cudaError_t e = pq::launch_qdot_tc(a, stream);
-        if (e != cudaErrorNotSupported) return map_cuda(e);
-    }
+    if (path == PQ_PATH_MMA) return map_cuda(pq::launch_qdot_mma(a, stream));
+    // automatic, by M (measured on GB300 at K = 4096, N = 11008, graphs of
+    // back-to-back calls): the dp4a streaming kernel up to 8 rows (12.3 us at
+    // M = 4, 17.3 us at M = 8), the warp-level MMA kernel for 9..16 rows (24.7 us
+    // at M = 16, against 31.8 us for dp4a and 28.6 us for tcgen05), the tcgen05
+    // kernel above (30.6 us at M = 32, 39.6 us at M = 64); a shape a kernel
+    // declines (K % 128 != 0 for tcgen05) goes to the dp4a kernel, which takes
+    // every shape
+    cudaError_t e = cudaErrorNotSupported;
+    if (M > 16) e = pq::launch_qdot_tc(a, stream);
+    else if (M > 8) e = pq::launch_qdot_mma(a, stream);
+    if (e != cudaErrorNotSupported) return map_cuda(e);
     return map_cuda(pq::launch_qdot_simt(a, stream));
 }
 

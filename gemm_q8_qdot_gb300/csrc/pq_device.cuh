@@ -2,6 +2,7 @@
 // cache hints, packed byte arithmetic.  Inline PTX is written here by hand.
 #pragma once
 #include <cstdint>
+#include <cuda_fp16.h>
 
 namespace pq {
 
@@ -137,6 +138,38 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 // the programmatic-serialization attribute.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// int8x4 -> two f16x2 (exact): bias the bytes to unsigned, put them under the
+// f16 exponent of 1024 (0x64xx = 1024 + u), subtract 1152 = 1024 + 128.  lo
+// holds bytes 0 and 1 (byte 0 in the low half), hi bytes 2 and 3.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140u);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342u);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&ha);
+    hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+// Packed f32 pairs (low word first) and the sm_100+ paired multiply / FMA,
+// each element rounded as its scalar counterpart: one instruction for two.
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
 
 // Sum of the 32 signed-byte products of two Q8_0 blocks: eight dp4a.
 __device__ __forceinline__ int block_dot(const u32x8& a, const u32x8& w) {

@@ -73,6 +73,10 @@ cudaError_t launch_qdot_tc_q50(const QdotArgs& a, cudaStream_t stream);
 // tcgen05 tensor-core kernel.  cudaErrorNotSupported if the device is not sm_103.
 cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream);
 
+// Warp-level MMA kernel (mma.sync m16n8k16, f16 operands, exact block sums) for
+// 1 <= M <= 64; cudaErrorNotSupported otherwise.
+cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream);
+
 // The current device's workspace of at least `bytes` (allocated on first use,
 // grown on demand, never freed before exit).
 cudaError_t device_workspace(size_t bytes, void** out);

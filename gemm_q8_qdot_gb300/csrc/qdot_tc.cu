@@ -207,19 +207,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsig
     }
 }
 
-// int8x4 -> two f16x2 (exact): bias the bytes to unsigned, put them under the
-// f16 exponent of 1024 (0x64xx = 1024 + u), subtract 1152 = 1024 + 128.
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    const uint32_t u = w ^ 0x80808080u;
-    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140u);
-    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342u);
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));
-    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
-    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
-    lo = *reinterpret_cast<const uint32_t*>(&ha);
-    hi = *reinterpret_cast<const uint32_t*>(&hb);
-}
-
 // Q5_0: the four bits of x spread to bit 0 of four bytes (x * 0x00204081 puts
 // bit i at bit 8i, no carries), and four biased elements q in [0, 31] (one per
 // byte) -> two f16x2 of q - 16, exact (placed under the f16 exponent of 1024,
@@ -234,25 +221,6 @@ __device__ __forceinline__ void q5_to_f16x4(uint32_t q, uint32_t& lo, uint32_t& 
     const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
     lo = *reinterpret_cast<const uint32_t*>(&ha);
     hi = *reinterpret_cast<const uint32_t*>(&hb);
-}
-
-// Packed f32 pairs (low word first) and the sm_100+ paired FMA, each element
-// rounded as its scalar counterpart: one instruction for two accumulators.
-__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
 }
 
 // Exact split of an f32 into three bf16 whose sum is the value (normal range).

@@ -76,9 +76,11 @@ typedef enum {
 
 /* Kernel path selector for pq_qdot_q8_0_ex / pq_qdot_q8_0_blocksums. */
 enum {
-    PQ_PATH_AUTO = 0,  /* by M: the dp4a streaming kernels up to M = 16, tensor cores above */
+    PQ_PATH_AUTO = 0,  /* by M: dp4a up to M = 8, the warp-level MMA for 9..16, tcgen05 above */
     PQ_PATH_SIMT = 1,  /* dp4a (CUDA-core) streaming kernel, any M */
-    PQ_PATH_TC = 2     /* tcgen05 tensor-core kernel (f16 operands, exact integer block sums) */
+    PQ_PATH_TC = 2,    /* tcgen05 tensor-core kernel (f16 operands, exact integer block sums) */
+    PQ_PATH_MMA = 3    /* warp-level tensor-core kernel (mma.sync m16n8k16, f16 operands, exact
+                          integer block sums), M <= 64 */
 };
 
 /* Layout of the weight-scale plane WS. */
@@ -193,8 +195,8 @@ int pq_quantize_qdot_q8_0_noalloc(const float* x, const int8_t* W, const float* 
  * The integer stage alone, for verification: S[i, j, b] = sum over k in
  * block b of A[i, k] * W[j, k] ("Quantized built-ins and formats": "the
  * inner sum in integers"), computed by the engine of `path` (PQ_PATH_SIMT:
- * dp4a; PQ_PATH_TC: the tensor-core MMA with f32 accumulation, exact because
- * every partial sum is an integer below 2^24).  S: int32 [M, N, K/32],
+ * dp4a; PQ_PATH_TC and PQ_PATH_MMA (M <= 64): the tensor-core MMAs with f32
+ * accumulation, exact because every partial sum is an integer below 2^24).  S: int32 [M, N, K/32],
  * 4-byte aligned, overwritten.  |S| <= 32 * 128 * 128 = 524288.
  */
 int pq_qdot_q8_0_blocksums(const int8_t* A, const int8_t* W, int32_t* S,

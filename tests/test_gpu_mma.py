@@ -1,0 +1,106 @@
+"""GPU parity of the warp-level tensor-core path (mma.sync m16n8k16, M <= 64).
+
+Same bars as the other paths: outputs within |C - out| <= 1e-5 * sum_b |t_b| +
+1e-6 of the CPU oracle element by element, block sums identical.  Shapes cover
+one to four 16-row m-tiles, ragged weight-row tiles (N not a multiple of 8 or
+64), single-block K, K split over clusters of CTAs (including a short last
+split), both weight-scale layouts, graph capture, and the full-size workloads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_q8_qdot_gb300 import workloads
+from tests.test_gpu_parity import (assert_within_bound, dev, host, quantized_workload, rand_operands,
+                                   sampled_check)
+
+pytestmark = pytest.mark.gpu
+
+MMA_SHAPES = [(1, 1, 32), (1, 64, 128), (2, 7, 32), (3, 65, 256), (5, 130, 1056), (8, 64, 4096),
+              (15, 200, 384), (16, 128, 96), (17, 257, 512), (31, 100, 2048), (32, 640, 3072),
+              (33, 90, 160), (47, 300, 1024), (48, 1100, 4096), (63, 129, 640), (64, 1000, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", MMA_SHAPES)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_qdot_mma(pq, M, N, K, layout):
+    a, a_s, w, w_s = rand_operands(M * 131 + N * 7 + K + layout, M, N, K)
+    out, bound = oracle.qdot(a, a_s, w, w_s)
+    ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+    C = torch.full((M, N), float("nan"), device="cuda:0")
+    pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(ws), C, ws_layout=layout, path=pq.PATH_MMA)
+    pq.check_device()
+    assert_within_bound(C, out, bound, f"mma M={M} N={N} K={K} layout={layout}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 9, 32), (7, 70, 256), (16, 64, 4096), (40, 130, 1280), (64, 72, 512)])
+def test_blocksums_mma_exact(pq, M, N, K):
+    """The integer stage alone: identical to the oracle's int64 block sums,
+    including blocks at the extreme |S| = 32 * 128 * 128."""
+    a, _, w, _ = rand_operands(M * 5 + N + K, M, N, K)
+    a[:, :32] = -128
+    w[:, :32] = -128
+    a[:, 32:64] = 127
+    S_ref = oracle.blocksums(a, w)
+    S = pq.qdot_q8_0_blocksums(dev(a), dev(w), path=pq.PATH_MMA)
+    pq.check_device()
+    assert np.array_equal(host(S).astype(np.int64), S_ref)
+
+
+def test_qdot_mma_extreme_values(pq):
+    """Every product at its largest magnitude and scales over a wide range."""
+    M, N, K = 20, 72, 1024
+    a = np.full((M, K), -128, dtype=np.int8)
+    w = np.full((N, K), -128, dtype=np.int8)
+    w[1::2] = 127
+    rng = np.random.default_rng(3)
+    a_s = workloads.random_scales(rng, (M, K // 32), 1e-6, 1e3)
+    w_s = workloads.random_scales(rng, (N, K // 32), 1e-6, 1e3)
+    out, bound = oracle.qdot(a, a_s, w, w_s)
+    C = pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(w_s), path=pq.PATH_MMA)
+    pq.check_device()
+    assert_within_bound(C, out, bound, "extreme values")
+
+
+def test_qdot_mma_rejects_more_than_64_rows(pq):
+    M, N, K = 65, 16, 64
+    a, a_s, w, w_s = rand_operands(1, M, N, K)
+    with pytest.raises(pq.PQError) as ei:
+        pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(w_s), path=pq.PATH_MMA)
+    assert ei.value.code == pq.PQ_ERR_UNSUPPORTED
+
+
+def test_qdot_mma_in_a_graph(pq):
+    """Captured with clusters and programmatic dependent launches, replayed twice."""
+    M, N, K = 24, 500, 2048
+    a, a_s, w, w_s = rand_operands(99, M, N, K)
+    out, bound = oracle.qdot(a, a_s, w, w_s)
+    A, AS, W, WS = dev(a), dev(a_s), dev(w), dev(w_s)
+    C = torch.full((M, N), float("nan"), device="cuda:0")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(3):
+            pq.qdot_q8_0_ex(A, AS, W, WS, C, path=pq.PATH_MMA)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    pq.check_device()
+    assert_within_bound(C, out, bound, "graph")
+
+
+@pytest.mark.parametrize("name", [n for n in workloads.Q8_WORKLOADS if 1 < workloads.Q8_WORKLOADS[n].M <= 64])
+def test_qdot_mma_workload_full(pq, name):
+    """The small-batch workloads at full size through this path, sampled columns."""
+    x, w, qa, sa, qw, sw = quantized_workload(name)
+    M, N = qa.shape[0], qw.shape[0]
+    A, AS = pq.quantize_q8_0(dev(x))
+    W, WS = pq.quantize_q8_0(dev(w))
+    C = pq.qdot_q8_0_ex(A, AS, W, WS, path=pq.PATH_MMA)
+    pq.check_device()
+    rng = np.random.default_rng(2)
+    cols = np.unique(np.concatenate([rng.choice(N, 512, replace=False), [0, N - 1]]))
+    sampled_check(C, qa, sa, qw, sw, np.arange(M), cols, name)
+    assert torch.isfinite(C).all()
