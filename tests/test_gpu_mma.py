@@ -19,7 +19,9 @@ pytestmark = pytest.mark.gpu
 
 MMA_SHAPES = [(1, 1, 32), (1, 64, 128), (2, 7, 32), (3, 65, 256), (5, 130, 1056), (8, 64, 4096),
               (15, 200, 384), (16, 128, 96), (17, 257, 512), (31, 100, 2048), (32, 640, 3072),
-              (33, 90, 160), (47, 300, 1024), (48, 1100, 4096), (63, 129, 640), (64, 1000, 4096)]
+              (33, 90, 160), (47, 300, 1024), (48, 1100, 4096), (63, 129, 640), (64, 1000, 4096),
+              # more row tiles than SMs, ragged last tile, splits of unequal length
+              (4, 8, 128), (8, 100, 512), (12, 333, 2048), (16, 1000, 4096), (16, 5000, 1024)]
 
 
 @pytest.mark.parametrize("M,N,K", MMA_SHAPES)
@@ -71,9 +73,10 @@ def test_qdot_mma_rejects_more_than_64_rows(pq):
     assert ei.value.code == pq.PQ_ERR_UNSUPPORTED
 
 
-def test_qdot_mma_in_a_graph(pq):
+@pytest.mark.parametrize("M", [12, 24])
+def test_qdot_mma_in_a_graph(pq, M):
     """Captured with clusters and programmatic dependent launches, replayed twice."""
-    M, N, K = 24, 500, 2048
+    N, K = 500, 2048
     a, a_s, w, w_s = rand_operands(99, M, N, K)
     out, bound = oracle.qdot(a, a_s, w, w_s)
     A, AS, W, WS = dev(a), dev(a_s), dev(w), dev(w_s)

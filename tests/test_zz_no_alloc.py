@@ -41,7 +41,8 @@ def _bound(x, w, w_s):
     return oracle.qdot(qa, sa, w, w_s)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (4, 1000, 4096), (24, 300, 1024), (64, 257, 14336), (128, 300, 1024)])
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (4, 1000, 4096), (12, 700, 2048), (16, 257, 4096), (24, 300, 1024),
+                                   (64, 257, 14336), (128, 300, 1024)])
 def test_noalloc_matches_allocating_entry_point(pq, M, N, K):
     lib = _c_abi(pq)
     rng = np.random.default_rng(M * 7 + N + K)
