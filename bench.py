@@ -76,6 +76,7 @@ KERNEL_SOURCES = {
     "qdot_fused": ["gemm_q8_qdot_gb300/csrc/qdot_simt.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
     "qdot_q50": ["gemm_q8_qdot_gb300/csrc/qdot_q50.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
     "qdot_mma": ["gemm_q8_qdot_gb300/csrc/qdot_mma.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
+    "qdot_q50_fused": ["gemm_q8_qdot_gb300/csrc/qdot_q50.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
 }
 
 
@@ -239,8 +240,9 @@ class Problem:
 
     A step quantizes the activation rows and contracts them with the weights:
     for M <= 8 through the one-call fused entry point (pq_quantize_qdot_q8_0,
-    which also writes the quantized rows), otherwise pq_quantize_q8_0 then
-    pq_qdot_q8_0; `fused=False` forces the two-call sequence.
+    or pq_quantize_q50_qdot for Q5_0 weights, which also writes the quantized
+    rows), otherwise pq_quantize_q8_0 then pq_qdot_q8_0 / pq_q50_qdot;
+    `fused=False` forces the two-call sequence.
     """
 
     def __init__(self, pq, wl: workloads.Workload, device, fused: bool = True):
@@ -248,7 +250,7 @@ class Problem:
         self.wl = wl
         self.pq = pq
         self.q50 = wl.w_format == "q5_0"
-        self.fused = fused and wl.M <= 8 and not self.q50
+        self.fused = fused and wl.M <= 8
         x = workloads.activations(wl)
         self.x_host = torch.from_numpy(x).pin_memory()
         if self.q50:
@@ -277,7 +279,10 @@ class Problem:
             if events is not None:
                 events[0].record()
                 events[1].record()
-            self.pq.quantize_qdot_q8_0(self.x, self.W[c], self.WS[c], self.C, A=self.A, AS=self.AS)
+            if self.q50:
+                self.pq.quantize_q50_qdot(self.x, self.W[c], self.WS[c], self.C, A=self.A, AS=self.AS)
+            else:
+                self.pq.quantize_qdot_q8_0(self.x, self.W[c], self.WS[c], self.C, A=self.A, AS=self.AS)
             if events is not None:
                 events[2].record()
             return
@@ -392,8 +397,8 @@ def time_e2e(prob: Problem, steps: int, warmup: int):
 
 
 def fused_is_one_kernel(prob: Problem) -> bool:
-    """Whether pq_quantize_qdot_q8_0 runs as the single fused kernel for this shape
-    (one row, at most 32 columns per CTA and two CTAs per SM in one wave)."""
+    """Whether the one-call step (pq_quantize_qdot_q8_0 / pq_quantize_q50_qdot) runs as a
+    single fused kernel for this shape (one row, 32 columns per CTA, at most two waves)."""
     import torch
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     return prob.wl.M == 1 and -(-prob.wl.N // 32) <= 2 * sms
@@ -408,7 +413,7 @@ def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str, one_kernel
         peak = float(peaks["hbm_gbs"])
         # the kernel the automatic path runs for this M (pq_api.cu: dp4a up to 8
         # rows, the warp-level MMA for 9..16, tcgen05 above)
-        kernel = "qdot_q50" if prob.q50 else \
+        kernel = ("qdot_q50_fused" if one_kernel else "qdot_q50") if prob.q50 else \
             ("qdot_fused" if one_kernel else "qdot_simt") if wl.M <= 8 else \
             "qdot_mma" if wl.M <= 16 else "qdot_tc"
         traffic = recorded_traffic(kernel, wl.name)
@@ -449,7 +454,8 @@ def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sample
     dom_ms = (ms / steps) if one_kernel else qdot_only_ms
     kernel_ms["dominant"] = round(dom_ms, 5)
     res = {"value": round(value / scale, 3), "unit": unit, "ms_per_step": round(t_max * 1e3 / steps, 5),
-           "step": ("pq_quantize_qdot_q8_0 (one kernel)" if one_kernel else "pq_quantize_qdot_q8_0 (two kernels)")
+           "step": (("pq_quantize_q50_qdot" if prob.q50 else "pq_quantize_qdot_q8_0") +
+                    (" (one kernel)" if one_kernel else " (two kernels)"))
            if prob.fused else ("pq_quantize_q8_0 + pq_q50_qdot" if prob.q50 else "pq_quantize_q8_0 + pq_qdot_q8_0"),
            "kernel_ms": kernel_ms,
            "roofline": roofline_for(prob, dom_ms, peaks, peak_src, one_kernel), "weight_copies": prob.copies,

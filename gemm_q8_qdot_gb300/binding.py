@@ -27,8 +27,8 @@ PATH_AUTO, PATH_SIMT, PATH_TC, PATH_MMA = 0, 1, 2, 3
 WS_N_KB, WS_KB_N = 0, 1
 
 EXPORTS = ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
-           "pq_quantize_qdot_q8_0_noalloc", "pq_qdot_q8_0_blocksums", "pq_q50_qdot", "pq_q50_blocksums",
-           "pq_check_device", "pq_strerror", "pq_version")
+           "pq_quantize_qdot_q8_0_noalloc", "pq_qdot_q8_0_blocksums", "pq_q50_qdot", "pq_quantize_q50_qdot",
+           "pq_q50_blocksums", "pq_check_device", "pq_strerror", "pq_version")
 
 _lib: ctypes.CDLL | None = None
 
@@ -60,14 +60,15 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pq_quantize_qdot_q8_0_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_qdot_q8_0_blocksums.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_q50_qdot.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
+    lib.pq_quantize_q50_qdot.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_q50_blocksums.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     lib.pq_check_device.argtypes = [vp]
     lib.pq_strerror.argtypes = [i32]
     lib.pq_strerror.restype = ctypes.c_char_p
     lib.pq_version.argtypes = []
     for fn in ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
-               "pq_quantize_qdot_q8_0_noalloc", "pq_qdot_q8_0_blocksums", "pq_q50_qdot", "pq_q50_blocksums",
-               "pq_check_device", "pq_version"):
+               "pq_quantize_qdot_q8_0_noalloc", "pq_qdot_q8_0_blocksums", "pq_q50_qdot", "pq_quantize_q50_qdot",
+               "pq_q50_blocksums", "pq_check_device", "pq_version"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -197,6 +198,22 @@ def q50_qdot(A, AS, W5, WS, C=None, ws_layout: int = WS_N_KB, stream=None):
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     _check(load().pq_q50_qdot(_ptr(A), _ptr(AS), _ptr(W5), _ptr(WS), _ptr(C), M, N, K, int(ws_layout),
                               _stream(stream)), "pq_q50_qdot")
+    return C
+
+
+def quantize_q50_qdot(x, W5, WS, C=None, A=None, AS=None, ws_layout: int = WS_N_KB, stream=None):
+    """One decode step against Q5_0 weights via pq_quantize_q50_qdot: C = q50_qdot_t(quantize(x), W5);
+    A/AS optionally receive the quantized rows (both or neither)."""
+    if x.dtype != torch.float32:
+        raise TypeError("x must be float32")
+    M, K = x.shape
+    N = W5.shape[0]
+    if W5.dtype != torch.uint8 or W5.shape[1] != K // 32 * 20:
+        raise ValueError("W5 must be uint8 [N, K/32 * 20]")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(load().pq_quantize_q50_qdot(_ptr(x), _ptr(A), _ptr(AS), _ptr(W5), _ptr(WS), _ptr(C), M, N, K,
+                                       int(ws_layout), _stream(stream)), "pq_quantize_q50_qdot")
     return C
 
 

@@ -248,6 +248,36 @@ int pq_q50_qdot(const int8_t* A, const float* AS, const uint8_t* W5, const float
     return map_cuda(pq::launch_qdot_q50(a, stream));
 }
 
+int pq_quantize_q50_qdot(const float* x, int8_t* A, float* AS, const uint8_t* W5, const float* WS, float* C,
+                         int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream) {
+    if (ws_layout != PQ_WS_N_KB && ws_layout != PQ_WS_KB_N) return PQ_ERR_INVALID_ARG;
+    int st = check_qdot_shape(M, N, K);
+    if (st != PQ_OK) return st;
+    if ((__int128)N * (K / 32) * 20 > (__int128)INT64_MAX) return PQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return PQ_OK;
+    if (!x || !W5 || !WS || !C) return PQ_ERR_INVALID_ARG;
+    if ((A == nullptr) != (AS == nullptr)) return PQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(W5, 4) || !aligned(WS, 4) || !aligned(C, 4)) return PQ_ERR_ALIGN;
+    if (A && (!aligned(A, 16) || !aligned(AS, 4))) return PQ_ERR_ALIGN;
+    // one kernel for a single row whose grid fits two waves
+    pq::FusedArgs f{x, A, AS, reinterpret_cast<const int8_t*>(W5), WS, C, M, N, K, ws_layout};
+    cudaError_t e = pq::launch_qdot_q50_fused(f, stream);
+    if (e != cudaErrorNotSupported) return map_cuda(e);
+    // otherwise the quantizer, then q50_qdot_t; the quantized rows go to A / AS,
+    // or to this device's workspace
+    if (!A) {
+        void* ws = nullptr;
+        const size_t qbytes = (static_cast<size_t>(M * K) + 255) & ~size_t(255);
+        e = pq::device_workspace(qbytes + static_cast<size_t>(M * (K / 32)) * sizeof(float), &ws);
+        if (e != cudaSuccess) return map_cuda(e);
+        A = static_cast<int8_t*>(ws);
+        AS = reinterpret_cast<float*>(static_cast<char*>(ws) + qbytes);
+    }
+    st = pq_quantize_q8_0(x, A, AS, M, K, stream);
+    if (st != PQ_OK) return st;
+    return pq_q50_qdot(A, AS, W5, WS, C, M, N, K, ws_layout, stream);
+}
+
 int pq_q50_blocksums(const int8_t* A, const uint8_t* W5, int32_t* S, int64_t M, int64_t N, int64_t K,
                      cudaStream_t stream) {
     int st = check_qdot_shape(M, N, K);
@@ -281,7 +311,7 @@ const char* pq_strerror(int code) {
     }
 }
 
-int pq_version(void) { return 102; }
+int pq_version(void) { return 103; }
 
 int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles) {
     if (skip_stage < -1) return PQ_ERR_INVALID_ARG;

@@ -65,6 +65,11 @@ cudaError_t launch_qdot_fused(const FusedArgs& a, cudaStream_t stream);
 // blocks, [N, K/32 * 20] bytes; any M.
 cudaError_t launch_qdot_q50(const QdotArgs& a, cudaStream_t stream);
 
+// Fused quantize + dp4a contraction against Q5_0 weights (a.W points at the
+// Q5_0 blocks) for one activation row; cudaErrorNotSupported as for
+// launch_qdot_fused.
+cudaError_t launch_qdot_q50_fused(const FusedArgs& a, cudaStream_t stream);
+
 // tcgen05 tensor-core kernel for Q5_0 weights (a.W points at the Q5_0 blocks,
 // 16-byte aligned): prompt shapes only (M > 64), no block-sum mode;
 // cudaErrorNotSupported otherwise or when the device is not sm_103.

@@ -25,6 +25,8 @@
 // at bit 8i, no carries); q - 16 per byte without borrows is
 // ((q | 0x80) - 0x10) ^ 0x80 on all four bytes at once, a signed byte in
 // [-16, 15].  Then 8 dp4a against the activation block, exact in int32.
+#include <atomic>
+
 #include "pq_internal.h"
 #include "pq_device.cuh"
 
@@ -180,7 +182,148 @@ cudaError_t launch_by_m(const QdotArgs& a, bool v8, cudaStream_t stream) {
     return launch_tile<4, 2, 2, SUMS, WSL>(a, v8, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Fused decode step against Q5_0 weights: quantize the activation row x [1, K]
+// into this CTA's shared memory with the quantizer's exact arithmetic, then
+// contract it with the Q5_0 rows as qdot_q50_kernel does (one output column
+// per warp).  The order of the memory traffic is that of the Q8_0 fused step:
+// an L2 prefetch of the start of the CTA's weight rows before
+// griddepcontrol.wait, x loaded and quantized first after it, the first round
+// of weight loads issued once the first round of x is quantized, the next
+// kernel let in once the quantized row is in shared memory, and the optional
+// A / AS outputs written in 16-byte pieces spread over all CTAs.
+constexpr int kQ50FusedWarps = 32;            // warps (= output columns) per CTA
+constexpr int64_t kQ50PrefetchBytes = 4096;   // bytes of each weight row prefetched into L2
+
+template <int U, int WSL, int NW>
+__global__ void __launch_bounds__(NW * 32)
+qdot_q50_fused_kernel(FusedArgs p) {
+    extern __shared__ __align__(16) uint8_t fsm[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t N = p.N, K = p.K, KB = K >> 5;
+    const int64_t row_bytes = KB * kQ50Bytes;
+    int8_t* a_s = reinterpret_cast<int8_t*>(fsm);       // [K]
+    float* as_s = reinterpret_cast<float*>(fsm + K);    // [KB]
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * NW + warp;
+    const bool jv = j < N;
+    const uint8_t* wrow = reinterpret_cast<const uint8_t*>(p.W) + (jv ? j : 0) * row_bytes;
+
+    if (lane == 0 && jv) {
+        const int64_t kb = row_bytes < kQ50PrefetchBytes ? row_bytes : kQ50PrefetchBytes;
+        if ((kb % 16) == 0 && (reinterpret_cast<uintptr_t>(wrow) & 15) == 0)
+            prefetch_l2(wrow, static_cast<uint32_t>(kb));
+    }
+    pdl_wait();
+
+    // weights of round `bb`: U blocks per lane, read once per launch
+    const uint64_t wpol = l2_weight_policy(true);
+    Q50Block wb[U];
+    float wsv[U];
+    auto load_round = [&](int64_t bb) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t b = bb + u * 32 + lane;
+            if (jv && b < KB) {
+                wb[u] = ld_q50(wrow + b * kQ50Bytes, wpol);
+                wsv[u] = ld_wscale(WSL == 0 ? p.WS + j * KB + b : p.WS + b * N + j, wpol);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 5; ++t) wb[u].w[t] = 0u;
+                wsv[u] = 0.0f;
+            }
+        }
+    };
+
+    // quantize x: 8 lanes per Q8_0 block, 4 floats each (every thread of the CTA
+    // works); the next round's x load is issued before the current round is
+    // quantized, and the first weight round right after the first x round
+    const int64_t nthr = KB * 8;
+    constexpr int64_t kRound = NW * 32;
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 xv = threadIdx.x < nthr ? ld_stream_f4(p.x + threadIdx.x * 4) : zero4;
+    for (int64_t base = 0; base < nthr; base += kRound) {  // CTA-uniform
+        const int64_t t = base + threadIdx.x;
+        const int64_t tn = t + kRound;
+        const float4 xn = tn < nthr ? ld_stream_f4(p.x + tn * 4) : zero4;
+        const float d = q8_scale_of<8>(amax4(xv));  // every lane of the warp takes part
+        if (t < nthr) {
+            *reinterpret_cast<uint32_t*>(a_s + t * 4) = q8_pack4(xv, d, __frcp_rn(d));
+            if ((threadIdx.x & 7) == 0) as_s[t >> 3] = d;
+        }
+        xv = xn;
+        if (base == 0) load_round(0);
+    }
+    __syncthreads();
+    pdl_trigger();
+
+    if (p.A != nullptr) {
+        // piece q (16 bytes of A, or one scale of AS) goes to CTA q % grid
+        const int64_t g = gridDim.x;
+        for (int64_t q = threadIdx.x * g + blockIdx.x; q < K / 16; q += kRound * g)
+            reinterpret_cast<uint4*>(p.A)[q] = reinterpret_cast<const uint4*>(a_s)[q];
+        for (int64_t q = threadIdx.x * g + blockIdx.x; q < KB; q += kRound * g) p.AS[q] = as_s[q];
+    }
+    if (!jv) return;
+
+    float acc = 0.0f;
+    for (int64_t bb = 0; bb < KB; bb += 32 * U) {
+        if (bb > 0) load_round(bb);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t b = bb + u * 32 + lane;
+            if (b >= KB) continue;
+            const uint4* pa = reinterpret_cast<const uint4*>(a_s + b * 32);
+            const uint4 a0 = pa[0], a1 = pa[1];
+            u32x8 av;
+            av.v[0] = a0.x; av.v[1] = a0.y; av.v[2] = a0.z; av.v[3] = a0.w;
+            av.v[4] = a1.x; av.v[5] = a1.y; av.v[6] = a1.z; av.v[7] = a1.w;
+            acc = fmaf(as_s[b] * wsv[u], static_cast<float>(block_dot(av, q50_unpack(wb[u]))), acc);
+        }
+    }
+    const float v = warp_sum(acc);
+    if (lane == 0) p.C[j] = v;
+}
+
+template <int WSL>
+cudaError_t launch_q50_fused(const FusedArgs& a, cudaStream_t stream) {
+    constexpr int NW = kQ50FusedWarps;
+    const size_t smem = static_cast<size_t>(a.K) + static_cast<size_t>(a.K / 32) * 4;
+    if (smem > 200 * 1024) return cudaErrorNotSupported;
+    const int64_t grid = (a.N + NW - 1) / NW;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    auto kern = qdot_q50_fused_kernel<4, WSL, NW>;
+    if (smem > 48 * 1024) {
+        static std::atomic<int> raised[64];  // per device (the attribute is set in its context)
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorNotSupported;
+        if (static_cast<int>(smem) > raised[dev].load()) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+            raised[dev].store(static_cast<int>(smem));
+        }
+    }
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NW * 32), smem, stream, a);
+}
+
 }  // namespace
+
+cudaError_t launch_qdot_q50_fused(const FusedArgs& a, cudaStream_t stream) {
+    // one row (the decode step), at most two waves of CTAs (one 1024-thread CTA per SM)
+    if (a.M != 1) return cudaErrorNotSupported;
+    static std::atomic<int> sm_count[64];  // the SM count of each device, queried once
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorNotSupported;
+    int sms = sm_count[dev].load(std::memory_order_relaxed);
+    if (sms <= 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            return cudaErrorNotSupported;
+        sm_count[dev].store(sms, std::memory_order_relaxed);
+    }
+    if ((a.N + kQ50FusedWarps - 1) / kQ50FusedWarps > 2 * static_cast<int64_t>(sms)) return cudaErrorNotSupported;
+    return a.ws_layout == 0 ? launch_q50_fused<0>(a, stream) : launch_q50_fused<1>(a, stream);
+}
 
 cudaError_t launch_qdot_q50(const QdotArgs& a, cudaStream_t stream) {
     // the activation blocks take 256-bit loads when A is 32-byte aligned

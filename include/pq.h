@@ -227,6 +227,21 @@ int pq_q50_qdot(const int8_t* A, const float* AS, const uint8_t* W5, const float
                 int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);
 
 /*
+ * One decode step against Q5_0 weights in one call: quantize the activation
+ * rows x [M, K] f32 to Q8_0 (exactly as pq_quantize_q8_0) and contract them
+ * with the Q5_0 weight W5 as pq_q50_qdot does -- the Q5_0 counterpart of
+ * pq_quantize_qdot_q8_0 ("Quantized built-ins and formats", built-in table:
+ * q50_qdot_t takes Q8_0 activations).  For one row (M == 1) and N up to
+ * 64 x the SM count this is one kernel, in which every CTA quantizes x into
+ * its shared memory while L2 prefetches the start of its weight rows, then
+ * streams them; otherwise it is the quantizer followed by pq_q50_qdot.
+ * A / AS, the workspace, alignment and overlap rules are those of
+ * pq_quantize_qdot_q8_0; W5 as for pq_q50_qdot.
+ */
+int pq_quantize_q50_qdot(const float* x, int8_t* A, float* AS, const uint8_t* W5, const float* WS, float* C,
+                         int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);
+
+/*
  * The integer stage of pq_q50_qdot alone, for verification: S[i, j, b] =
  * sum over e < 32 of A[i, 32b + e] * (q[j, 32b + e] - 16), int32 [M, N, K/32],
  * 4-byte aligned, overwritten.
@@ -245,7 +260,8 @@ int pq_check_device(cudaStream_t stream);
 /* A static, human-readable name for a pq_status code. */
 const char* pq_strerror(int code);
 
-/* ABI version of this header: major * 100 + minor (1.01: pq_quantize_qdot_q8_0; 1.02: Q5_0 weights). */
+/* ABI version of this header: major * 100 + minor (1.01: pq_quantize_qdot_q8_0; 1.02: Q5_0 weights;
+   1.03: pq_quantize_q50_qdot and PQ_PATH_MMA). */
 int pq_version(void);
 
 #ifdef __cplusplus

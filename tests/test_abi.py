@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert lib.pq_version() == 102
+    assert lib.pq_version() == 103
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert lib.pq_strerror(code).decode()
     assert "unknown" in lib.pq_strerror(99).decode()
@@ -143,3 +143,20 @@ def test_q50_entry_checks(lib):
     assert lib.pq_q50_blocksums(P16, P16, None, 1, 1, 32, None) == binding.PQ_ERR_INVALID_ARG
     assert lib.pq_q50_blocksums(P16, P16, P2, 1, 1, 32, None) == binding.PQ_ERR_ALIGN
     assert lib.pq_q50_blocksums(P16, P16, P16, 1, 1, 33, None) == binding.PQ_ERR_SHAPE
+
+
+def fused_q50(lib, x=P16, A=None, AS=None, W5=P16, WS=P16, C=P16, M=1, N=1, K=32, layout=0):
+    return lib.pq_quantize_q50_qdot(x, A, AS, W5, WS, C, M, N, K, layout, None)
+
+
+def test_fused_q50_entry_checks(lib):
+    assert fused_q50(lib, K=48) == binding.PQ_ERR_SHAPE
+    assert fused_q50(lib, N=-2) == binding.PQ_ERR_SHAPE
+    assert fused_q50(lib, M=0, x=None, W5=None, WS=None, C=None) == binding.PQ_OK
+    assert fused_q50(lib, x=None) == binding.PQ_ERR_INVALID_ARG
+    assert fused_q50(lib, W5=None) == binding.PQ_ERR_INVALID_ARG
+    assert fused_q50(lib, A=P16, AS=None) == binding.PQ_ERR_INVALID_ARG  # A and AS come together
+    assert fused_q50(lib, x=P8) == binding.PQ_ERR_ALIGN
+    assert fused_q50(lib, W5=P2) == binding.PQ_ERR_ALIGN
+    assert fused_q50(lib, A=P8, AS=P16) == binding.PQ_ERR_ALIGN
+    assert fused_q50(lib, layout=4) == binding.PQ_ERR_INVALID_ARG

@@ -167,3 +167,33 @@ def test_q50_prompt_workload_full(pq):
     sub = C[torch.from_numpy(rows).to(DEV)][:, torch.from_numpy(cols).to(DEV)]
     within(sub, out, bound, "q50 prompt full size")
     assert torch.isfinite(C).all()
+
+
+# ------------------------------------------------------------ fused quantize + q50_qdot_t
+
+FUSED_SHAPES = [(1, 1, 32), (1, 300, 1056), (1, 4096, 4096), (1, 40, 14336), (1, 9000, 128), (1, 9800, 256),
+                (3, 65, 256), (8, 100, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", FUSED_SHAPES)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_quantize_q50_qdot(pq, M, N, K, layout):
+    """One call: the quantized rows bit-identical to the oracle's quantizer, the result
+    within tolerance of the oracle's q50_qdot_t on those rows (one kernel for M = 1 while
+    the grid fits two waves, the quantizer then q50_qdot_t otherwise)."""
+    rng = np.random.default_rng(M * 11 + N + K + layout)
+    x = (rng.standard_normal((M, K)) * np.exp(rng.uniform(-3, 3, size=(M, 1)))).astype(np.float32)
+    _, _, w5, w_s = operands(N * 3 + K, 1, N, K)
+    qa, sa = oracle.quantize_q8_0(x)
+    ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+    out, bound = oracle.qdot_q5_0(qa, sa, w5, ws, ws_layout=layout)
+    A = torch.full((M, K), 77, dtype=torch.int8, device=DEV)
+    AS = torch.full((M, K // 32), -1.0, dtype=torch.float32, device=DEV)
+    C = pq.quantize_q50_qdot(dev(x), dev(w5), dev(ws), A=A, AS=AS, ws_layout=layout)
+    pq.check_device()
+    assert np.array_equal(A.cpu().numpy(), qa)
+    assert np.array_equal(AS.cpu().numpy().view(np.uint32), sa.view(np.uint32))
+    within(C, out, bound, f"fused q50 M={M} N={N} K={K} layout={layout}")
+    C2 = pq.quantize_q50_qdot(dev(x), dev(w5), dev(ws), ws_layout=layout)  # without A / AS
+    pq.check_device()
+    within(C2, out, bound, "fused q50, no A/AS")
