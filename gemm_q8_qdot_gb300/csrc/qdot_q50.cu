@@ -20,11 +20,12 @@
 // 0.125 of scale.
 //
 // Decode in registers: the low and high nibbles of the four data words give
-// elements 0..15 and 16..31 in dp4a word order; the matching four qh bits are
-// spread to bit 4 of each byte ((x * 0x00204081) & 0x01010101 puts bit i of x
-// at bit 8i, no carries); q - 16 per byte without borrows is
-// ((q | 0x80) - 0x10) ^ 0x80 on all four bytes at once, a signed byte in
-// [-16, 15].  Then 8 dp4a against the activation block, exact in int32.
+// elements 0..15 and 16..31 in dp4a word order; the matching four qh bits go
+// to bit 4 of each byte ((x * 0x02040810) & 0x10101010 puts bit i of x at bit
+// 8i + 4, no carries), giving the unsigned q in [0, 31] per byte.  Then
+//   sum_e a_e (q_e - 16) = sum_e a_e q_e - 16 sum_e a_e:
+// 8 dp4a of signed activation bytes with unsigned q bytes, minus 16 times the
+// activation block's byte sum, exact in int32.
 #include <atomic>
 
 #include "pq_internal.h"
@@ -47,25 +48,41 @@ __device__ __forceinline__ Q50Block ld_q50(const uint8_t* p, uint64_t pol) {
     return b;
 }
 
-__device__ __forceinline__ uint32_t spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
+// The four bits of x at bit 4 of the four bytes.
+__device__ __forceinline__ uint32_t spread4_bit4(uint32_t x) { return (x * 0x02040810u) & 0x10101010u; }
 
-__device__ __forceinline__ uint32_t minus16(uint32_t q) {
-    return ((q | 0x80808080u) - 0x10101010u) ^ 0x80808080u;
-}
-
-// The block's 32 elements as signed bytes, word t = elements 4t .. 4t+3.
+// The block's 32 elements as unsigned q in [0, 31], word t = elements 4t .. 4t+3.
 __device__ __forceinline__ u32x8 q50_unpack(const Q50Block& b) {
     u32x8 r;
     const uint32_t qh = b.w[0];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         const uint32_t w = b.w[1 + t];
-        const uint32_t lo = (w & 0x0F0F0F0Fu) | (spread4((qh >> (4 * t)) & 0xFu) << 4);
-        const uint32_t hi = ((w >> 4) & 0x0F0F0F0Fu) | (spread4((qh >> (16 + 4 * t)) & 0xFu) << 4);
-        r.v[t] = minus16(lo);
-        r.v[4 + t] = minus16(hi);
+        r.v[t] = (w & 0x0F0F0F0Fu) | spread4_bit4((qh >> (4 * t)) & 0xFu);
+        r.v[4 + t] = ((w >> 4) & 0x0F0F0F0Fu) | spread4_bit4((qh >> (16 + 4 * t)) & 0xFu);
     }
     return r;
+}
+
+// sum of a_e * q_e over a block: signed activation bytes, unsigned q bytes
+__device__ __forceinline__ int block_dot_su(const u32x8& a, const u32x8& q) {
+    int s = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) asm("dp4a.s32.u32 %0, %1, %2, %0;" : "+r"(s) : "r"(a.v[t]), "r"(q.v[t]));
+    return s;
+}
+
+// sum of the 32 signed activation bytes of a block
+__device__ __forceinline__ int block_sum(const u32x8& a) {
+    int s = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) s = __dp4a(static_cast<int>(a.v[t]), 0x01010101, s);
+    return s;
+}
+
+// sum_e a_e (q_e - 16) of a block
+__device__ __forceinline__ int q50_block_dot(const u32x8& a, const u32x8& q, int a_sum) {
+    return block_dot_su(a, q) - 16 * a_sum;
 }
 
 template <int MR, int COLS, int U, bool V8, bool SUMS, int WSL>
@@ -140,11 +157,12 @@ qdot_q50_kernel(QdotArgs p) {
             for (int r = 0; r < MR; ++r) {
                 if (!iv[r]) continue;
                 const u32x8 av = ld_block<V8, false>(arow[r] + b * 32);
+                const int asum = block_sum(av);
                 float as = 0.0f;
                 if constexpr (!SUMS) as = ld_f32(p.AS + (i0 + r) * KB + b);
 #pragma unroll
                 for (int c = 0; c < COLS; ++c) {
-                    const int s = block_dot(av, wq[c]);
+                    const int s = q50_block_dot(av, wq[c], asum);
                     if constexpr (SUMS) {
                         if (jv[c]) p.S[((i0 + r) * N + (j0 + c)) * KB + b] = s;
                     } else {
@@ -205,6 +223,7 @@ qdot_q50_fused_kernel(FusedArgs p) {
     const int64_t row_bytes = KB * kQ50Bytes;
     int8_t* a_s = reinterpret_cast<int8_t*>(fsm);       // [K]
     float* as_s = reinterpret_cast<float*>(fsm + K);    // [KB]
+    int* sum_s = reinterpret_cast<int*>(fsm + K + KB * 4);  // [KB] byte sums of the quantized blocks
     const int64_t j = static_cast<int64_t>(blockIdx.x) * NW + warp;
     const bool jv = j < N;
     const uint8_t* wrow = reinterpret_cast<const uint8_t*>(p.W) + (jv ? j : 0) * row_bytes;
@@ -247,9 +266,17 @@ qdot_q50_fused_kernel(FusedArgs p) {
         const int64_t tn = t + kRound;
         const float4 xn = tn < nthr ? ld_stream_f4(p.x + tn * 4) : zero4;
         const float d = q8_scale_of<8>(amax4(xv));  // every lane of the warp takes part
+        const uint32_t packed = q8_pack4(xv, d, __frcp_rn(d));
+        int bsum = __dp4a(static_cast<int>(packed), 0x01010101, 0);  // the block's byte sum over its 8 lanes
+        bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
+        bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
+        bsum += __shfl_xor_sync(0xffffffffu, bsum, 4);
         if (t < nthr) {
-            *reinterpret_cast<uint32_t*>(a_s + t * 4) = q8_pack4(xv, d, __frcp_rn(d));
-            if ((threadIdx.x & 7) == 0) as_s[t >> 3] = d;
+            *reinterpret_cast<uint32_t*>(a_s + t * 4) = packed;
+            if ((threadIdx.x & 7) == 0) {
+                as_s[t >> 3] = d;
+                sum_s[t >> 3] = bsum;
+            }
         }
         xv = xn;
         if (base == 0) load_round(0);
@@ -278,7 +305,7 @@ qdot_q50_fused_kernel(FusedArgs p) {
             u32x8 av;
             av.v[0] = a0.x; av.v[1] = a0.y; av.v[2] = a0.z; av.v[3] = a0.w;
             av.v[4] = a1.x; av.v[5] = a1.y; av.v[6] = a1.z; av.v[7] = a1.w;
-            acc = fmaf(as_s[b] * wsv[u], static_cast<float>(block_dot(av, q50_unpack(wb[u]))), acc);
+            acc = fmaf(as_s[b] * wsv[u], static_cast<float>(q50_block_dot(av, q50_unpack(wb[u]), sum_s[b])), acc);
         }
     }
     const float v = warp_sum(acc);
@@ -288,7 +315,7 @@ qdot_q50_fused_kernel(FusedArgs p) {
 template <int WSL>
 cudaError_t launch_q50_fused(const FusedArgs& a, cudaStream_t stream) {
     constexpr int NW = kQ50FusedWarps;
-    const size_t smem = static_cast<size_t>(a.K) + static_cast<size_t>(a.K / 32) * 4;
+    const size_t smem = static_cast<size_t>(a.K) + static_cast<size_t>(a.K / 32) * 8;
     if (smem > 200 * 1024) return cudaErrorNotSupported;
     const int64_t grid = (a.N + NW - 1) / NW;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
