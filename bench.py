@@ -381,17 +381,24 @@ def time_graph(prob: Problem, steps: int, warmup: int, world: int, sampler=None)
 
 
 def time_e2e(prob: Problem, steps: int, warmup: int):
-    """Through the public API with host buffers: H2D of x, quantize, qdot, D2H of C, per step."""
+    """Through the public API with host buffers, per step: the H2D copy of x from pinned host
+    memory, the decode step, the D2H copy of C into pinned host memory (for Q8_0 weights one
+    pq_quantize_qdot_q8_0_host call enqueues all three), then a synchronize."""
     import torch
+    stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     for t in range(warmup + steps):
         if t == warmup:
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-        prob.x.copy_(prob.x_host, non_blocking=True)
-        prob.step(t)
-        prob.C_host.copy_(prob.C, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        if prob.q50:
+            prob.x.copy_(prob.x_host, non_blocking=True)
+            prob.step(t)
+            prob.C_host.copy_(prob.C, non_blocking=True)
+        else:
+            c = t % prob.copies
+            prob.pq.quantize_qdot_q8_0_host(prob.x_host, prob.W[c], prob.WS[c], prob.C_host)
+        stream.synchronize()
     dt = time.perf_counter() - t0
     return dt, prob.x_host.numel() * 4, prob.C_host.numel() * 4
 

@@ -27,8 +27,8 @@ PATH_AUTO, PATH_SIMT, PATH_TC, PATH_MMA = 0, 1, 2, 3
 WS_N_KB, WS_KB_N = 0, 1
 
 EXPORTS = ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
-           "pq_quantize_qdot_q8_0_noalloc", "pq_qdot_q8_0_blocksums", "pq_q50_qdot", "pq_quantize_q50_qdot",
-           "pq_q50_blocksums", "pq_check_device", "pq_strerror", "pq_version")
+           "pq_quantize_qdot_q8_0_noalloc", "pq_quantize_qdot_q8_0_host", "pq_qdot_q8_0_blocksums", "pq_q50_qdot",
+           "pq_quantize_q50_qdot", "pq_q50_blocksums", "pq_check_device", "pq_strerror", "pq_version")
 
 _lib: ctypes.CDLL | None = None
 
@@ -58,6 +58,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pq_qdot_q8_0_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp]
     lib.pq_quantize_qdot_q8_0.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_quantize_qdot_q8_0_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp]
+    lib.pq_quantize_qdot_q8_0_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_qdot_q8_0_blocksums.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_q50_qdot.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_quantize_q50_qdot.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
@@ -67,8 +68,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pq_strerror.restype = ctypes.c_char_p
     lib.pq_version.argtypes = []
     for fn in ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
-               "pq_quantize_qdot_q8_0_noalloc", "pq_qdot_q8_0_blocksums", "pq_q50_qdot", "pq_quantize_q50_qdot",
-               "pq_q50_blocksums", "pq_check_device", "pq_version"):
+               "pq_quantize_qdot_q8_0_noalloc", "pq_quantize_qdot_q8_0_host", "pq_qdot_q8_0_blocksums",
+               "pq_q50_qdot", "pq_quantize_q50_qdot", "pq_q50_blocksums", "pq_check_device", "pq_version"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -161,6 +162,25 @@ def quantize_qdot_q8_0(x, W, WS, C=None, A=None, AS=None, ws_layout: int = WS_N_
     _check(load().pq_quantize_qdot_q8_0(_ptr(x), _ptr(A), _ptr(AS), _ptr(W), _ptr(WS), _ptr(C), M, N, K,
                                         int(ws_layout), _stream(stream)), "pq_quantize_qdot_q8_0")
     return C
+
+
+def quantize_qdot_q8_0_host(x_host, W, WS, C_host, ws_layout: int = WS_N_KB, stream=None):
+    """pq_quantize_qdot_q8_0_host: one decode step from host x_host [M, K] f32 into host C_host
+    [M, N] f32 (both page-locked CPU tensors); enqueued on the stream, which the caller
+    synchronizes before reading C_host."""
+    if x_host.dtype != torch.float32 or C_host.dtype != torch.float32:
+        raise TypeError("x_host and C_host must be float32")
+    if x_host.is_cuda or C_host.is_cuda:
+        raise ValueError("x_host and C_host must be host tensors")
+    if not (x_host.is_contiguous() and C_host.is_contiguous()):
+        raise ValueError("x_host and C_host must be contiguous")
+    M, K = x_host.shape
+    N = W.shape[0]
+    if tuple(C_host.shape) != (M, N):
+        raise ValueError("C_host must be [M, N]")
+    _check(load().pq_quantize_qdot_q8_0_host(x_host.data_ptr(), _ptr(W), _ptr(WS), C_host.data_ptr(), M, N, K,
+                                             int(ws_layout), _stream(stream)), "pq_quantize_qdot_q8_0_host")
+    return C_host
 
 
 def quantize_qdot_q8_0_noalloc(x, W, WS, C=None, ws_layout: int = WS_N_KB, stream=None):

@@ -45,13 +45,15 @@ cudaError_t device_workspace(size_t bytes, void** out) {
     return cudaSuccess;
 }
 
-// Per-(device, stream) workspaces (the tensor-core path's pre-tiled
-// activations): at most 64 pairs; allocated on the first call on a stream,
-// grown (cudaFree + cudaMalloc) when a larger one arrives, kept until exit.
-cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out) {
+// Per-(device, stream, kind) workspaces (kind 0: the tensor-core path's
+// pre-tiled activations; kind 1: the host-buffer step's device copies of x
+// and C): at most 64 triples; allocated on the first call on a stream, grown
+// (cudaFree + cudaMalloc) when a larger one arrives, kept until exit.
+cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out, int kind) {
     struct Slot {
         int dev;
         cudaStream_t stream;
+        int kind;
         void* ptr;
         size_t size;
     };
@@ -64,7 +66,7 @@ cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out) {
     std::lock_guard<std::mutex> lk(mu);
     Slot* sl = nullptr;
     for (int i = 0; i < nslots; ++i)
-        if (slots[i].dev == dev && slots[i].stream == stream) sl = &slots[i];
+        if (slots[i].dev == dev && slots[i].stream == stream && slots[i].kind == kind) sl = &slots[i];
     if (sl && sl->size >= bytes) {
         *out = sl->ptr;
         return cudaSuccess;
@@ -80,7 +82,7 @@ cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out) {
     if (!sl) {
         if (nslots == 64) return cudaErrorMemoryAllocation;
         sl = &slots[nslots++];
-        *sl = Slot{dev, stream, nullptr, 0};
+        *sl = Slot{dev, stream, kind, nullptr, 0};
     }
     if (sl->ptr) {
         e = cudaFree(sl->ptr);  // synchronizes the device: no earlier call still uses it
@@ -217,6 +219,30 @@ int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W,
     return qdot_impl(A, AS, W, WS, C, nullptr, M, N, K, ws_layout, PQ_PATH_AUTO, stream);
 }
 
+int pq_quantize_qdot_q8_0_host(const float* x_host, const int8_t* W, const float* WS, float* C_host, int64_t M,
+                               int64_t N, int64_t K, int ws_layout, cudaStream_t stream) {
+    if (ws_layout != PQ_WS_N_KB && ws_layout != PQ_WS_KB_N) return PQ_ERR_INVALID_ARG;
+    int st = check_qdot_shape(M, N, K);
+    if (st != PQ_OK) return st;
+    if (M == 0 || N == 0) return PQ_OK;
+    if (!x_host || !W || !WS || !C_host) return PQ_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(WS, 4)) return PQ_ERR_ALIGN;
+    // device copies of x and C in this stream's staging workspace
+    const size_t xbytes = static_cast<size_t>(M * K) * sizeof(float);
+    const size_t cbytes = static_cast<size_t>(M * N) * sizeof(float);
+    const size_t coff = (xbytes + 255) & ~size_t(255);
+    void* ws = nullptr;
+    cudaError_t e = pq::stream_workspace(stream, coff + cbytes, &ws, 1);
+    if (e != cudaSuccess) return map_cuda(e);
+    float* x = static_cast<float*>(ws);
+    float* C = reinterpret_cast<float*>(static_cast<char*>(ws) + coff);
+    e = cudaMemcpyAsync(x, x_host, xbytes, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return map_cuda(e);
+    st = pq_quantize_qdot_q8_0(x, nullptr, nullptr, W, WS, C, M, N, K, ws_layout, stream);
+    if (st != PQ_OK) return st;
+    return map_cuda(cudaMemcpyAsync(C_host, C, cbytes, cudaMemcpyDeviceToHost, stream));
+}
+
 int pq_qdot_q8_0_blocksums(const int8_t* A, const int8_t* W, int32_t* S, int64_t M, int64_t N,
                            int64_t K, int path, cudaStream_t stream) {
     int st = check_qdot_shape(M, N, K);
@@ -311,7 +337,7 @@ const char* pq_strerror(int code) {
     }
 }
 
-int pq_version(void) { return 103; }
+int pq_version(void) { return 104; }
 
 int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles) {
     if (skip_stage < -1) return PQ_ERR_INVALID_ARG;

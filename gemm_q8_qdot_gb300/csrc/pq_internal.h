@@ -91,7 +91,7 @@ cudaError_t device_workspace(size_t bytes, void** out);
 // it; allocated or grown on demand).  Fails without allocating while `stream`
 // is being captured and the workspace is too small, or when the table of
 // streams is full; callers then take a path that needs no workspace.
-cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out);
+cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out, int kind = 0);
 
 // qdot_t (automatic kernel path) without any device allocation; returns a pq_status.
 int qdot_noalloc(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C, int64_t M, int64_t N,

@@ -160,6 +160,22 @@ int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W,
                           float* C, int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);
 
 /*
+ * One decode step with the activations and the result in host memory: the
+ * host-to-device copy of x_host [M, K] f32, pq_quantize_qdot_q8_0 on that copy
+ * (A = AS = NULL), and the device-to-host copy of the result into C_host
+ * [M, N] f32, all enqueued on `stream` in that order.  The call returns once
+ * they are enqueued: synchronize the stream before reading C_host.  x_host and
+ * C_host should be page-locked (cudaHostAlloc or cudaHostRegister) for the
+ * copies to run asynchronously.  The device copies of x and C live in a
+ * workspace of this (device, stream) pair, allocated on the first call on the
+ * stream and grown when a larger one arrives (that call must not be inside a
+ * stream capture), kept until exit.  W, WS and the rules of the contraction
+ * as for pq_quantize_qdot_q8_0.
+ */
+int pq_quantize_qdot_q8_0_host(const float* x_host, const int8_t* W, const float* WS, float* C_host,
+                               int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);
+
+/*
  * pq_quantize_qdot_q8_0 without any device allocation.  (The Phobos pages
  * have no counterpart: this is a property of the library, not of the method.)
  *
@@ -261,7 +277,7 @@ int pq_check_device(cudaStream_t stream);
 const char* pq_strerror(int code);
 
 /* ABI version of this header: major * 100 + minor (1.01: pq_quantize_qdot_q8_0; 1.02: Q5_0 weights;
-   1.03: pq_quantize_q50_qdot and PQ_PATH_MMA). */
+   1.03: pq_quantize_q50_qdot and PQ_PATH_MMA; 1.04: pq_quantize_qdot_q8_0_host). */
 int pq_version(void);
 
 #ifdef __cplusplus

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert lib.pq_version() == 103
+    assert lib.pq_version() == 104
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert lib.pq_strerror(code).decode()
     assert "unknown" in lib.pq_strerror(99).decode()
@@ -160,3 +160,18 @@ def test_fused_q50_entry_checks(lib):
     assert fused_q50(lib, W5=P2) == binding.PQ_ERR_ALIGN
     assert fused_q50(lib, A=P8, AS=P16) == binding.PQ_ERR_ALIGN
     assert fused_q50(lib, layout=4) == binding.PQ_ERR_INVALID_ARG
+
+
+def host_step(lib, x=P16, W=P16, WS=P16, C=P16, M=1, N=1, K=32, layout=0):
+    return lib.pq_quantize_qdot_q8_0_host(x, W, WS, C, M, N, K, layout, None)
+
+
+def test_host_step_entry_checks(lib):
+    assert host_step(lib, K=40) == binding.PQ_ERR_SHAPE
+    assert host_step(lib, M=-3) == binding.PQ_ERR_SHAPE
+    assert host_step(lib, M=0, x=None, W=None, WS=None, C=None) == binding.PQ_OK
+    for which in ("x", "W", "WS", "C"):
+        assert host_step(lib, **{which: None}) == binding.PQ_ERR_INVALID_ARG
+    assert host_step(lib, W=P8) == binding.PQ_ERR_ALIGN
+    assert host_step(lib, WS=P2) == binding.PQ_ERR_ALIGN
+    assert host_step(lib, layout=9) == binding.PQ_ERR_INVALID_ARG

@@ -413,3 +413,37 @@ def test_quantize_qdot_workload_full(pq, name):
     rng = np.random.default_rng(2)
     cols = np.sort(rng.choice(N, min(N, 1024), replace=False))
     sampled_check(C, qa, sa, qw, sw, np.arange(M), cols, name)
+
+
+# ------------------------------------------------------------------ host-buffer decode step
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (1, 9800, 256), (4, 300, 1024), (1, 64, 256)])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_quantize_qdot_host_buffers(pq, M, N, K, layout):
+    """x and C in page-locked host memory: the copies and the step enqueued by one call;
+    the result matches the oracle on the quantized rows, and a second call of another
+    size on the same stream (workspace regrown) is correct too."""
+    rng = np.random.default_rng(M * 7 + N + K + layout)
+    x = (rng.standard_normal((M, K)) * np.exp(rng.uniform(-3, 3, size=(M, 1)))).astype(np.float32)
+    _, _, w, w_s = rand_operands(N + 5 * K, 1, N, K)
+    ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+    qa, sa = oracle.quantize_q8_0(x)
+    out, bound = oracle.qdot(qa, sa, w, w_s)
+    x_host = torch.from_numpy(x).pin_memory()
+    C_host = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.Stream()
+    W, WS = dev(w), dev(ws)
+    torch.cuda.synchronize()
+    pq.quantize_qdot_q8_0_host(x_host, W, WS, C_host, ws_layout=layout, stream=stream)
+    stream.synchronize()
+    pq.check_device()
+    assert_within_bound(C_host.numpy(), out, bound, f"host step M={M} N={N} K={K} layout={layout}")
+    # twice the rows on the same stream
+    x2 = np.concatenate([x, x[::-1] * 0.5]).astype(np.float32)
+    qa2, sa2 = oracle.quantize_q8_0(x2)
+    out2, bound2 = oracle.qdot(qa2, sa2, w, w_s)
+    C2 = torch.empty((2 * M, N), dtype=torch.float32).pin_memory()
+    pq.quantize_qdot_q8_0_host(torch.from_numpy(x2).pin_memory(), W, WS, C2, ws_layout=layout, stream=stream)
+    stream.synchronize()
+    pq.check_device()
+    assert_within_bound(C2.numpy(), out2, bound2, "host step, regrown workspace")
