@@ -159,7 +159,6 @@ struct Cfg {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;    // + alignment slack
     static constexpr int kOct = (BM + BN) / 8;            // row octets converted per f16 stage
-    static constexpr int kOctPerWarp = (kOct + NCONV - 1) / NCONV;
     static constexpr int kSplitPerThread = ((BM + BN) * 2 + NCONV * 32 - 1) / (NCONV * 32);
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
     static_assert(NEPI == 8, "epilogue warps: two column halves over the four TMEM lane quadrants");
