@@ -277,6 +277,16 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         r.nst = 2 * max(0, min(ngroups, r.g_begin + prm.groups_per_split) - r.g_begin);
         return r;
     };
+    // The CTA's units: round-robin for the 128-column tiles (the prompt shapes:
+    // CTAs running at the same time then share weight tiles in L2); a
+    // contiguous range for the narrow tiles, whose K is split, so that a tile's
+    // consecutive splits run on one CTA, which adds them in registers and
+    // writes the tile once.
+    const int u_first = ESC ? static_cast<int>(static_cast<int64_t>(blockIdx.x) * prm.units / gridDim.x)
+                            : static_cast<int>(blockIdx.x);
+    const int u_end = ESC ? static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * prm.units / gridDim.x)
+                          : prm.units;
+    const int u_step = ESC ? 1 : static_cast<int>(gridDim.x);
 
     pdl_trigger();
     if (threadIdx.x == 0) {
@@ -337,7 +347,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                                 (prm.has_scales ? (PREX ? 0 : CF::kXS) + CF::kYS : 0);
             int issued8 = 0, issued16 = 0;
             int gi = 0;  // int8-stage counter over all units of this CTA
-            for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
+            for (int u = u_first; u < u_end; u += u_step) {
                 const Unit un = unit(u);
                 const int n8 = un.nst / 2;
                 for (int i = 0; i < n8; ++i, ++gi) {
@@ -394,7 +404,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             constexpr uint32_t idesc_p = tc::idesc_bf16_f32(BM, BN);
             int g = 0, gi = 0;  // g: TMEM hand-offs (blocks, or ESC scale groups)
             bool gok = false;   // ESC: the group's buffer was free
-            for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
+            for (int u = u_first; u < u_end; u += u_step) {
                 const int nst = unit(u).nst;
                 for (int i = 0; i < nst; ++i, ++gi) {
                     const int s = gi % S16;
@@ -463,7 +473,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int r_in = lane & 7;      // row within an octet
         const int c4 = lane >> 3;       // 16-byte chunk within this half's 64 bytes of an int8 row
         int g8 = 0, g16 = 0;
-        for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
+        for (int u = u_first; u < u_end; u += u_step) {
             const int n8 = unit(u).nst / 2;
             for (int i = 0; i < n8; ++i, ++g8) {
                 const int s8 = g8 % S8;
@@ -607,7 +617,7 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         for (int t = 0; t < CF::kCW / 2; ++t) acc[t] = 0ull;
 
         int g = 0;  // block counter over all units of this CTA
-        for (int u = blockIdx.x; u < prm.units; u += gridDim.x) {
+        for (int u = u_first; u < u_end; u += u_step) {
             const Unit cu = unit(u);
             const int nblk = cu.nst * 2;
             const int64_t p = cu.p0 + prow;
@@ -718,9 +728,10 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                     if (lane == 0) tc::mbar_arrive(&tempty[buf]);
                 }
             }
+            // the tile's last unit on this CTA: write it and start the next from zero
+            const bool tile_end = !ESC || u + 1 >= u_end || (u + 1) / prm.splits != u / prm.splits;
             if constexpr (!SUMS) {
-                // the unit's last block: write its tile and start the next from zero
-                if (*abort_flag == 0 && pv) {
+                if (tile_end && *abort_flag == 0 && pv) {
                     float accf[CF::kCW];
 #pragma unroll
                     for (int t = 0; t < CF::kCW / 2; ++t) {
@@ -749,8 +760,10 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         }
                     }
                 }
+                if (tile_end) {
 #pragma unroll
-                for (int t = 0; t < CF::kCW / 2; ++t) acc[t] = 0ull;
+                    for (int t = 0; t < CF::kCW / 2; ++t) acc[t] = 0ull;
+                }
             }
         }
     }
