@@ -404,11 +404,14 @@ def time_e2e(prob: Problem, steps: int, warmup: int):
 
 
 def fused_is_one_kernel(prob: Problem) -> bool:
-    """Whether the one-call step (pq_quantize_qdot_q8_0 / pq_quantize_q50_qdot) runs as a
-    single fused kernel for this shape (one row, 32 columns per CTA, at most two waves)."""
+    """Whether the one-call step runs as a single fused kernel for this shape: one row
+    (pq_quantize_qdot_q8_0: any N, its CTAs take further columns beyond one per SM;
+    pq_quantize_q50_qdot: 32 columns per CTA, at most two waves)."""
     import torch
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    return prob.wl.M == 1 and -(-prob.wl.N // 32) <= 2 * sms
+    if prob.wl.M != 1:
+        return False
+    return -(-prob.wl.N // 32) <= 2 * sms if prob.q50 else True
 
 
 def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str, one_kernel: bool = False):

@@ -31,6 +31,7 @@
 //
 // SUMS = true instead stores every block sum S[i, j, b] as int32 (the
 // verification entry point pq_qdot_q8_0_blocksums).
+#include <algorithm>
 #include <atomic>
 
 #include "pq_internal.h"
@@ -207,7 +208,10 @@ cudaError_t launch_by_m(const QdotArgs& a, bool v8, cudaStream_t stream) {
 // When the quantized row is requested (A / AS), every CTA writes a few 16-byte
 // pieces of it from shared memory: a single writer CTA would be the last to
 // finish and delay the step.
-template <int U, bool V8, int WSL, int NW>
+// MULTI: N exceeds the grid (one CTA per SM), so each warp takes further
+// columns; otherwise one column per warp (the loop costs the single-column
+// grids ~3 %, measured).
+template <int U, bool V8, int WSL, int NW, bool MULTI>
 __global__ void __launch_bounds__(NW * 32)
 qdot_fused_kernel(FusedArgs p) {
     extern __shared__ __align__(16) uint8_t fsm[];
@@ -216,17 +220,22 @@ qdot_fused_kernel(FusedArgs p) {
     const int64_t N = p.N, K = p.K, KB = K >> 5;
     int8_t* a_s = reinterpret_cast<int8_t*>(fsm);           // [K]
     float* as_s = reinterpret_cast<float*>(fsm + K);        // [KB]
-    const int64_t j = static_cast<int64_t>(blockIdx.x) * NW + warp;
-    const bool jv = j < N;
+    // the warp's columns: j0, j0 + jstride, ... (one each unless N exceeds the grid)
+    const int64_t j0 = static_cast<int64_t>(blockIdx.x) * NW + warp;
+    const int64_t jstride = static_cast<int64_t>(gridDim.x) * NW;
+    int64_t j = j0;
+    bool jv = j < N;
     const int8_t* wrow = p.W + (jv ? j : 0) * K;
 
-    if (lane == 0 && jv) {
-        // the row's first kPrefetchBytes (the whole row up to K = 4096):
+    if (lane == 0) {
+        // each column's first kPrefetchBytes (the whole row up to K = 4096):
         // prefetching whole long rows (K = 14336) measured slower than this
         const int64_t kb = K < kPrefetchBytes ? K : kPrefetchBytes;
-        prefetch_l2(wrow, static_cast<uint32_t>(kb));
-        if (WSL == 0 && (reinterpret_cast<uintptr_t>(p.WS + j * KB) & 15) == 0 && (kb / 32 * 4) % 16 == 0)
-            prefetch_l2(p.WS + j * KB, static_cast<uint32_t>(kb / 32 * 4));
+        for (int64_t jj = j0; jj < (MULTI ? N : (j0 < N ? j0 + 1 : j0)); jj += jstride) {
+            prefetch_l2(p.W + jj * K, static_cast<uint32_t>(kb));
+            if (WSL == 0 && (reinterpret_cast<uintptr_t>(p.WS + jj * KB) & 15) == 0 && (kb / 32 * 4) % 16 == 0)
+                prefetch_l2(p.WS + jj * KB, static_cast<uint32_t>(kb / 32 * 4));
+        }
     }
     pdl_wait();
 
@@ -238,7 +247,7 @@ qdot_fused_kernel(FusedArgs p) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t b = bb + u * 32 + lane;
-            if (jv && b < KB) {
+            if (jv && b < KB) {  // jv: the first column exists (the later ones do by the loop)
                 wv[u] = ld_wblock<V8>(wrow + b * 32, wpol);
                 wsv[u] = ld_wscale(WSL == 0 ? p.WS + j * KB + b : p.WS + b * N + j, wpol);
             } else {
@@ -279,41 +288,50 @@ qdot_fused_kernel(FusedArgs p) {
         for (int64_t q = threadIdx.x * g + blockIdx.x; q < KB; q += kRound * g) p.AS[q] = as_s[q];
     }
     if (!jv) return;
-
-    float acc = 0.0f;
-    for (int64_t bb = 0; bb < KB; bb += 32 * U) {
-        if (bb > 0) load_round(bb);
+    for (;;) {
+        float acc = 0.0f;
+        for (int64_t bb = 0; bb < KB; bb += 32 * U) {
+            if (bb > 0) load_round(bb);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t b = bb + u * 32 + lane;
-            if (b >= KB) continue;
-            const uint4* pa = reinterpret_cast<const uint4*>(a_s + b * 32);
-            const uint4 a0 = pa[0], a1 = pa[1];
-            u32x8 av;
-            av.v[0] = a0.x; av.v[1] = a0.y; av.v[2] = a0.z; av.v[3] = a0.w;
-            av.v[4] = a1.x; av.v[5] = a1.y; av.v[6] = a1.z; av.v[7] = a1.w;
-            acc = fmaf(as_s[b] * wsv[u], static_cast<float>(block_dot(av, wv[u])), acc);
+            for (int u = 0; u < U; ++u) {
+                const int64_t b = bb + u * 32 + lane;
+                if (b >= KB) continue;
+                const uint4* pa = reinterpret_cast<const uint4*>(a_s + b * 32);
+                const uint4 a0 = pa[0], a1 = pa[1];
+                u32x8 av;
+                av.v[0] = a0.x; av.v[1] = a0.y; av.v[2] = a0.z; av.v[3] = a0.w;
+                av.v[4] = a1.x; av.v[5] = a1.y; av.v[6] = a1.z; av.v[7] = a1.w;
+                acc = fmaf(as_s[b] * wsv[u], static_cast<float>(block_dot(av, wv[u])), acc);
+            }
         }
+        const float v = warp_sum(acc);
+        if (lane == 0) p.C[j] = v;
+        if constexpr (!MULTI) break;
+        j += jstride;  // a further column: its first round (the first column's was loaded above)
+        if (j >= N) break;
+        wrow = p.W + j * K;
+        load_round(0);
     }
-    const float v = warp_sum(acc);
-    if (lane == 0) p.C[j] = v;
 }
 
 template <int U, int WSL, int NW>
-cudaError_t launch_fused(const FusedArgs& a, bool v8, cudaStream_t stream) {
+cudaError_t launch_fused(const FusedArgs& a, bool v8, int sms, cudaStream_t stream) {
     const size_t smem = static_cast<size_t>(a.K) + static_cast<size_t>(a.K / 32) * 4;
     if (smem > 200 * 1024) return cudaErrorNotSupported;
     // one output column per warp; NW warps per CTA quantize x once for NW columns
-    const int64_t grid = (a.N + NW - 1) / NW;
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    auto kern = v8 ? qdot_fused_kernel<U, true, WSL, NW> : qdot_fused_kernel<U, false, WSL, NW>;
+    // one CTA per SM at most (its 1024 or 896 threads hold the SM's registers);
+    // beyond that each warp takes further columns
+    const int64_t grid = std::min<int64_t>((a.N + NW - 1) / NW, sms);
+    const bool multi = (a.N + NW - 1) / NW > sms;
+    auto kern = v8 ? (multi ? qdot_fused_kernel<U, true, WSL, NW, true> : qdot_fused_kernel<U, true, WSL, NW, false>)
+                   : (multi ? qdot_fused_kernel<U, false, WSL, NW, true> : qdot_fused_kernel<U, false, WSL, NW, false>);
     // beyond the default 48 KB of dynamic shared memory (K > 43690) the kernel's
     // limit is raised once for the largest size met (it is per function, not per call)
     if (smem > 48 * 1024) {
-        static std::atomic<int> raised[64][2];  // per device (the attribute is set in its context)
+        static std::atomic<int> raised[64][4];  // per device (the attribute is set in its context) and kernel
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorNotSupported;
-        std::atomic<int>& r = raised[dev][v8 ? 1 : 0];
+        std::atomic<int>& r = raised[dev][(v8 ? 1 : 0) + (multi ? 2 : 0)];
         if (static_cast<int>(smem) > r.load()) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));
@@ -327,7 +345,8 @@ cudaError_t launch_fused(const FusedArgs& a, bool v8, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_qdot_fused(const FusedArgs& a, cudaStream_t stream) {
-    // one row (the decode step), at most two waves of CTAs (one 1024-thread CTA per SM)
+    // one row (the decode step); at most one CTA per SM, whose warps take further
+    // columns when N exceeds the grid
     if (a.M != 1) return cudaErrorNotSupported;
     // the SM count of each device, queried once
     static std::atomic<int> sm_count[64];
@@ -340,14 +359,12 @@ cudaError_t launch_qdot_fused(const FusedArgs& a, cudaStream_t stream) {
         sm_count[dev].store(sms, std::memory_order_relaxed);
     }
     const bool long_rows = a.K >= kLongRowK;
-    const int nw = long_rows ? kFusedWarpsLongRows : kFusedWarps;
-    if ((a.N + nw - 1) / nw > 2 * static_cast<int64_t>(sms)) return cudaErrorNotSupported;
     const bool v8 = (reinterpret_cast<uintptr_t>(a.W) & 31u) == 0;
     if (long_rows)
-        return a.ws_layout == 0 ? launch_fused<4, 0, kFusedWarpsLongRows>(a, v8, stream)
-                                : launch_fused<4, 1, kFusedWarpsLongRows>(a, v8, stream);
-    return a.ws_layout == 0 ? launch_fused<4, 0, kFusedWarps>(a, v8, stream)
-                            : launch_fused<4, 1, kFusedWarps>(a, v8, stream);
+        return a.ws_layout == 0 ? launch_fused<4, 0, kFusedWarpsLongRows>(a, v8, sms, stream)
+                                : launch_fused<4, 1, kFusedWarpsLongRows>(a, v8, sms, stream);
+    return a.ws_layout == 0 ? launch_fused<4, 0, kFusedWarps>(a, v8, sms, stream)
+                            : launch_fused<4, 1, kFusedWarps>(a, v8, sms, stream);
 }
 
 cudaError_t launch_qdot_simt(const QdotArgs& a, cudaStream_t stream) {

@@ -356,7 +356,9 @@ def test_qdot_workload_full_tc(pq, name):
 
 FUSED_SHAPES = [(1, 64, 256), (1, 300, 1056), (2, 17, 128), (3, 129, 512), (4, 64, 4096), (7, 33, 96),
                 (8, 257, 256), (1, 40, 14336), (1, 4000, 64), (1, 9000, 128), (1, 96, 49152),
-                (9, 130, 512), (16, 300, 4096)]
+                (9, 130, 512), (16, 300, 4096),
+                # one row, more columns than one CTA per SM holds: warps take further columns
+                (1, 14336, 4096), (1, 5000, 49152)]
 
 
 @pytest.mark.parametrize("M,N,K", FUSED_SHAPES)
