@@ -143,10 +143,11 @@ int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const flo
  * pq_qdot_q8_0_ex with the given weight-scale layout, automatic path) -- the
  * quantizer feeding qdot_t that "Quantized built-ins and formats", section
  * "Q8_0", describes ("the activations are quantized the same way").  For one
- * row (M == 1) and N up to 64 x the SM count this is one kernel, in which
- * every CTA quantizes x into its shared memory while L2 prefetches its weight
- * rows, then streams them; otherwise it is the quantizer followed by qdot_t,
- * launched so that the second overlaps the first.  A [M, K] int8 and AS [M, K/32] f32
+ * row (M == 1) this is one kernel, in which every CTA quantizes x into its
+ * shared memory while L2 prefetches its weight rows, then streams them (at
+ * most one CTA per SM; its warps take further columns when N needs more);
+ * otherwise it is the quantizer followed by qdot_t, launched so that the
+ * second overlaps the first.  A [M, K] int8 and AS [M, K/32] f32
  * optionally receive the quantized rows (both null, or both non-null).  When
  * they are null and the two-kernel route is taken, the rows go to a
  * per-device workspace that the library allocates on the first such call and
