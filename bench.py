@@ -361,12 +361,17 @@ def time_graph(prob: Problem, steps: int, warmup: int, world: int, sampler=None)
         with torch.cuda.stream(stream):
             gr.replay()
     torch.cuda.synchronize()
-    g_warm.replay()
-    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()  # before the warm replays: its thread start leaves no idle gap before timing
+    # warm replays of the W warm-up steps and of the timed steps themselves right
+    # before the timed replay, so that the GPU has no idle gap to fall out of its
+    # load state in; then the barrier (a no-op for one rank) and a synchronize
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+        g.replay()
+    stream.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    if sampler:
-        sampler.start()
     t0 = time.perf_counter()
     ms = _replay_ms(g, stream)
     t1 = time.perf_counter()
