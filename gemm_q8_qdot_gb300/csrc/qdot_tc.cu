@@ -775,6 +775,17 @@ qdot_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
 }
 
+// Zeroes C before a split-K contraction adds its partial tiles.  A kernel
+// rather than a memset node, so that it takes part in the programmatic
+// dependent launches: it starts while the previous kernel runs, and the
+// contraction kernel's prologue overlaps it.
+__global__ void __launch_bounds__(256) zero_f32_kernel(float* __restrict__ p, int64_t n) {
+    pdl_wait();  // the previous kernel may still read or write C
+    pdl_trigger();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = 0.0f;
+}
+
 // Pre-tiles the activation operand X = A [P, K] (with its scales AS [P, K/32])
 // for the PREX kernels: one CTA per (128-row tile, 64-K f16 stage) writes the
 // stage's f16 tile in the UMMA K-major 128-byte-swizzle layout (row r at r * 128
@@ -1048,7 +1059,9 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
     }
     cudaError_t e = cudaSuccess;
     if (prm.atomic) {
-        e = cudaMemsetAsync(a.C, 0, static_cast<size_t>(a.M * a.N) * sizeof(float), stream);
+        const int64_t n = a.M * a.N;
+        const int64_t blocks = std::min<int64_t>((n + 1023) / 1024, 2 * sms);
+        e = launch_pdl(zero_f32_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, a.C, n);
         if (e != cudaSuccess) return e;
     }
     // six converter warps (measured 8 % faster than four at M = 512; eight
