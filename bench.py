@@ -239,10 +239,10 @@ class Problem:
     """Device buffers of one workload: f32 activations, rotating Q8_0 weight copies, outputs.
 
     A step quantizes the activation rows and contracts them with the weights:
-    for M <= 8 through the one-call fused entry point (pq_quantize_qdot_q8_0,
-    or pq_quantize_q50_qdot for Q5_0 weights, which also writes the quantized
-    rows), otherwise pq_quantize_q8_0 then pq_qdot_q8_0 / pq_q50_qdot;
-    `fused=False` forces the two-call sequence.
+    for M <= 16 (M <= 8 with Q5_0 weights) through the one-call entry point
+    (pq_quantize_qdot_q8_0, or pq_quantize_q50_qdot for Q5_0 weights, which
+    also writes the quantized rows), otherwise pq_quantize_q8_0 then
+    pq_qdot_q8_0 / pq_q50_qdot; `fused=False` forces the two-call sequence.
     """
 
     def __init__(self, pq, wl: workloads.Workload, device, fused: bool = True):
@@ -250,7 +250,7 @@ class Problem:
         self.wl = wl
         self.pq = pq
         self.q50 = wl.w_format == "q5_0"
-        self.fused = fused and wl.M <= 8
+        self.fused = fused and wl.M <= (8 if self.q50 else 16)
         x = workloads.activations(wl)
         self.x_host = torch.from_numpy(x).pin_memory()
         if self.q50:
@@ -409,14 +409,15 @@ def time_e2e(prob: Problem, steps: int, warmup: int):
 
 
 def fused_is_one_kernel(prob: Problem) -> bool:
-    """Whether the one-call step runs as a single fused kernel for this shape: one row
-    (pq_quantize_qdot_q8_0: any N, its CTAs take further columns beyond one per SM;
-    pq_quantize_q50_qdot: 32 columns per CTA, at most two waves)."""
+    """Whether the one-call step runs as a single fused kernel for this shape:
+    pq_quantize_qdot_q8_0 for one row (any N, its CTAs take further columns beyond
+    one per SM) and for 9..16 rows (the warp-level MMA kernel quantizes the rows
+    itself); pq_quantize_q50_qdot for one row (32 columns per CTA, at most two waves)."""
     import torch
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    if prob.wl.M != 1:
-        return False
-    return -(-prob.wl.N // 32) <= 2 * sms if prob.q50 else True
+    if prob.q50:
+        return prob.wl.M == 1 and -(-prob.wl.N // 32) <= 2 * sms
+    return prob.wl.M == 1 or 9 <= prob.wl.M <= 16
 
 
 def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str, one_kernel: bool = False):
@@ -462,10 +463,11 @@ def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sample
     else:
         kernel_ms.update({"quantize": round(quant_ms, 5), "qdot": round(qdot_ms, 5)})
     # duration of the dominant kernel: a step that is one kernel (the fused decode
-    # step) is timed exactly by the step time; otherwise the mean launch of a graph
+    # step, or the fused step of 9..16 rows) is timed exactly by the step time;
+    # otherwise the mean launch of a graph
     # of that kernel alone (event-record nodes between kernels add their own
     # latency, so the in-graph event figure is an upper bound, reported beside it)
-    one_kernel = prob.fused and prob.wl.M == 1 and fused_is_one_kernel(prob)
+    one_kernel = prob.fused and fused_is_one_kernel(prob)
     dom_ms = (ms / steps) if one_kernel else qdot_only_ms
     kernel_ms["dominant"] = round(dom_ms, 5)
     res = {"value": round(value / scale, 3), "unit": unit, "ms_per_step": round(t_max * 1e3 / steps, 5),

@@ -204,6 +204,12 @@ int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W,
     pq::FusedArgs f{x, A, AS, W, WS, C, M, N, K, ws_layout};
     cudaError_t e = pq::launch_qdot_fused(f, stream);
     if (e != cudaErrorNotSupported) return map_cuda(e);
+    // 9..16 rows (the warp-level MMA path of qdot_t): one kernel as well, whose
+    // CTAs quantize the rows of their K ranges themselves
+    if (M > 8 && M <= 16) {
+        e = pq::launch_qdot_mma_fused(f, stream);
+        if (e != cudaErrorNotSupported) return map_cuda(e);
+    }
     // otherwise the quantizer, then qdot_t (the second launch overlaps the first);
     // the quantized rows go to A / AS, or to this device's workspace
     if (!A) {
@@ -337,7 +343,7 @@ const char* pq_strerror(int code) {
     }
 }
 
-int pq_version(void) { return 104; }
+int pq_version(void) { return 105; }
 
 int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles) {
     if (skip_stage < -1) return PQ_ERR_INVALID_ARG;

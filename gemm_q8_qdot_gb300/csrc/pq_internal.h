@@ -82,6 +82,11 @@ cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream);
 // 1 <= M <= 64; cudaErrorNotSupported otherwise.
 cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream);
 
+// Fused quantize + warp-level MMA contraction (1 <= M <= 64): every CTA
+// quantizes the rows of its K range itself; a.A / a.AS, when given, receive the
+// quantized rows.  cudaErrorNotSupported as for launch_qdot_mma.
+cudaError_t launch_qdot_mma_fused(const FusedArgs& a, cudaStream_t stream);
+
 // The current device's workspace of at least `bytes` (allocated on first use,
 // grown on demand, never freed before exit).
 cudaError_t device_workspace(size_t bytes, void** out);

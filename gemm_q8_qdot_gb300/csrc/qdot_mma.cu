@@ -30,6 +30,9 @@
 //   memory once; the warps read A fragments from there and the weights from
 //   global memory (8 bytes per lane and block, after an L2 prefetch of the
 //   CTA's rows issued before the launch waits on its predecessor).
+//   In the fused step the CTA quantizes the f32 activation rows of its K range
+//   itself, with the row quantizer's arithmetic, instead of reading A and AS;
+//   the CTAs of the first weight-row tile also store the quantized rows.
 //   K order inside a block: lane q of a row group holds k = 8q .. 8q + 7 of
 //   the block; MMA step 0 takes 8q .. 8q + 3 and step 1 takes 8q + 4 .. 8q + 7
 //   (as K positions 2q, 2q + 1, 2q + 8, 2q + 9).  Weights and activations use
@@ -63,6 +66,9 @@ struct MmaParams {
     const float* WS;    // WS[n * ws_r + b * ws_b]
     float* C;           // [M, N]
     int32_t* S;         // block-sum mode: [M, N, K/32]
+    const float* X;     // fused step: f32 [M, K] rows quantized in the staging (A, AS unused), or null
+    int8_t* Aq;         // fused step: optional outputs, the quantized rows [M, K] and their scales [M, K/32]
+    float* ASq;
     int64_t M, N, K;
     int64_t ws_r, ws_b;
     int nb;             // blocks per K split (the last split may have fewer)
@@ -192,7 +198,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MT, SUMS>()) qdot_
         }
     };
     if (ws_fast) ws_load(0);
-    {
+    if (SUMS || p.X == nullptr) {
         constexpr int kPass = 8;  // 16-byte chunks per lane per pass
         const int cpr = nbp * 2;  // chunks per row
         for (int base = 0; base < R * cpr; base += kMmaWarps * 32 * kPass) {
@@ -220,13 +226,60 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MT, SUMS>()) qdot_
                 }
             }
         }
+    } else {
+        // the fused step: two lanes per Q8_0 block, 16 floats each; the block's
+        // scale is the max over both lanes, then the quantizer's per-element
+        // rounding (bytes and scales bit-identical to pq_quantize_q8_0); rows
+        // past M and blocks past nb quantize zeros (q = 0, d = 0)
+        constexpr int kPass = 2;  // blocks halves per lane per pass
+        const int cpr = nbp * 2;  // 16-element chunks per row
+        const bool store_q = p.Aq != nullptr && blockIdx.x == 0;
+        for (int base = 0; base < R * cpr; base += kMmaWarps * 32 * kPass) {
+            float4 v[kPass][4];
+#pragma unroll
+            for (int j = 0; j < kPass; ++j) {
+                const int i = base + (j * kMmaWarps + warp) * 32 + lane;  // chunk index, row-major
+                const int r = i / cpr, c = i - r * cpr;
+                const bool live = i < R * cpr && r < p.M && c < nb * 2;
+                const float* src = p.X + r * p.K + static_cast<int64_t>(b0) * 32 + c * 16;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) v[j][h] = live ? ld_stream_f4(src + 4 * h) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < kPass; ++j) {
+                const int i = base + (j * kMmaWarps + warp) * 32 + lane;
+                const int r = i / cpr, c = i - r * cpr;
+                // lanes 2t and 2t + 1 hold one block (cpr is even); every lane takes part
+                const float d = q8_scale_of<2>(fmaxf(fmaxf(amax4(v[j][0]), amax4(v[j][1])),
+                                                     fmaxf(amax4(v[j][2]), amax4(v[j][3]))));
+                if (i < R * cpr) {
+                    const float rc = __frcp_rn(d);
+                    const uint4 q = make_uint4(q8_pack4(v[j][0], d, rc), q8_pack4(v[j][1], d, rc),
+                                               q8_pack4(v[j][2], d, rc), q8_pack4(v[j][3], d, rc));
+                    uint4 o0, o1;
+                    i8x4_to_f16x4(q.x, o0.x, o0.y);
+                    i8x4_to_f16x4(q.y, o0.z, o0.w);
+                    i8x4_to_f16x4(q.z, o1.x, o1.y);
+                    i8x4_to_f16x4(q.w, o1.z, o1.w);
+                    *reinterpret_cast<uint4*>(a16 + r * p.a_stride + c * 32) = o0;
+                    *reinterpret_cast<uint4*>(a16 + r * p.a_stride + c * 32 + 16) = o1;
+                    if ((lane & 1) == 0) as_s[(c >> 1) * R + r] = f2_pack(__float_as_uint(d), __float_as_uint(d));
+                    if (store_q && r < p.M && c < nb * 2) {
+                        *reinterpret_cast<uint4*>(p.Aq + r * p.K + static_cast<int64_t>(b0) * 32 + c * 16) = q;
+                        if ((lane & 1) == 0) p.ASq[r * static_cast<int64_t>(KB) + b0 + (c >> 1)] = d;
+                    }
+                }
+            }
+        }
     }
     if constexpr (!SUMS) {
+        if (p.X == nullptr) {
 #pragma unroll 4
-        for (int i = tid; i < nbp * R; i += kMmaThreads) {
-            const int b = i / R, r = i - b * R;
-            const float v = (r < p.M && b < nb) ? p.AS[r * static_cast<int64_t>(KB) + b0 + b] : 0.0f;
-            as_s[i] = f2_pack(__float_as_uint(v), __float_as_uint(v));
+            for (int i = tid; i < nbp * R; i += kMmaThreads) {
+                const int b = i / R, r = i - b * R;
+                const float v = (r < p.M && b < nb) ? p.AS[r * static_cast<int64_t>(KB) + b0 + b] : 0.0f;
+                as_s[i] = f2_pack(__float_as_uint(v), __float_as_uint(v));
+            }
         }
         if (ws_fast) {
             ws_store(0);
@@ -408,18 +461,17 @@ int sm_count_of_current_device() {
     return sms;
 }
 
-}  // namespace
-
-cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream) {
-    if (a.M < 1 || a.M > 64 || a.N < 1 || a.K % 32 != 0 || a.K > 0x7fffffffLL ||
-        a.N > 0x7fffffffLL * int64_t(kMmaRows))
+// Chooses the K split and launches; p holds the operands, the shape and the
+// weight-scale layout (ws_r, ws_b) on entry.
+cudaError_t launch_mma(MmaParams p, bool sums, cudaStream_t stream) {
+    if (p.M < 1 || p.M > 64 || p.N < 1 || p.K % 32 != 0 || p.K > 0x7fffffffLL ||
+        p.N > 0x7fffffffLL * int64_t(kMmaRows))
         return cudaErrorNotSupported;
-    const bool sums = a.S != nullptr;
     const int sms = sm_count_of_current_device();
     if (sms <= 0) return cudaErrorNotSupported;
-    const int MT = static_cast<int>((a.M + 15) / 16);
-    const int64_t KB = a.K / 32;
-    const int64_t tiles = (a.N + kMmaRows - 1) / kMmaRows;
+    const int MT = static_cast<int>((p.M + 15) / 16);
+    const int64_t KB = p.K / 32;
+    const int64_t tiles = (p.N + kMmaRows - 1) / kMmaRows;
     auto smem_of = [&](int64_t nb) {
         const int64_t nbp = (nb + kUnroll - 1) / kUnroll * kUnroll;
         const int a_stride = static_cast<int>((nbp * 64 + 127) / 128 * 128 + 64);
@@ -440,18 +492,6 @@ cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream) {
         ks = s;
         if (smem_of(nb) <= 44 * 1024 && tiles * s >= 4 * static_cast<int64_t>(sms)) break;
     }
-    MmaParams p{};
-    p.A = a.A;
-    p.AS = a.AS;
-    p.W = a.W;
-    p.WS = a.WS;
-    p.C = a.C;
-    p.S = a.S;
-    p.M = a.M;
-    p.N = a.N;
-    p.K = a.K;
-    p.ws_r = a.ws_layout == 0 ? KB : 1;
-    p.ws_b = a.ws_layout == 0 ? 1 : a.N;
     p.nb = static_cast<int>((KB + ks - 1) / ks);
     ks = static_cast<int>((KB + p.nb - 1) / p.nb);  // no empty split
     p.nbp = (p.nb + kUnroll - 1) / kUnroll * kUnroll;
@@ -463,6 +503,40 @@ cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream) {
         case 3: return sums ? launch_mt<3, true>(p, tiles, ks, stream) : launch_mt<3, false>(p, tiles, ks, stream);
         default: return sums ? launch_mt<4, true>(p, tiles, ks, stream) : launch_mt<4, false>(p, tiles, ks, stream);
     }
+}
+
+}  // namespace
+
+cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream) {
+    MmaParams p{};
+    p.A = a.A;
+    p.AS = a.AS;
+    p.W = a.W;
+    p.WS = a.WS;
+    p.C = a.C;
+    p.S = a.S;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.ws_r = a.ws_layout == 0 ? a.K / 32 : 1;
+    p.ws_b = a.ws_layout == 0 ? 1 : a.N;
+    return launch_mma(p, a.S != nullptr, stream);
+}
+
+cudaError_t launch_qdot_mma_fused(const FusedArgs& f, cudaStream_t stream) {
+    MmaParams p{};
+    p.X = f.x;
+    p.Aq = f.A;
+    p.ASq = f.AS;
+    p.W = f.W;
+    p.WS = f.WS;
+    p.C = f.C;
+    p.M = f.M;
+    p.N = f.N;
+    p.K = f.K;
+    p.ws_r = f.ws_layout == 0 ? f.K / 32 : 1;
+    p.ws_b = f.ws_layout == 0 ? 1 : f.N;
+    return launch_mma(p, false, stream);
 }
 
 }  // namespace pq

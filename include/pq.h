@@ -145,9 +145,11 @@ int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const flo
  * "Q8_0", describes ("the activations are quantized the same way").  For one
  * row (M == 1) this is one kernel, in which every CTA quantizes x into its
  * shared memory while L2 prefetches its weight rows, then streams them (at
- * most one CTA per SM; its warps take further columns when N needs more);
- * otherwise it is the quantizer followed by qdot_t, launched so that the
- * second overlaps the first.  A [M, K] int8 and AS [M, K/32] f32
+ * most one CTA per SM; its warps take further columns when N needs more).
+ * For 9 to 16 rows it is one kernel too: the warp-level MMA kernel of qdot_t,
+ * each of whose CTAs quantizes the rows of its K range itself.  Otherwise it
+ * is the quantizer followed by qdot_t, launched so that the second overlaps
+ * the first.  A [M, K] int8 and AS [M, K/32] f32
  * optionally receive the quantized rows (both null, or both non-null).  When
  * they are null and the two-kernel route is taken, the rows go to a
  * per-device workspace that the library allocates on the first such call and
@@ -278,7 +280,8 @@ int pq_check_device(cudaStream_t stream);
 const char* pq_strerror(int code);
 
 /* ABI version of this header: major * 100 + minor (1.01: pq_quantize_qdot_q8_0; 1.02: Q5_0 weights;
-   1.03: pq_quantize_q50_qdot and PQ_PATH_MMA; 1.04: pq_quantize_qdot_q8_0_host). */
+   1.03: pq_quantize_q50_qdot and PQ_PATH_MMA; 1.04: pq_quantize_qdot_q8_0_host; 1.05: one kernel
+   for 9..16 rows in pq_quantize_qdot_q8_0). */
 int pq_version(void);
 
 #ifdef __cplusplus

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert lib.pq_version() == 104
+    assert lib.pq_version() == 105
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert lib.pq_strerror(code).decode()
     assert "unknown" in lib.pq_strerror(99).decode()

@@ -107,3 +107,56 @@ def test_qdot_mma_workload_full(pq, name):
     cols = np.unique(np.concatenate([rng.choice(N, 512, replace=False), [0, N - 1]]))
     sampled_check(C, qa, sa, qw, sw, np.arange(M), cols, name)
     assert torch.isfinite(C).all()
+
+
+# ------------------------------------------------------------------ fused step, 9..16 rows
+
+@pytest.mark.parametrize("M,N,K", [(9, 300, 1024), (12, 1000, 4096), (16, 129, 96), (14, 700, 14336)])
+def test_fused_step_equals_quantizer_then_mma(pq, M, N, K):
+    """pq_quantize_qdot_q8_0 at 9..16 rows quantizes inside the MMA kernel: its rows,
+    scales and C are bit-identical to the quantizer followed by this path's qdot_t."""
+    rng = np.random.default_rng(M * 17 + N + K)
+    x = (rng.standard_normal((M, K)) * np.exp(rng.uniform(-4, 4, size=(M, 1)))).astype(np.float32)
+    x[1, :64] = 0.0  # two all-zero blocks: d = 0, q = 0
+    _, _, w, w_s = rand_operands(N + K, 1, N, K)
+    X, W, WS = dev(x), dev(w), dev(w_s)
+    A = torch.full((M, K), 77, dtype=torch.int8, device="cuda:0")
+    AS = torch.full((M, K // 32), -1.0, dtype=torch.float32, device="cuda:0")
+    C = pq.quantize_qdot_q8_0(X, W, WS, A=A, AS=AS)
+    A2, AS2 = pq.quantize_q8_0(X)
+    C2 = pq.qdot_q8_0_ex(A2, AS2, W, WS, path=pq.PATH_MMA)
+    pq.check_device()
+    assert torch.equal(A, A2) and torch.equal(AS, AS2)
+    assert torch.equal(C, C2)
+    qa, sa = oracle.quantize_q8_0(x)
+    out, bound = oracle.qdot(qa, sa, w, w_s)
+    assert_within_bound(C, out, bound, f"fused mma M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M", [12, 16])
+def test_fused_step_in_a_graph(pq, M):
+    """The one-kernel step captured once and replayed on new activations: each replay
+    quantizes the rows it finds in x."""
+    N, K = 600, 2048
+    _, _, w, w_s = rand_operands(5, 1, N, K)
+    W, WS = dev(w), dev(w_s)
+    X = torch.empty((M, K), dtype=torch.float32, device="cuda:0")
+    A = torch.empty((M, K), dtype=torch.int8, device="cuda:0")
+    AS = torch.empty((M, K // 32), dtype=torch.float32, device="cuda:0")
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda:0")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        pq.quantize_qdot_q8_0(X, W, WS, C, A=A, AS=AS)
+    rng = np.random.default_rng(M)
+    for _ in range(2):
+        x = (rng.standard_normal((M, K)) * 3.0).astype(np.float32)
+        X.copy_(torch.from_numpy(x))
+        g.replay()
+        torch.cuda.synchronize()
+        pq.check_device()
+        qa, sa = oracle.quantize_q8_0(x)
+        assert np.array_equal(host(A), qa) and np.array_equal(host(AS).view(np.uint32), sa.view(np.uint32))
+        out, bound = oracle.qdot(qa, sa, w, w_s)
+        assert_within_bound(C, out, bound, "graph replay")

@@ -122,7 +122,7 @@ def near_tie_rows(rows, K, seed):
     return x
 
 
-@pytest.mark.parametrize("rows,K", [(1, 4096), (1, 14336), (3, 1024), (64, 256)])
+@pytest.mark.parametrize("rows,K", [(1, 4096), (1, 14336), (3, 1024), (64, 256), (12, 2048), (16, 512)])
 def test_quantize_near_ties(pq, rows, K):
     """The quantizer's rounding against the oracle's IEEE division on near-tie quotients:
     the standalone quantizer and the fused step's quantized rows, bit for bit."""
@@ -356,7 +356,10 @@ def test_qdot_workload_full_tc(pq, name):
 
 FUSED_SHAPES = [(1, 64, 256), (1, 300, 1056), (2, 17, 128), (3, 129, 512), (4, 64, 4096), (7, 33, 96),
                 (8, 257, 256), (1, 40, 14336), (1, 4000, 64), (1, 9000, 128), (1, 96, 49152),
-                (9, 130, 512), (16, 300, 4096),
+                # 9..16 rows: the warp-level MMA kernel quantizes the rows itself (one split,
+                # several splits, a short last split, ragged N, long K)
+                (9, 130, 512), (16, 300, 4096), (10, 5, 32), (15, 129, 96), (12, 333, 2048),
+                (13, 1000, 4096), (16, 2000, 14336), (11, 64, 1056),
                 # one row, more columns than one CTA per SM holds: warps take further columns
                 (1, 14336, 4096), (1, 5000, 49152)]
 
@@ -401,7 +404,7 @@ def test_quantize_qdot_large_m(pq):
     assert_within_bound(C, out, bound, "two-kernel route")
 
 
-@pytest.mark.parametrize("name", [n for n in workloads.Q8_WORKLOADS if workloads.Q8_WORKLOADS[n].M <= 8])
+@pytest.mark.parametrize("name", [n for n in workloads.Q8_WORKLOADS if workloads.Q8_WORKLOADS[n].M <= 16])
 def test_quantize_qdot_workload_full(pq, name):
     """Decode / small-batch workloads at full size through the one-call step."""
     x, w, qa, sa, qw, sw = quantized_workload(name)
