@@ -422,7 +422,7 @@ def test_quantize_qdot_workload_full(pq, name):
 
 # ------------------------------------------------------------------ host-buffer decode step
 
-@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (1, 9800, 256), (4, 300, 1024), (1, 64, 256)])
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (1, 9800, 256), (4, 300, 1024), (1, 64, 256), (12, 500, 1024)])
 @pytest.mark.parametrize("layout", [0, 1])
 def test_quantize_qdot_host_buffers(pq, M, N, K, layout):
     """x and C in page-locked host memory: the copies and the step enqueued by one call;
