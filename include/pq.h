@@ -157,7 +157,7 @@ int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const flo
  * capture); the workspace is shared by all calls on the device, so calls of
  * this kind must not overlap on different streams.  x: 16-byte aligned f32
  * [M, K]; A 16-byte aligned; AS, WS, C 4-byte aligned.  C must not overlap
- * any input.
+ * any input, and A, AS must not overlap x, W, WS or C.
  */
 int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W, const float* WS,
                           float* C, int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);
