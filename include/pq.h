@@ -191,6 +191,8 @@ int pq_quantize_qdot_q8_0_host(const float* x_host, const int8_t* W, const float
  * automatic path), but the quantized rows and their scales are kept in a
  * fixed array of PQ_NOALLOC_SCRATCH_BYTES (1 MiB) that is part of the library
  * and that every GPU which loads the library holds until the process exits.
+ * Where pq_quantize_qdot_q8_0 runs one kernel (one row; 9 to 16 rows) this
+ * call runs the same kernel and leaves the array alone.
  * The caller still passes x, W, WS and C (same layouts and alignment as
  * pq_quantize_qdot_q8_0); nothing else is allocated, by this call or by the
  * kernels it starts.
