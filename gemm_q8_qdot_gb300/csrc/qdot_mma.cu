@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MT, SUMS>()) qdot_
         // scale is the max over both lanes, then the quantizer's per-element
         // rounding (bytes and scales bit-identical to pq_quantize_q8_0); rows
         // past M and blocks past nb quantize zeros (q = 0, d = 0)
-        constexpr int kPass = 2;  // blocks halves per lane per pass
+        constexpr int kPass = 2;  // block halves per lane per pass
         const int cpr = nbp * 2;  // 16-element chunks per row
         const bool store_q = p.Aq != nullptr && blockIdx.x == 0;
         for (int base = 0; base < R * cpr; base += kMmaWarps * 32 * kPass) {
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_min_blocks<MT, SUMS>()) qdot_
                 const int i = base + (j * kMmaWarps + warp) * 32 + lane;  // chunk index, row-major
                 const int r = i / cpr, c = i - r * cpr;
                 const bool live = i < R * cpr && r < p.M && c < nb * 2;
-                const float* src = p.X + r * p.K + static_cast<int64_t>(b0) * 32 + c * 16;
+                const float* src = p.X + (live ? r * p.K + static_cast<int64_t>(b0) * 32 + c * 16 : 0);
 #pragma unroll
                 for (int h = 0; h < 4; ++h) v[j][h] = live ? ld_stream_f4(src + 4 * h) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
