@@ -523,63 +523,182 @@ def int8_library_rate():
         return None
 
 
-def cpu_baseline(name: str, budget_s: float = 10.0):
-    """The oracle, as it stands, on a bounded sample of the workload (rank 0, host cores)."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the Arm part code)."""
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return f"implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return "unknown"
+
+
+def _oracle_rate(wl, omp: bool, budget_s: float):
+    """One bounded sample of the workload on the oracle: the activation rows quantized and
+    contracted with the first n weight rows, n grown until one step takes about budget_s / 3;
+    returns (units per second in the workload's unit, n, steps, seconds)."""
     import oracle
-    wl = workloads.WORKLOADS[name]
     x = workloads.activations(wl)
-    qw, sw = oracle.quantize_q8_0(workloads.weights(wl))
+    per_col = 1.125 * wl.K if wl.M <= 64 else 2.0 * wl.M * wl.K  # weight bytes or ops per column
+    scale = 1e9 if wl.M <= 64 else 1e12
+    n = min(wl.N, 16)
+    while True:
+        if wl.w_format == "q5_0":
+            w5, ws = workloads.q50_weights(wl, N=n)
+        else:
+            qw, sw = oracle.quantize_q8_0(workloads.weights(wl, N=n), omp=omp)
+        t0 = time.perf_counter()
+        qa, sa = oracle.quantize_q8_0(x, omp=omp)
+        if wl.w_format == "q5_0":
+            oracle.qdot_q5_0(qa, sa, w5, ws, omp=omp)
+        else:
+            oracle.qdot(qa, sa, qw, sw, omp=omp)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 3 or n == wl.N:
+            break
+        n = min(wl.N, max(n + 1, int(n * min(16.0, budget_s / 3 / max(dt, 1e-6)))))
     steps, t0 = 0, time.perf_counter()
     while True:
-        qa, sa = oracle.quantize_q8_0(x)
-        oracle.qdot(qa, sa, qw, sw)
+        qa, sa = oracle.quantize_q8_0(x, omp=omp)
+        if wl.w_format == "q5_0":
+            oracle.qdot_q5_0(qa, sa, w5, ws, omp=omp)
+        else:
+            oracle.qdot(qa, sa, qw, sw, omp=omp)
         steps += 1
         dt = time.perf_counter() - t0
-        if dt >= budget_s:
+        if dt >= budget_s * 2 / 3:
             break
-    return {"value": round(wl.weight_bytes * steps / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
-            "kind": "oracle", "sample": f"{steps} full steps of {name} (quantize x + qdot_t, single thread) "
-                                        f"in {dt:.1f} s"}
+    unit_bytes = wl.weight_bytes / wl.N if wl.M <= 64 else per_col
+    return unit_bytes * n * steps / dt / scale, n, steps, dt
+
+
+def oracle_threads():
+    """(True, threads) when the oracle's OpenMP build loads, else (False, 1)."""
+    import oracle
+    try:
+        return True, oracle.threads(True)
+    except Exception:  # no OpenMP runtime: the single-thread build is the baseline
+        return False, 1
+
+
+def cpu_baseline(name: str, budget_s: float = 4.0):
+    """The oracle, as it stands, on a bounded sample of the workload (rank 0, host cores):
+    the OpenMP build on every host core (the reported value) and the single-thread build
+    beside it."""
+    wl = workloads.WORKLOADS[name]
+    omp, cores = oracle_threads()
+    v_all, n_all, st_all, dt_all = _oracle_rate(wl, omp, budget_s)
+    v_one, n_one, st_one, dt_one = _oracle_rate(wl, False, budget_s)
+    unit = "GB/s" if wl.M <= 64 else "TOPS"
+    return {"value": round(v_all, 5), "unit": unit, "cores": cores, "kind": "oracle",
+            "cpu": cpu_model(), "single_thread": round(v_one, 5),
+            "sample": f"{name}: x quantized + contracted with the first {n_all} of {wl.N} weight rows, "
+                      f"{st_all} steps in {dt_all:.1f} s on every core; single thread {n_one} rows, "
+                      f"{st_one} steps in {dt_one:.1f} s"}
 
 
 def reference_arm(args):
-    """--impl reference: the CPU oracle on the headline workload, on the host cores."""
+    """--impl reference: the CPU oracle (OpenMP build, every host core) on the headline
+    workload and metric, a bounded sample of weight rows per step."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     import oracle
+    omp, cores = oracle_threads()
     wl = workloads.WORKLOADS[args.workload]
     x = workloads.activations(wl)
-    qw, sw = oracle.quantize_q8_0(workloads.weights(wl))
+    qw, sw = oracle.quantize_q8_0(workloads.weights(wl), omp=omp)
     # calibrate one full step; sample columns so that W + K steps stay near 60 s
     t0 = time.perf_counter()
-    qa, sa = oracle.quantize_q8_0(x)
-    oracle.qdot(qa, sa, qw, sw)
+    qa, sa = oracle.quantize_q8_0(x, omp=omp)
+    oracle.qdot(qa, sa, qw, sw, omp=omp)
     full = time.perf_counter() - t0
     budget = 60.0
     frac = min(1.0, budget / max(1e-9, full * (args.steps + args.warmup)))
     ncols = max(1, int(wl.N * frac))
     qw_s, sw_s = qw[:ncols], sw[:ncols]
     for _ in range(args.warmup):
-        qa, sa = oracle.quantize_q8_0(x)
-        oracle.qdot(qa, sa, qw_s, sw_s)
+        qa, sa = oracle.quantize_q8_0(x, omp=omp)
+        oracle.qdot(qa, sa, qw_s, sw_s, omp=omp)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        qa, sa = oracle.quantize_q8_0(x)
-        oracle.qdot(qa, sa, qw_s, sw_s)
+        qa, sa = oracle.quantize_q8_0(x, omp=omp)
+        oracle.qdot(qa, sa, qw_s, sw_s, omp=omp)
     dt = time.perf_counter() - t0
-    wbytes = ncols * wl.K + 4 * ncols * (wl.K // 32)
-    value = wbytes * args.steps / dt / 1e9
-    sample = f"{ncols} of {wl.N} weight rows per step ({args.steps} steps, single thread)"
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+    if wl.M <= 64:
+        units, unit, scale = ncols * wl.K + 4 * ncols * (wl.K // 32), "GB/s", 1e9
+    else:
+        units, unit, scale = 2 * wl.M * ncols * wl.K, "TOPS", 1e12
+    value = units * args.steps / dt / scale
+    sample = f"{ncols} of {wl.N} weight rows per step ({args.steps} steps, {cores} threads)"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64/f64",
             "data": "synthetic", "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
-            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": cores, "kind": "oracle",
+                             "cpu": cpu_model(), "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+WORKLOAD_FIELDS = ["value", "unit", "ms_per_step", "roofline_frac", "cpu_baseline_value"]
+
+
+def compact(res: dict, cpu: dict | None = None):
+    """One workload's figures for the final line, in the order of WORKLOAD_FIELDS."""
+    if "error" in res:
+        return {"error": res["error"][:80]}
+    return [res["value"], res["unit"], res["ms_per_step"], round(res["roofline"]["frac"], 4),
+            float(f"{cpu['value']:.4g}") if cpu else None]
+
+
+def final_line(head: dict, others: dict, cpus: dict, args, world: int, clocks: dict) -> dict:
+    """The one JSON line: the contract's keys for the headline workload, then the prompt GEMM
+    (the metric's second half) and a compact figure per workload as the last keys, so that
+    the end of the line carries every workload."""
+    wl = workloads.WORKLOADS[args.workload]
+    launches_per_step = 1 if head["step"].endswith("(one kernel)") else 2
+    line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "M": wl.M, "K": wl.K, "N": wl.N,
+                       "parallelism": head.get("parallelism", "single"),
+                       "l2": f"{head['weight_copies']} rotating weight copies (>= 2x L2)",
+                       "timing": "K steps in one CUDA graph, events on the launching stream"},
+            "roofline": head["roofline"], "e2e": head["e2e"], "step": head["step"],
+            "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
+    if args.workload in cpus:
+        line["cpu_baseline"] = cpus[args.workload]
+    prompt = head if args.workload == PROMPT else others.get(PROMPT)
+    if prompt and "roofline" in prompt:
+        rl = {k: prompt["roofline"][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+        for k in ("int8_library_tops", "frac_of_int8_library"):
+            if k in prompt["roofline"]:
+                rl[k] = prompt["roofline"][k]
+        line["prompt"] = {"workload": PROMPT, "value": prompt["value"], "unit": prompt["unit"],
+                          "ms_per_step": prompt["ms_per_step"], "roofline": rl}
+    allres = {args.workload: head, **others}
+    line["workloads"] = {"fields": WORKLOAD_FIELDS,
+                         **{n: compact(r, cpus.get(n)) for n, r in allres.items()}}
+    return line
 
 
 def main(argv=None):
@@ -628,24 +747,15 @@ def main(argv=None):
             rl = prompt_res["roofline"]
             rl["int8_library_tops"] = rate
             rl["frac_of_int8_library"] = round(rl["achieved"] / rate, 3)
-    launches_per_step = 1 if head["step"].endswith("(one kernel)") else 2
-    line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
-            "data": "synthetic",
-            "config": {"workload": args.workload, "M": workloads.WORKLOADS[args.workload].M,
-                       "K": workloads.WORKLOADS[args.workload].K, "N": workloads.WORKLOADS[args.workload].N,
-                       "parallelism": f"replicas{world}" if world > 1 else "single",
-                       "l2": f"{head['weight_copies']} rotating weight copies (>= 2x L2 = {2 * L2_BYTES >> 20} MiB)",
-                       "timing": "K steps in one CUDA graph, events on the launching stream"},
-            "roofline": head["roofline"], "kernel_ms": head["kernel_ms"], "e2e": head["e2e"],
-            "step": head["step"], "two_call": head.get("two_call"),
-            "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
-    if others:
-        line["other_workloads"] = others
+    cpus = {}
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload)
+        for name in [args.workload] + [n for n in others if "error" not in others[n]]:
+            cpus[name] = cpu_baseline(name, 6.0 if name == args.workload else 2.0)
+    line = final_line(head, others, cpus, args, world, clocks)
     if rank == 0:
+        # every figure of every workload, on stderr; stdout carries the one line
+        print("bench detail: " + json.dumps({"headline": {args.workload: head}, "others": others,
+                                             "cpu_baseline": cpus}), file=sys.stderr, flush=True)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -1,7 +1,7 @@
 // Allocation-free form of the one-call decode step (pq_quantize_qdot_q8_0).
 //
 // pq_quantize_qdot_q8_0 keeps the quantized activation rows in a workspace it
-// allocates with cudaMalloc on first use.  Some callers cannot let a library
+// allocates (cudaMallocAsync) on first use.  Some callers cannot let a library
 // allocate device memory: code that records its work into a CUDA graph
 // (allocation is not allowed while a stream is being captured), serving loops
 // that must never stall on cudaMalloc / cudaFree (both can synchronize the
@@ -61,7 +61,9 @@ extern "C" int pq_quantize_qdot_q8_0_noalloc(const float* x, const int8_t* W, co
                                              int64_t M, int64_t N, int64_t K, int ws_layout,
                                              cudaStream_t stream) {
     if (ws_layout != PQ_WS_N_KB && ws_layout != PQ_WS_KB_N) return PQ_ERR_INVALID_ARG;
-    if (M < 0 || N < 0 || K <= 0 || (K % 32) != 0) return PQ_ERR_SHAPE;
+    // the same shape rules as the allocating entry point
+    const int shape = pq::check_qdot_shape(M, N, K);
+    if (shape != PQ_OK) return shape;
     if (M == 0 || N == 0) return PQ_OK;
     // the quantized rows and their scales must fit the fixed array
     if (M > static_cast<int64_t>(kScratchBytes) || K > static_cast<int64_t>(kScratchBytes)) return PQ_ERR_SCRATCH;

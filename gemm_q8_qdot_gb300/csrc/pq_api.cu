@@ -14,41 +14,19 @@
 
 namespace pq {
 
-// Per-device workspace for the quantized rows of pq_quantize_qdot_q8_0 calls
-// that do not pass A / AS: allocated on the first such call on a device,
-// grown (cudaFree + cudaMalloc) when a larger one arrives, kept until exit.
-cudaError_t device_workspace(size_t bytes, void** out) {
-    static std::mutex mu;
-    static void* ptr[64] = {};
-    static size_t have[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(mu);
-    if (have[dev] < bytes) {
-        if (ptr[dev]) {
-            e = cudaFree(ptr[dev]);  // synchronizes the device: no earlier call still uses it
-            if (e != cudaSuccess) return e;
-            ptr[dev] = nullptr;
-            have[dev] = 0;
-        }
-        const size_t want = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
-        e = cudaMalloc(&ptr[dev], want);
-        if (e != cudaSuccess) {
-            ptr[dev] = nullptr;
-            return e;
-        }
-        have[dev] = want;
-    }
-    *out = ptr[dev];
-    return cudaSuccess;
-}
-
 // Per-(device, stream, kind) workspaces (kind 0: the tensor-core path's
 // pre-tiled activations; kind 1: the host-buffer step's device copies of x
-// and C): at most 64 triples; allocated on the first call on a stream, grown
-// (cudaFree + cudaMalloc) when a larger one arrives, kept until exit.
+// and C; kind 2: the quantized rows of a two-kernel pq_quantize_qdot_q8_0 /
+// pq_quantize_q50_qdot call without A / AS), at most 64 triples.
+//
+// A workspace is allocated on the first call that needs it on its stream,
+// with cudaMallocAsync on that stream: the allocation is ordered with the
+// stream's work and synchronizes nothing else.  A larger call replaces it by
+// one at least twice as large; the replaced one is kept (never freed before
+// exit), so work enqueued earlier on the stream, and graphs captured earlier
+// that refer to it, stay valid, and no call ever waits on a cudaFree.  With
+// the doubling, the replaced workspaces of a triple add up to less than its
+// current one.
 cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out, int kind) {
     struct Slot {
         int dev;
@@ -60,6 +38,8 @@ cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out, int 
     static std::mutex mu;
     static Slot slots[64];
     static int nslots = 0;
+    static void* retired[64 * 48] = {};  // replaced workspaces, kept until exit
+    static int nretired = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -71,7 +51,7 @@ cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out, int 
         *out = sl->ptr;
         return cudaSuccess;
     }
-    // allocating (or freeing) is not allowed while the stream is being captured
+    // allocating is not allowed while the stream is being captured
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     e = cudaStreamIsCapturing(stream, &cs);
     if (e != cudaSuccess) {
@@ -79,26 +59,24 @@ cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out, int 
         return e;
     }
     if (cs != cudaStreamCaptureStatusNone) return cudaErrorNotPermitted;
-    if (!sl) {
-        if (nslots == 64) return cudaErrorMemoryAllocation;
-        sl = &slots[nslots++];
-        *sl = Slot{dev, stream, kind, nullptr, 0};
-    }
-    if (sl->ptr) {
-        e = cudaFree(sl->ptr);  // synchronizes the device: no earlier call still uses it
-        if (e != cudaSuccess) return e;
-        sl->ptr = nullptr;
-        sl->size = 0;
-    }
-    const size_t want = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
-    e = cudaMalloc(&sl->ptr, want);
+    if (!sl && nslots == 64) return cudaErrorMemoryAllocation;
+    if (sl && sl->ptr && nretired == 64 * 48) return cudaErrorMemoryAllocation;
+    size_t want = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
+    if (sl && want < 2 * sl->size) want = 2 * sl->size;
+    void* p = nullptr;
+    e = cudaMallocAsync(&p, want, stream);
     if (e != cudaSuccess) {
-        sl->ptr = nullptr;
         cudaGetLastError();
         return e;
     }
+    if (!sl) {
+        sl = &slots[nslots++];
+        *sl = Slot{dev, stream, kind, nullptr, 0};
+    }
+    if (sl->ptr) retired[nretired++] = sl->ptr;
+    sl->ptr = p;
     sl->size = want;
-    *out = sl->ptr;
+    *out = p;
     return cudaSuccess;
 }
 
@@ -116,9 +94,11 @@ int map_cuda(cudaError_t e) {
     return PQ_ERR_CUDA;
 }
 
+}  // namespace
+
 // Shape checks shared by the qdot entry points: sizes >= 0, K a positive
 // multiple of 32, every element count representable.
-int check_qdot_shape(int64_t M, int64_t N, int64_t K) {
+int pq::check_qdot_shape(int64_t M, int64_t N, int64_t K) {
     if (M < 0 || N < 0 || K <= 0 || (K % 32) != 0) return PQ_ERR_SHAPE;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return PQ_ERR_SHAPE;
     // M*K, N*K, M*N and M*N*K/32 must fit in int64
@@ -127,6 +107,10 @@ int check_qdot_shape(int64_t M, int64_t N, int64_t K) {
     if (mk > lim || nk > lim || mn > lim || mn * (K / 32) > lim) return PQ_ERR_SHAPE;
     return PQ_OK;
 }
+
+namespace {
+
+using pq::check_qdot_shape;
 
 int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C,
               int32_t* S, int64_t M, int64_t N, int64_t K, int ws_layout, int path,
@@ -211,11 +195,11 @@ int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W,
         if (e != cudaErrorNotSupported) return map_cuda(e);
     }
     // otherwise the quantizer, then qdot_t (the second launch overlaps the first);
-    // the quantized rows go to A / AS, or to this device's workspace
+    // the quantized rows go to A / AS, or to this stream's workspace
     if (!A) {
         void* ws = nullptr;
         const size_t qbytes = (static_cast<size_t>(M * K) + 255) & ~size_t(255);
-        e = pq::device_workspace(qbytes + static_cast<size_t>(M * (K / 32)) * sizeof(float), &ws);
+        e = pq::stream_workspace(stream, qbytes + static_cast<size_t>(M * (K / 32)) * sizeof(float), &ws, 2);
         if (e != cudaSuccess) return map_cuda(e);
         A = static_cast<int8_t*>(ws);
         AS = reinterpret_cast<float*>(static_cast<char*>(ws) + qbytes);
@@ -296,11 +280,11 @@ int pq_quantize_q50_qdot(const float* x, int8_t* A, float* AS, const uint8_t* W5
     cudaError_t e = pq::launch_qdot_q50_fused(f, stream);
     if (e != cudaErrorNotSupported) return map_cuda(e);
     // otherwise the quantizer, then q50_qdot_t; the quantized rows go to A / AS,
-    // or to this device's workspace
+    // or to this stream's workspace
     if (!A) {
         void* ws = nullptr;
         const size_t qbytes = (static_cast<size_t>(M * K) + 255) & ~size_t(255);
-        e = pq::device_workspace(qbytes + static_cast<size_t>(M * (K / 32)) * sizeof(float), &ws);
+        e = pq::stream_workspace(stream, qbytes + static_cast<size_t>(M * (K / 32)) * sizeof(float), &ws, 2);
         if (e != cudaSuccess) return map_cuda(e);
         A = static_cast<int8_t*>(ws);
         AS = reinterpret_cast<float*>(static_cast<char*>(ws) + qbytes);

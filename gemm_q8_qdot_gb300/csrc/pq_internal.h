@@ -87,16 +87,18 @@ cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream);
 // quantized rows.  cudaErrorNotSupported as for launch_qdot_mma.
 cudaError_t launch_qdot_mma_fused(const FusedArgs& a, cudaStream_t stream);
 
-// The current device's workspace of at least `bytes` (allocated on first use,
-// grown on demand, never freed before exit).
-cudaError_t device_workspace(size_t bytes, void** out);
-
 // A workspace of at least `bytes` for work enqueued on `stream` of the current
-// device (one per device and stream, so calls on different streams never share
-// it; allocated or grown on demand).  Fails without allocating while `stream`
-// is being captured and the workspace is too small, or when the table of
-// streams is full; callers then take a path that needs no workspace.
+// device (one per device, stream and kind, so calls on different streams never
+// share it; allocated stream-ordered on first use, replaced by one at least
+// twice as large when a larger call arrives, never freed before exit).  Fails
+// without allocating while `stream` is being captured and the workspace is too
+// small, or when the table of streams is full; callers then take a path that
+// needs no workspace.
 cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out, int kind = 0);
+
+// Shape checks of the qdot entry points (sizes >= 0, K a positive multiple of
+// 32, element counts representable in int64); returns a pq_status.
+int check_qdot_shape(int64_t M, int64_t N, int64_t K);
 
 // qdot_t (automatic kernel path) without any device allocation; returns a pq_status.
 int qdot_noalloc(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C, int64_t M, int64_t N,

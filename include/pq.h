@@ -21,9 +21,13 @@
  *   Memory.  All tensors are row-major and dense (the innermost index is
  *   contiguous, no padding).  Every pointer is a DEVICE pointer owned by the
  *   caller; the library never frees it or keeps it.  The only device memory
- *   the library allocates is the workspace some entry points keep per device
- *   or per stream (documented with each); it is allocated on first use and
- *   grown on demand, never per call.
+ *   the library allocates is the workspace some entry points keep per
+ *   (device, stream) pair (documented with each).  It is allocated with
+ *   cudaMallocAsync on that stream on first use (ordered with the stream's
+ *   work, no device-wide synchronization) and replaced by one at least twice
+ *   as large when a larger call arrives; a replaced workspace is kept until
+ *   exit, never freed, so work enqueued or captured earlier that refers to it
+ *   stays valid.  No entry point calls cudaFree.
  *   Base alignment: int8 tensors (A, W, q) and f32 inputs read as vectors
  *   (x) start on a 16-byte boundary; the f32 scale planes and C on a 4-byte
  *   boundary.  (The pages ask 16 bytes of every tensor base, "Kernel ABI",
@@ -112,10 +116,9 @@ int pq_quantize_q8_0(const float* x, int8_t* q, float* s,
  *
  * Workspace (tensor-core path, M > 64): the activations are converted once
  * per call, by a small kernel enqueued before the contraction, into a
- * workspace that belongs to the (device, stream) pair.  It is allocated on
- * the first such call on that stream and grown when a larger one arrives
- * (cudaMalloc / cudaFree, which synchronize the device), and kept until
- * exit.  A call made while its stream is being captured, whose workspace does
+ * workspace that belongs to the (device, stream) pair (allocated and grown
+ * as stated at the top of this header).  A call made while its stream is
+ * being captured, whose workspace does
  * not exist yet or is too small, allocates nothing and lets the kernel convert
  * the activations itself (same results); so does
  * pq_quantize_qdot_q8_0_noalloc, and so does every stream past the 64th.
@@ -152,10 +155,9 @@ int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const flo
  * the first.  A [M, K] int8 and AS [M, K/32] f32
  * optionally receive the quantized rows (both null, or both non-null).  When
  * they are null and the two-kernel route is taken, the rows go to a
- * per-device workspace that the library allocates on the first such call and
- * grows when a larger one arrives (that call must not be inside a stream
- * capture); the workspace is shared by all calls on the device, so calls of
- * this kind must not overlap on different streams.  x: 16-byte aligned f32
+ * workspace of this (device, stream) pair, allocated on the first such call
+ * on the stream and grown when a larger one arrives (that call must not be
+ * inside a stream capture; see the top of this header).  x: 16-byte aligned f32
  * [M, K]; A 16-byte aligned; AS, WS, C 4-byte aligned.  C must not overlap
  * any input, and A, AS must not overlap x, W, WS or C.
  */
@@ -172,7 +174,7 @@ int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W,
  * copies to run asynchronously.  The device copies of x and C live in a
  * workspace of this (device, stream) pair, allocated on the first call on the
  * stream and grown when a larger one arrives (that call must not be inside a
- * stream capture), kept until exit.  W, WS and the rules of the contraction
+ * stream capture; see the top of this header).  W, WS and the rules of the contraction
  * as for pq_quantize_qdot_q8_0.
  */
 int pq_quantize_qdot_q8_0_host(const float* x_host, const int8_t* W, const float* WS, float* C_host,

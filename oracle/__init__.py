@@ -39,7 +39,7 @@ QK = 32
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "q8_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
-_libs: dict[int, ctypes.CDLL] = {}
+_libs: dict[tuple[int, bool], ctypes.CDLL] = {}
 _lock = threading.Lock()
 
 _I8P = ctypes.POINTER(ctypes.c_int8)
@@ -49,28 +49,36 @@ _I64P = ctypes.POINTER(ctypes.c_int64)
 _I64 = ctypes.c_int64
 
 
-def lib_path(mutant: int = 0) -> str:
-    return os.path.join(_BUILD, f"liboracle_m{mutant}.so")
+def lib_path(mutant: int = 0, omp: bool = False) -> str:
+    return os.path.join(_BUILD, f"liboracle_m{mutant}{'_omp' if omp else ''}.so")
 
 
-def build(mutant: int = 0, force: bool = False) -> str:
-    """Compile q8_oracle.c into a shared library (mutant 0 = the real oracle)."""
-    out = lib_path(mutant)
+def build(mutant: int = 0, force: bool = False, omp: bool = False) -> str:
+    """Compile q8_oracle.c into a shared library (mutant 0 = the real oracle).
+
+    omp=True builds the same source with -fopenmp: the loops over quantizer
+    rows and output elements run on every host core, each row and element
+    still computed by the single-thread build's sequential loop.
+    """
+    out = lib_path(mutant, omp)
     if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
         return out
     os.makedirs(_BUILD, exist_ok=True)
     tmp = f"{out}.{os.getpid()}.tmp"
     cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
            "-shared", "-fPIC", f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
+    if omp:
+        cmd.insert(1, "-fopenmp")
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
 
 
-def _lib(mutant: int = 0) -> ctypes.CDLL:
+def _lib(mutant: int = 0, omp: bool = False) -> ctypes.CDLL:
+    key = (mutant, omp)
     with _lock:
-        if mutant not in _libs:
-            lib = ctypes.CDLL(build(mutant))
+        if key not in _libs:
+            lib = ctypes.CDLL(build(mutant, omp=omp))
             lib.oracle_quantize_q8_0.argtypes = [_F32P, _I8P, _F32P, _I64, _I64]
             lib.oracle_blocksums_q8_0.argtypes = [_I8P, _I8P, _I64P, _I64, _I64, _I64]
             lib.oracle_qdot_q8_0.argtypes = [_I8P, _F32P, _I8P, _F32P, _F64P, _F64P, _I64, _I64, _I64]
@@ -86,9 +94,15 @@ def _lib(mutant: int = 0) -> ctypes.CDLL:
                        "oracle_qdot_q5_0"):
                 getattr(lib, fn).restype = None
             lib.oracle_mutant.restype = ctypes.c_int
+            lib.oracle_threads.restype = ctypes.c_int
             assert lib.oracle_mutant() == mutant
-            _libs[mutant] = lib
-        return _libs[mutant]
+            _libs[key] = lib
+        return _libs[key]
+
+
+def threads(omp: bool = True) -> int:
+    """Host threads the (omp) build's loops run on."""
+    return int(_lib(0, omp).oracle_threads())
 
 
 def _p(arr: np.ndarray, ctype):
@@ -99,7 +113,7 @@ def _c(arr, dtype) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(arr), dtype=dtype)
 
 
-def quantize_q8_0(x, mutant: int = 0):
+def quantize_q8_0(x, mutant: int = 0, omp: bool = False):
     """x f32 [R, K] -> (q int8 [R, K], s f32 [R, K/32])."""
     x = _c(x, np.float32)
     if x.ndim == 1:
@@ -109,12 +123,12 @@ def quantize_q8_0(x, mutant: int = 0):
         raise ValueError("K must be a multiple of 32")
     q = np.empty((R, K), np.int8)
     s = np.empty((R, K // QK), np.float32)
-    _lib(mutant).oracle_quantize_q8_0(_p(x, ctypes.c_float), _p(q, ctypes.c_int8),
+    _lib(mutant, omp).oracle_quantize_q8_0(_p(x, ctypes.c_float), _p(q, ctypes.c_int8),
                                       _p(s, ctypes.c_float), R, K)
     return q, s
 
 
-def blocksums(a, w, mutant: int = 0) -> np.ndarray:
+def blocksums(a, w, mutant: int = 0, omp: bool = False) -> np.ndarray:
     """a int8 [M, K], w int8 [N, K] -> S int64 [M, N, K/32] (exact block sums)."""
     a = _c(a, np.int8)
     w = _c(w, np.int8)
@@ -123,12 +137,12 @@ def blocksums(a, w, mutant: int = 0) -> np.ndarray:
     if K != K2 or K % QK:
         raise ValueError("shape mismatch")
     S = np.empty((M, N, K // QK), np.int64)
-    _lib(mutant).oracle_blocksums_q8_0(_p(a, ctypes.c_int8), _p(w, ctypes.c_int8),
+    _lib(mutant, omp).oracle_blocksums_q8_0(_p(a, ctypes.c_int8), _p(w, ctypes.c_int8),
                                        _p(S, ctypes.c_int64), M, N, K)
     return S
 
 
-def qdot(a, a_scales, w, w_scales, ws_layout: int = 0, mutant: int = 0):
+def qdot(a, a_scales, w, w_scales, ws_layout: int = 0, mutant: int = 0, omp: bool = False):
     """qdot_t in double: returns (out f64 [M, N], bound f64 [M, N]).
 
     ws_layout 0: w_scales [N, K/32] (qdot_t); 1: w_scales [K/32, N] (qmma_t).
@@ -146,7 +160,7 @@ def qdot(a, a_scales, w, w_scales, ws_layout: int = 0, mutant: int = 0):
         raise ValueError("w_scales shape mismatch")
     out = np.empty((M, N), np.float64)
     bound = np.empty((M, N), np.float64)
-    lib = _lib(mutant)
+    lib = _lib(mutant, omp)
     args = (_p(a, ctypes.c_int8), _p(a_scales, ctypes.c_float), _p(w, ctypes.c_int8),
             _p(w_scales, ctypes.c_float), _p(out, ctypes.c_double), _p(bound, ctypes.c_double),
             M, N, K)
@@ -162,18 +176,18 @@ def qdot(a, a_scales, w, w_scales, ws_layout: int = 0, mutant: int = 0):
 Q50_BYTES = 20  # bytes per 32-element Q5_0 block without its scale
 
 
-def decode_q5_0(w5, K: int, mutant: int = 0) -> np.ndarray:
+def decode_q5_0(w5, K: int, mutant: int = 0, omp: bool = False) -> np.ndarray:
     """Q5_0 blocks uint8 [R, K/32 * 20] -> int8 [R, K] (q - 16)."""
     w5 = _c(w5, np.uint8)
     R = w5.shape[0]
     if K % QK or w5.shape[1] != K // QK * Q50_BYTES:
         raise ValueError("shape mismatch")
     w = np.empty((R, K), np.int8)
-    _lib(mutant).oracle_decode_q5_0(_p(w5, ctypes.c_uint8), _p(w, ctypes.c_int8), R, K)
+    _lib(mutant, omp).oracle_decode_q5_0(_p(w5, ctypes.c_uint8), _p(w, ctypes.c_int8), R, K)
     return w
 
 
-def blocksums_q5_0(a, w5, mutant: int = 0) -> np.ndarray:
+def blocksums_q5_0(a, w5, mutant: int = 0, omp: bool = False) -> np.ndarray:
     """a int8 [M, K], Q5_0 blocks [N, K/32 * 20] -> S int64 [M, N, K/32]."""
     a = _c(a, np.int8)
     w5 = _c(w5, np.uint8)
@@ -182,12 +196,12 @@ def blocksums_q5_0(a, w5, mutant: int = 0) -> np.ndarray:
     if K % QK or w5.shape[1] != K // QK * Q50_BYTES:
         raise ValueError("shape mismatch")
     S = np.empty((M, N, K // QK), np.int64)
-    _lib(mutant).oracle_blocksums_q5_0(_p(a, ctypes.c_int8), _p(w5, ctypes.c_uint8),
+    _lib(mutant, omp).oracle_blocksums_q5_0(_p(a, ctypes.c_int8), _p(w5, ctypes.c_uint8),
                                        _p(S, ctypes.c_int64), M, N, K)
     return S
 
 
-def qdot_q5_0(a, a_scales, w5, w_scales, ws_layout: int = 0, mutant: int = 0):
+def qdot_q5_0(a, a_scales, w5, w_scales, ws_layout: int = 0, mutant: int = 0, omp: bool = False):
     """q50_qdot_t (ws_layout 0) / q50_qmma_t scale layout (1) in double: (out, bound)."""
     a = _c(a, np.int8)
     w5 = _c(w5, np.uint8)
@@ -202,7 +216,7 @@ def qdot_q5_0(a, a_scales, w5, w_scales, ws_layout: int = 0, mutant: int = 0):
         raise ValueError("w_scales shape mismatch")
     out = np.empty((M, N), np.float64)
     bound = np.empty((M, N), np.float64)
-    _lib(mutant).oracle_qdot_q5_0(_p(a, ctypes.c_int8), _p(a_scales, ctypes.c_float),
+    _lib(mutant, omp).oracle_qdot_q5_0(_p(a, ctypes.c_int8), _p(a_scales, ctypes.c_float),
                                   _p(w5, ctypes.c_uint8), _p(w_scales, ctypes.c_float),
                                   _p(out, ctypes.c_double), _p(bound, ctypes.c_double),
                                   M, N, K, int(ws_layout))

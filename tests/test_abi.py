@@ -175,3 +175,20 @@ def test_host_step_entry_checks(lib):
     assert host_step(lib, W=P8) == binding.PQ_ERR_ALIGN
     assert host_step(lib, WS=P2) == binding.PQ_ERR_ALIGN
     assert host_step(lib, layout=9) == binding.PQ_ERR_INVALID_ARG
+
+
+def noalloc(lib, x=P16, W=P16, WS=P16, C=P16, M=1, N=1, K=32, layout=0):
+    return lib.pq_quantize_qdot_q8_0_noalloc(x, W, WS, C, M, N, K, layout, None)
+
+
+def test_noalloc_rejects_the_shapes_the_allocating_step_rejects(lib):
+    """The allocation-free step takes the allocating step's shape rules: an N beyond the
+    size limit, or a product that overflows int64, is PQ_ERR_SHAPE on both, before any
+    scratch-size check."""
+    for kw in ({"N": 1 << 41}, {"M": 1, "N": 1 << 40, "K": 1 << 30}, {"K": 48}, {"N": -1}):
+        assert fused(lib, **kw) == binding.PQ_ERR_SHAPE, kw
+        assert noalloc(lib, **kw) == binding.PQ_ERR_SHAPE, kw
+    assert noalloc(lib, M=0, x=None, W=None, WS=None, C=None) == binding.PQ_OK
+    assert noalloc(lib, M=1 << 20, K=4096) == binding.PQ_ERR_SCRATCH
+    assert noalloc(lib, x=None) == binding.PQ_ERR_INVALID_ARG
+    assert noalloc(lib, layout=2) == binding.PQ_ERR_INVALID_ARG

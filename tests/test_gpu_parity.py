@@ -272,14 +272,17 @@ def test_qdot_workload_full_simt(pq, name):
 TC_SHAPES = [(1, 16, 128), (9, 100, 256), (16, 128, 128), (17, 300, 384), (33, 130, 128), (64, 257, 512),
              (65, 64, 256), (130, 200, 128), (256, 384, 1024), (300, 129, 256),
              # narrow tiles over many scale groups, split along K into units of unequal length
-             (5, 2000, 2048), (24, 700, 3072), (48, 1100, 4096)]
+             (5, 2000, 2048), (24, 700, 3072), (48, 1100, 4096),
+             # many more output tiles than SMs: every persistent CTA takes several tiles
+             # in turn and carries its pipeline phases from one to the next
+             (512, 14336, 128), (384, 2048, 1024)]
 
 
 @pytest.mark.parametrize("M,N,K", TC_SHAPES)
 @pytest.mark.parametrize("layout", [0, 1])
 def test_qdot_tc_small(pq, M, N, K, layout):
     a, a_s, w, w_s = rand_operands(M * 31 + N * 7 + K + layout, M, N, K)
-    out, bound = oracle.qdot(a, a_s, w, w_s)
+    out, bound = oracle.qdot(a, a_s, w, w_s, omp=True)
     ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
     if layout == 1 and N % 4 != 0:
         # the [K/32, N] scale plane is loaded by TMA only when its rows are 16-byte
@@ -350,6 +353,28 @@ def test_qdot_workload_full_tc(pq, name):
     sampled_check(C, qa, sa, qw, sw, rows, np.unique(cols), name)
     # a property at full size: every row of C is finite
     assert torch.isfinite(C).all()
+
+
+def test_qdot_prompt_full_rows_and_columns(pq):
+    """The prompt GEMM (M = 512, K = 4096, N = 14336) at full size, as benchmarked, on
+    complete rows and columns: one row inside every 128-row band (all 14336 columns) and
+    one column inside every 128-column band (all 512 rows).  Together they cross every
+    128 x 128 output tile, so every unit of work a persistent CTA takes -- first, second
+    or third in its turn -- is compared with the oracle, not only a random sample."""
+    name = "prompt_m512_k4096_n14336"
+    x, w, qa, sa, qw, sw = quantized_workload(name)
+    M, N = qa.shape[0], qw.shape[0]
+    A, AS = pq.quantize_q8_0(dev(x))
+    W, WS = pq.quantize_q8_0(dev(w))
+    C = host(pq.qdot_q8_0(A, AS, W, WS))
+    pq.check_device()
+    rng = np.random.default_rng(2)
+    rows = np.array([b + rng.integers(0, min(128, M - b)) for b in range(0, M, 128)])
+    cols = np.array([b + rng.integers(0, min(128, N - b)) for b in range(0, N, 128)])
+    out, bound = oracle.qdot(qa[rows], sa[rows], qw, sw, omp=True)
+    assert_within_bound(C[rows], out, bound, f"{name} rows {rows.tolist()}")
+    out, bound = oracle.qdot(qa, sa, qw[cols], sw[cols], omp=True)
+    assert_within_bound(C[:, cols], out, bound, f"{name} {cols.size} columns")
 
 
 # ------------------------------------------------------------------ fused quantize + qdot

@@ -241,3 +241,30 @@ def test_oracle_on_workload_shapes():
     # dequantized product is close to the f32 product it approximates (Q8_0 error ~ 1%)
     ref = x.astype(np.float64) @ w.astype(np.float64).T
     assert np.abs(out - ref).max() <= 0.05 * np.abs(ref).max()
+
+
+def test_threaded_build_gives_the_same_bytes():
+    """The OpenMP build of the oracle (loops over rows and output elements shared among the
+    host cores, each element computed by the same sequential loop) returns exactly what the
+    single-thread build returns: quantized bytes, scales, block sums and qdot_t values."""
+    rng = np.random.default_rng(17)
+    x = (rng.standard_normal((37, 256)) * np.exp(rng.uniform(-8, 8, (37, 1)))).astype(np.float32)
+    q1, s1 = oracle.quantize_q8_0(x)
+    q2, s2 = oracle.quantize_q8_0(x, omp=True)
+    assert np.array_equal(q1, q2) and np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
+    a, a_s = q1[:5], s1[:5]
+    w, w_s = q1[5:], s1[5:]
+    assert np.array_equal(oracle.blocksums(a, w), oracle.blocksums(a, w, omp=True))
+    for layout in (0, 1):
+        ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+        o1, b1 = oracle.qdot(a, a_s, w, ws, ws_layout=layout)
+        o2, b2 = oracle.qdot(a, a_s, w, ws, ws_layout=layout, omp=True)
+        assert np.array_equal(o1.view(np.uint64), o2.view(np.uint64))
+        assert np.array_equal(b1.view(np.uint64), b2.view(np.uint64))
+    w5 = rng.integers(0, 256, (32, 256 // 32 * 20), dtype=np.uint8)
+    assert np.array_equal(oracle.decode_q5_0(w5, 256), oracle.decode_q5_0(w5, 256, omp=True))
+    assert np.array_equal(oracle.blocksums_q5_0(a, w5), oracle.blocksums_q5_0(a, w5, omp=True))
+    ws5 = np.abs(workloads.random_scales(rng, (32, 8)))
+    o1, _ = oracle.qdot_q5_0(a, a_s, w5, ws5)
+    o2, _ = oracle.qdot_q5_0(a, a_s, w5, ws5, omp=True)
+    assert np.array_equal(o1.view(np.uint64), o2.view(np.uint64))
