@@ -245,7 +245,9 @@ class Problem:
     pq_qdot_q8_0 / pq_q50_qdot; `fused=False` forces the two-call sequence.
     """
 
-    def __init__(self, pq, wl: workloads.Workload, device, fused: bool = True):
+    def __init__(self, pq, wl: workloads.Workload, device, fused: bool = True, split: tuple[int, int] = (0, 1)):
+        import dataclasses
+
         import torch
         self.wl = wl
         self.pq = pq
@@ -253,11 +255,15 @@ class Problem:
         self.fused = fused and wl.M <= (8 if self.q50 else 16)
         x = workloads.activations(wl)
         self.x_host = torch.from_numpy(x).pin_memory()
+        # column split over `world` ranks: this rank holds the weight rows of its shard
+        # of a layer world x N wide (drawn with a rank-dependent seed), x is replicated
+        self.rank, self.world = split
+        wl_w = dataclasses.replace(wl, index=wl.index + 1000 * self.rank) if self.rank else wl
         if self.q50:
-            w5, ws = workloads.q50_weights(wl)
+            w5, ws = workloads.q50_weights(wl_w)
             W, WS = torch.from_numpy(w5).to(device), torch.from_numpy(ws).to(device)
         else:
-            w = torch.from_numpy(workloads.weights(wl)).to(device)
+            w = torch.from_numpy(workloads.weights(wl_w)).to(device)
             W, WS = pq.quantize_q8_0(w)
             del w
         wbytes = W.numel() + WS.numel() * 4
@@ -270,10 +276,20 @@ class Problem:
         self.A = torch.empty((wl.M, wl.K), dtype=torch.int8, device=device)
         self.AS = torch.empty((wl.M, wl.K // 32), dtype=torch.float32, device=device)
         self.C = torch.empty((wl.M, wl.N), dtype=torch.float32, device=device)
-        self.C_host = torch.empty((wl.M, wl.N), dtype=torch.float32).pin_memory()
+        # the gathered output of the column split: rank r's [M, N] block at rows
+        # [r*M, (r+1)*M) (for M = 1 this is the row-major [1, world*N] result itself)
+        self.C_all = torch.empty((self.world * wl.M, wl.N), dtype=torch.float32, device=device) \
+            if self.world > 1 else None
+        self.C_host = torch.empty((self.world * wl.M, wl.N), dtype=torch.float32).pin_memory()
         torch.cuda.synchronize()
 
     def step(self, t: int, events=None):
+        self._step(t, events)
+        if self.C_all is not None:  # the column split's exchange: all-gather of C (NCCL)
+            import torch.distributed as dist
+            dist.all_gather_into_tensor(self.C_all, self.C)
+
+    def _step(self, t: int, events=None):
         c = t % self.copies
         if self.fused:
             if events is not None:
@@ -396,10 +412,10 @@ def time_e2e(prob: Problem, steps: int, warmup: int):
         if t == warmup:
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-        if prob.q50:
+        if prob.q50 or prob.world > 1:
             prob.x.copy_(prob.x_host, non_blocking=True)
-            prob.step(t)
-            prob.C_host.copy_(prob.C, non_blocking=True)
+            prob.step(t)  # with the column split: the local step, then the all-gather of C
+            prob.C_host.copy_(prob.C_all if prob.world > 1 else prob.C, non_blocking=True)
         else:
             c = t % prob.copies
             prob.pq.quantize_qdot_q8_0_host(prob.x_host, prob.W[c], prob.WS[c], prob.C_host)
@@ -445,9 +461,10 @@ def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str, one_kernel
             "algorithmic_flops": wl.ops}
 
 
-def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sampler=None, e2e=False):
+def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sampler=None, e2e=False,
+                 split: tuple[int, int] = (0, 1)):
     wl = workloads.WORKLOADS[name]
-    prob = Problem(pq, wl, device)
+    prob = Problem(pq, wl, device, split=split)
     ms, quant_ms, qdot_ms, qdot_only_ms, window = time_graph(prob, steps, warmup, world, sampler)
     per_rank_s = ms * 1e-3
     if wl.M == 1 or wl.M <= 64:
@@ -469,6 +486,8 @@ def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sample
     # latency, so the in-graph event figure is an upper bound, reported beside it)
     one_kernel = prob.fused and fused_is_one_kernel(prob)
     dom_ms = (ms / steps) if one_kernel else qdot_only_ms
+    if prob.world > 1:  # the step also holds the all-gather: the kernel's own event-bracketed time
+        dom_ms = qdot_ms
     kernel_ms["dominant"] = round(dom_ms, 5)
     res = {"value": round(value / scale, 3), "unit": unit, "ms_per_step": round(t_max * 1e3 / steps, 5),
            "step": (("pq_quantize_q50_qdot" if prob.q50 else "pq_quantize_qdot_q8_0") +
@@ -477,7 +496,7 @@ def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sample
            "kernel_ms": kernel_ms,
            "roofline": roofline_for(prob, dom_ms, peaks, peak_src, one_kernel), "weight_copies": prob.copies,
            "window": window}
-    if prob.fused:
+    if prob.fused and split[1] == 1:
         # the same step as two calls (quantizer, then qdot_t), for comparison
         two = Problem(pq, wl, device, fused=False)
         ms2, _, q2, _, _ = time_graph(two, steps, warmup, world)
@@ -710,6 +729,10 @@ def main(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-others", action="store_true", help="time only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--parallel", choices=["colsplit", "replicas"], default="colsplit",
+                    help="with N > 1 ranks: each rank holds an N-column shard of a layer N x wider "
+                         "and C is all-gathered every step (colsplit), or each rank runs an "
+                         "independent copy of the workload (replicas)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
@@ -724,11 +747,15 @@ def main(argv=None):
     pq.load()
     peaks, peak_src = load_peaks()
     sampler = ClockSampler(local)
+    split = (rank, world) if world > 1 and args.parallel == "colsplit" else (0, 1)
     head = run_workload(pq, args.workload, args.steps, args.warmup, world, device, peaks, peak_src,
-                        sampler=sampler, e2e=True)
+                        sampler=sampler, e2e=True, split=split)
+    head["parallelism"] = (f"colsplit{world}: each rank holds {workloads.WORKLOADS[args.workload].N} weight rows "
+                           f"of a {world}x wider layer, C all-gathered over NCCL every step"
+                           if split[1] > 1 else f"replicas{world}" if world > 1 else "single")
     clocks = sampler.summary(*head.pop("window"))
     others = {}
-    if not args.no_others:
+    if not args.no_others and split[1] == 1:
         for name in (PROMPT, "ffn_up_m1_k4096_n14336", "ffn_down_m1_k14336_n4096",
                      "smallm_m4_k4096_n11008", "smallm_m16_k4096_n11008", "smallm_m64_k4096_n11008",
                      "q50_decode_m1_k4096_n4096", "q50_prompt_m512_k4096_n14336"):
