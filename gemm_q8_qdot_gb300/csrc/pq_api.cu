@@ -88,8 +88,12 @@ constexpr int64_t kMaxDim = int64_t(1) << 40;
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 
+// The CUDA error behind this thread's last PQ_ERR_CUDA / PQ_ERR_UNSUPPORTED.
+thread_local int g_last_cuda_error = 0;
+
 int map_cuda(cudaError_t e) {
     if (e == cudaSuccess) return PQ_OK;
+    g_last_cuda_error = static_cast<int>(e);
     if (e == cudaErrorInvalidConfiguration || e == cudaErrorNotSupported) return PQ_ERR_UNSUPPORTED;
     return PQ_ERR_CUDA;
 }
@@ -308,9 +312,10 @@ int pq_q50_blocksums(const int8_t* A, const uint8_t* W5, int32_t* S, int64_t M, 
 
 int pq_check_device(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return PQ_ERR_CUDA;
-    unsigned status = 0;
+    unsigned status = 0, status_w = 0;
     if (pq::read_and_clear_status(&status) != cudaSuccess) return PQ_ERR_CUDA;
-    return status ? PQ_ERR_TIMEOUT : PQ_OK;
+    if (pq::read_and_clear_status_w(&status_w) != cudaSuccess) return PQ_ERR_CUDA;
+    return (status | status_w) ? PQ_ERR_TIMEOUT : PQ_OK;
 }
 
 const char* pq_strerror(int code) {
@@ -329,9 +334,20 @@ const char* pq_strerror(int code) {
 
 int pq_version(void) { return 105; }
 
+int pq_last_cuda_error(void) { return g_last_cuda_error; }
+
 int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles) {
     if (skip_stage < -1) return PQ_ERR_INVALID_ARG;
     pq::set_tc_test_hooks(skip_stage, timeout_cycles);
+    pq::set_tcw_test_hooks(skip_stage, timeout_cycles);
+    return PQ_OK;
+}
+
+int pq_debug_prompt_kernel_regs(void) { return pq::tcw_kernel_regs(); }
+
+int pq_debug_set_prompt_kernel(int which) {
+    if (which != 0 && which != 1) return PQ_ERR_INVALID_ARG;
+    pq::set_prompt_kernel(which);
     return PQ_OK;
 }
 

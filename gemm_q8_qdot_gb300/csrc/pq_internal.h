@@ -75,8 +75,14 @@ cudaError_t launch_qdot_q50_fused(const FusedArgs& a, cudaStream_t stream);
 // cudaErrorNotSupported otherwise or when the device is not sm_103.
 cudaError_t launch_qdot_tc_q50(const QdotArgs& a, cudaStream_t stream);
 
-// tcgen05 tensor-core kernel.  cudaErrorNotSupported if the device is not sm_103.
+// tcgen05 tensor-core kernels.  cudaErrorNotSupported if the device is not
+// sm_103.  Every shape runs the shared-memory kernel (launch_qdot_tc) unless
+// set_prompt_kernel(1) asks for the kernel that holds the weights in tensor
+// memory (launch_qdot_tcw) for the prompt shapes it takes (M > 64, scaled
+// output, a call that may allocate).
 cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream);
+cudaError_t launch_qdot_tcw(const QdotArgs& a, cudaStream_t stream);
+void set_prompt_kernel(int which);
 
 // Warp-level MMA kernel (mma.sync m16n8k16, f16 operands, exact block sums) for
 // 1 <= M <= 64; cudaErrorNotSupported otherwise.
@@ -104,12 +110,18 @@ int check_qdot_shape(int64_t M, int64_t N, int64_t K);
 int qdot_noalloc(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C, int64_t M, int64_t N,
                  int64_t K, int ws_layout, cudaStream_t stream);
 
-// Reads and clears the device status word (set by a bounded wait that gave up).
+// Reads and clears the device status words of the tensor-core kernels (set by
+// a bounded wait that gave up).
 cudaError_t read_and_clear_status(unsigned* status);
+cudaError_t read_and_clear_status_w(unsigned* status);
 
 // Test hooks of the tensor-core kernel: skip one producer stage so that the
 // consumers' bounded waits give up (-1: off), and the wait limit in SM clock
 // cycles (0: the default of about two seconds).
 void set_tc_test_hooks(int inject_skip_stage, unsigned long long timeout_cycles);
+void set_tcw_test_hooks(int inject_skip_group, unsigned long long timeout_cycles);
+// Registers a thread of the prompt kernel build chosen for the current device
+// (0: the device admits none, the shared-memory kernel runs instead).
+int tcw_kernel_regs();
 
 }  // namespace pq

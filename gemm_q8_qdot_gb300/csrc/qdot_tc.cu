@@ -1095,7 +1095,15 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+int g_prompt_kernel = 0;  // 0: this file's kernel; 1: the tensor-memory kernel where it applies
+
+void set_prompt_kernel(int which) { g_prompt_kernel = which; }
+
 cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream) {
+    if (a.S == nullptr && a.M > 64 && g_prompt_kernel == 1) {
+        const cudaError_t e = launch_qdot_tcw(a, stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
     return a.S != nullptr ? launch_tc<true>(a, stream) : launch_tc<false>(a, stream);
 }
 

@@ -1,0 +1,743 @@
+// qdot_t for prompt-sized M on the sm_103a tensor cores, with the weights held
+// in tensor memory as the MMA's A operand.
+//
+// What it computes ("Quantized built-ins and formats", section "Q8_0"; the
+// integer-tensor-core variant qmma_t in "Phobos Language Spec" section 10):
+//   out[i, j] = sum_b a_scales[i, b] * w_scales[j, b] * S[i, j, b],
+//   S[i, j, b] = sum_{k in block b} a[i, k] * w[j, k]   (an integer).
+//
+// Engine.  As in the other tensor-core kernel: int8 values are exact in f16,
+// and every partial sum of one 32-element block (|S| <= 2^19 < 2^24) is exact
+// in the f32 accumulator, so two K = 16 kind::f16 MMAs into a fresh TMEM
+// buffer give the block sums S exactly.  The scales are applied by the
+// epilogue warps in f32 registers: acc[j, i] += w_scale[j] * (a_scale[i] * S).
+//
+// Orientation.  The MMA's 128-row side (TMEM lanes) is a tile of 128 weight
+// rows j; its N = 128 side is a tile of 128 activation rows i.  The weights are
+// converted int8 -> f16 by four converter warps, which read the TMA-loaded
+// int8 tile from shared memory and write the f16 rows straight into tensor
+// memory (tcgen05.st), where the MMA reads them as its A operand.  The
+// activations were converted once per call into f16 MMA tiles by a small
+// kernel (tile_act_kernel) and arrive by bulk copy.  So the only shared-memory
+// traffic per block is the activation tile (written once, read once by the
+// MMA), the int8 weight tile (written once, read once) and the scales: the
+// 128 x 128 x 16 f16 MMA alone would take the whole shared-memory bandwidth
+// if both operands came from there.
+//
+// Tensor memory (512 columns): three 128-column accumulator buffers (one Q8_0
+// block each) and a ring of eight weight slots of 16 columns (one block of
+// 32 K f16 each).
+//
+// Warps (448 threads, one persistent CTA per SM over (activation tile, weight
+// tile, K split) units, the activation tile fastest, so the CTAs running at
+// the same time share weight tiles in L2):
+//   warp 0      producer: per scale group (128 K) the int8 weight tile and
+//               the weight-scale box (TMA), the group's activation scales,
+//               and two 64-K f16 activation stages (bulk copies);
+//   warp 1      MMA issuer (one thread), TMEM allocation;
+//   warps 2..5  converters, one per TMEM lane quadrant (warp % 4; 32 weight
+//               rows each);
+//   warps 6..13 epilogue: four lane quadrants x two column halves, each
+//               thread holding 4 weight rows x 16 activation rows of the
+//               accumulator tile in registers; the unit's end stores C.
+//
+// Safety.  Every mbarrier wait is bounded (a clock64 limit).  A wait that
+// gives up sets this file's device status word and a CTA-wide abort flag;
+// every role then runs out its loops without waiting or working, copies and
+// MMAs in flight are drained with bounded waits, TMEM is freed and the kernel
+// returns.  The host reads the status through read_and_clear_status.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "pq.h"
+#include "pq_device.cuh"
+#include "pq_internal.h"
+#include "tc_ptx.cuh"
+
+namespace pq {
+
+// Nonzero after a bounded on-device wait of this kernel gave up.
+__device__ unsigned g_pq_status_w;
+
+namespace {
+
+constexpr int TW = 128;                  // weight rows per tile (MMA M, TMEM lanes)
+constexpr int TA = 128;                  // activation rows per tile (MMA N)
+constexpr int GROUP = 4;                 // Q8_0 blocks per scale group (128 K)
+constexpr int kNbufD = 3;                // accumulator buffers, one block each
+constexpr int kWcol0 = kNbufD * TA;      // first TMEM column of the weight ring (384)
+constexpr int kWslots = 8;               // weight ring slots (one block = 16 columns)
+constexpr int kAct = TA * 64 * 2;        // one f16 activation stage: 128 rows x 64 K (16 KB)
+constexpr int kAsc = GROUP * TA * 4;     // activation scales of one group (2 KB)
+constexpr int kW8 = TW * 128;            // int8 weight tile of one group (16 KB)
+constexpr int kWsc = TW * GROUP * 4;     // weight scales of one group (2 KB)
+constexpr int S16 = 6;                   // f16 activation stages
+constexpr int S8 = 4;                    // int8 weight stages (groups)
+constexpr int SR = 6;                    // scale slots (groups)
+constexpr int kOffAct = 0;
+constexpr int kOffW8 = kOffAct + S16 * kAct;
+constexpr int kOffSc = kOffW8 + S8 * kW8;          // slot: weight scales, then activation scales
+constexpr int kSc = kWsc + kAsc;
+constexpr int kOffBar = kOffSc + SR * kSc;
+constexpr int kNumBars = 2 * S16 + 2 * S8 + 2 * SR + 2 * kWslots + 2 * kNbufD + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmem = kOffMisc + 16 + 1024;        // + alignment slack
+constexpr int kThreads = 448;            // 14 warps of 144 registers
+constexpr int kConv0 = 2;                // first converter warp
+constexpr int kEpi0 = 6;                 // first epilogue warp
+constexpr unsigned kBackoff = 64;        // ns between failed barrier tests of the waiting roles
+static_assert(kSmem <= 227 * 1024, "shared memory");
+static_assert(kAct % 1024 == 0 && kW8 % 1024 == 0 && kSc % 1024 == 0, "1024-byte aligned tiles");
+
+struct TcwParams {
+    float* C;                  // C[i * N + j], [M, N] row-major
+    int64_t M, N, K;
+    int ngroups;               // K / 128
+    int groups_per_split;
+    int splits;                // K splits per tile
+    int tiles_a;               // activation tiles
+    int units;                 // tiles_a * tiles_w * splits
+    int atomic;                // split-K: red.add into a zeroed C
+    int ws_rowmajor;           // 1: WS [N, K/32] (smem [row][4]); 0: WS [K/32, N] (smem [4][row])
+    const uint8_t* act;        // f16 activation stages: [tiles_a][K / 64] x kAct bytes
+    const uint8_t* asc;        // activation scales: [tiles_a][ngroups] x kAsc bytes
+    int inject_skip_stage;     // test hook: the producer skips this group (-1: off)
+    unsigned long long timeout_cycles;
+};
+
+__device__ __forceinline__ void set_abort(volatile int* abort_flag) {
+    if (*abort_flag == 0) {
+        *abort_flag = 1;
+        atomicOr(&g_pq_status_w, 1u);
+    }
+}
+
+// Waits for the phase of `bar` with the given parity; false if the CTA is
+// aborting or the wait ran past its limit (which starts the abort).  After a
+// failed test the thread sleeps about `backoff_ns` before the next, so that a
+// role that is waiting leaves the issue slots of its SM sub-partition to the
+// epilogue warps, which bound the kernel (0: test again at once).
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             unsigned long long limit, unsigned backoff_ns = 0) {
+    if (*abort_flag) return false;
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t n = 1;; ++n) {
+        if (backoff_ns) __nanosleep(backoff_ns);
+        if (tc::mbar_try_wait(bar, parity)) return true;
+        if ((n & 31) == 0) {
+            if (*abort_flag) return false;
+            if (static_cast<unsigned long long>(clock64() - t0) > limit) {
+                set_abort(abort_flag);
+                return false;
+            }
+        }
+    }
+}
+
+// Drain wait for work already in flight: ignores the abort flag, still bounded.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsigned long long limit) {
+    const long long t0 = clock64();
+    while (!tc::mbar_try_wait(bar, parity)) {
+        if (static_cast<unsigned long long>(clock64() - t0) > limit) {
+            atomicOr(&g_pq_status_w, 2u);
+            return;
+        }
+    }
+}
+
+// Warp-uniform bounded wait: lane 0 waits, the result is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long limit, int lane, unsigned backoff_ns = 0) {
+    int ok = 0;
+    if (lane == 0) ok = bounded_wait(bar, parity, abort_flag, limit, backoff_ns);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// NREG registers a thread (the launcher takes the largest build the device
+// admits with 448 threads)
+template <int NREG>
+__global__ void __maxnreg__(NREG)
+qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWS,
+                const TcwParams prm) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    uint64_t* full16 = bars;                  // f16 activation stage landed (producer, tx)
+    uint64_t* empty16 = full16 + S16;         // its MMAs completed (commit)
+    uint64_t* full8 = empty16 + S16;          // int8 weight tile landed (producer, tx)
+    uint64_t* empty8 = full8 + S8;            // converted (4 converter warps)
+    uint64_t* sfull = empty8 + S8;            // scales of a group landed (producer, tx)
+    uint64_t* sempty = sfull + SR;            // read (8 epilogue warps)
+    uint64_t* wfull = sempty + SR;            // weight slot written to TMEM (4 converter warps)
+    uint64_t* wempty = wfull + kWslots;       // its MMAs completed (commit)
+    uint64_t* tfull = wempty + kWslots;       // block sums in an accumulator buffer (commit)
+    uint64_t* tempty = tfull + kNbufD;        // read (8 epilogue warps)
+    uint64_t* drain = tempty + kNbufD;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    const uint32_t sbase = tc::smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const unsigned long long limit = prm.timeout_cycles;
+
+    // work unit u -> (activation tile, weight tile, K split) and its scale groups
+    struct Unit {
+        int a_tile;
+        int64_t i0, j0;   // first activation row, first weight row
+        int g_begin, ng;
+    };
+    auto unit = [&](int u) {
+        Unit r;
+        const int z = u % prm.splits;
+        const int t = u / prm.splits;
+        r.a_tile = t % prm.tiles_a;
+        r.i0 = static_cast<int64_t>(r.a_tile) * TA;
+        r.j0 = static_cast<int64_t>(t / prm.tiles_a) * TW;
+        r.g_begin = z * prm.groups_per_split;
+        r.ng = max(0, min(prm.ngroups, r.g_begin + prm.groups_per_split) - r.g_begin);
+        return r;
+    };
+    const int u_first = static_cast<int>(blockIdx.x);
+    const int u_step = static_cast<int>(gridDim.x);
+
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S16; ++i) {
+            tc::mbar_init(&full16[i], 1);
+            tc::mbar_init(&empty16[i], 1);
+        }
+        for (int i = 0; i < S8; ++i) {
+            tc::mbar_init(&full8[i], 1);
+            tc::mbar_init(&empty8[i], 4);
+        }
+        for (int i = 0; i < SR; ++i) {
+            tc::mbar_init(&sfull[i], 1);
+            tc::mbar_init(&sempty[i], 8);
+        }
+        for (int i = 0; i < kWslots; ++i) {
+            tc::mbar_init(&wfull[i], 4);
+            tc::mbar_init(&wempty[i], 1);  // the first kWslots / 2 are used: one per slot pair
+        }
+        for (int i = 0; i < kNbufD; ++i) {
+            tc::mbar_init(&tfull[i], 1);
+            tc::mbar_init(&tempty[i], 8);
+        }
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        tc::tma_prefetch_map(&tmW);
+        tc::tma_prefetch_map(&tmWS);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+        tc::tc_fence_before_sync();
+    }
+    __syncthreads();
+    tc::tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    // everything below reads global memory the preceding kernel may have written
+    pdl_wait();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int gi = 0;  // scale groups over all units of this CTA
+            int issued8 = 0, issuedS = 0, issued16 = 0;
+            for (int u = u_first; u < prm.units; u += u_step) {
+                const Unit un = unit(u);
+                for (int k = 0; k < un.ng; ++k, ++gi) {
+                    const int g = un.g_begin + k;
+                    if (gi == prm.inject_skip_stage) continue;  // test hook: this group never arrives
+                    // int8 weight tile of the group: 128 rows x 128 K, 128-byte swizzle
+                    const int s8 = gi % S8;
+                    if (bounded_wait(&empty8[s8], ((gi / S8) & 1) ^ 1, abort_flag, limit, kBackoff)) {
+                        issued8 = gi + 1;
+                        tc::mbar_arrive_expect_tx(&full8[s8], kW8);
+                        tc::tma_load_2d(smem + kOffW8 + s8 * kW8, &tmW, &full8[s8], g * 128,
+                                        static_cast<int>(un.j0));
+                    }
+                    // weight scales (TMA box) and activation scales (bulk copy) of the group
+                    const int sr = gi % SR;
+                    if (bounded_wait(&sempty[sr], ((gi / SR) & 1) ^ 1, abort_flag, limit, kBackoff)) {
+                        issuedS = gi + 1;
+                        tc::mbar_arrive_expect_tx(&sfull[sr], kSc);
+                        const int b0 = g * GROUP;
+                        tc::tma_load_2d(smem + kOffSc + sr * kSc, &tmWS, &sfull[sr],
+                                        prm.ws_rowmajor ? b0 : static_cast<int>(un.j0),
+                                        prm.ws_rowmajor ? static_cast<int>(un.j0) : b0);
+                        tc::bulk_copy_g2s(smem + kOffSc + sr * kSc + kWsc,
+                                          prm.asc + (static_cast<int64_t>(un.a_tile) * prm.ngroups + g) * kAsc, kAsc,
+                                          &sfull[sr]);
+                    }
+                    // the group's two f16 activation stages
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        const int si = 2 * gi + h;
+                        const int s16 = si % S16;
+                        if (!bounded_wait(&empty16[s16], ((si / S16) & 1) ^ 1, abort_flag, limit, kBackoff)) continue;
+                        issued16 = si + 1;
+                        tc::mbar_arrive_expect_tx(&full16[s16], kAct);
+                        tc::bulk_copy_g2s(smem + kOffAct + s16 * kAct,
+                                          prm.act + (static_cast<int64_t>(un.a_tile) * (2 * prm.ngroups) + 2 * g + h) *
+                                                        kAct,
+                                          kAct, &full16[s16]);
+                    }
+                }
+            }
+            // copies in flight land before the CTA may exit (the skipped test group excepted)
+            for (int i = max(0, issued8 - S8); i < issued8; ++i)
+                if (i != prm.inject_skip_stage) drain_wait(&full8[i % S8], (i / S8) & 1, limit);
+            for (int i = max(0, issuedS - SR); i < issuedS; ++i)
+                if (i != prm.inject_skip_stage) drain_wait(&sfull[i % SR], (i / SR) & 1, limit);
+            for (int i = max(0, issued16 - S16); i < issued16; ++i)
+                if (i / 2 != prm.inject_skip_stage) drain_wait(&full16[i % S16], (i / S16) & 1, limit);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_f16_f32(TW, TA);
+            int gb = 0;  // blocks over all units of this CTA
+            for (int u = u_first; u < prm.units; u += u_step) {
+                const int nblk = unit(u).ng * GROUP;
+                for (int k = 0; k < nblk; ++k, ++gb) {
+                    const int sw = gb % kWslots;
+                    const int si = gb >> 1;
+                    const int s16 = si % S16;
+                    const int buf = gb % kNbufD;
+                    bool ok = bounded_wait(&wfull[sw], (gb / kWslots) & 1, abort_flag, limit, kBackoff);
+                    if ((gb & 1) == 0)
+                        ok = ok && bounded_wait(&full16[s16], (si / S16) & 1, abort_flag, limit, kBackoff);
+                    ok = ok && bounded_wait(&tempty[buf], ((gb / kNbufD) & 1) ^ 1, abort_flag, limit, kBackoff);
+                    if (ok) {
+                        tc::tc_fence_after_sync();
+                        const uint32_t b0 = sbase + kOffAct + s16 * kAct;
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint32_t koff = static_cast<uint32_t>(((gb & 1) * 2 + kk) * 32);  // 16 f16 = 32 B
+                            tc::umma_f16_tmem_a(tmem_base + static_cast<uint32_t>(buf * TA),
+                                                tmem_base + static_cast<uint32_t>(kWcol0 + sw * 16 + kk * 8),
+                                                tc::sw128_kmajor_desc(b0 + koff), idesc, kk);
+                        }
+                    }
+                    // the commits arrive also after an abort, so that every barrier
+                    // keeps a consistent phase for the drains
+                    tc::umma_commit(&tfull[buf]);
+                    if (gb & 1) {  // both blocks of the f16 stage and of the weight-slot pair done
+                        tc::umma_commit(&wempty[sw >> 1]);
+                        tc::umma_commit(&empty16[s16]);
+                    }
+                }
+            }
+            tc::umma_commit(drain);  // arrives when every MMA issued above has completed
+            drain_wait(drain, 0, limit);
+        }
+    } else if (warp >= kConv0 && warp < kEpi0) {
+        // ------------------------------------------------------------ converters
+        // warp w converts weight rows 32 (w % 4) .. + 31 of the tile, one row per
+        // lane, into the TMEM lanes of the same numbers
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+        int gi = 0, gb = 0;
+        for (int u = u_first; u < prm.units; u += u_step) {
+            const int ng = unit(u).ng;
+            for (int k = 0; k < ng; ++k, ++gi) {
+                const int s8 = gi % S8;
+                const bool ok8 = warp_wait(&full8[s8], (gi / S8) & 1, abort_flag, limit, lane, kBackoff);
+                const uint32_t w8 = sbase + kOffW8 + s8 * kW8 + row * 128;
+#pragma unroll 1
+                for (int bb = 0; bb < GROUP; ++bb, ++gb) {
+                    const int sw = gb % kWslots;
+                    // slots are released in pairs (the MMA's blocks 2p and 2p + 1)
+                    const bool ok = ok8 && ((gb & 1) || warp_wait(&wempty[sw >> 1], ((gb / kWslots) & 1) ^ 1, abort_flag,
+                                                                  limit, lane, kBackoff));
+                    if (ok) {
+                        // block bb = 16-byte chunks 2bb, 2bb + 1 of the row (128-byte swizzle)
+                        const uint4 v0 = tc::lds128(w8 + (((2 * bb) ^ (row & 7)) << 4));
+                        const uint4 v1 = tc::lds128(w8 + (((2 * bb + 1) ^ (row & 7)) << 4));
+                        uint32_t f[16];
+                        i8x4_to_f16x4(v0.x, f[0], f[1]);
+                        i8x4_to_f16x4(v0.y, f[2], f[3]);
+                        i8x4_to_f16x4(v0.z, f[4], f[5]);
+                        i8x4_to_f16x4(v0.w, f[6], f[7]);
+                        i8x4_to_f16x4(v1.x, f[8], f[9]);
+                        i8x4_to_f16x4(v1.y, f[10], f[11]);
+                        i8x4_to_f16x4(v1.z, f[12], f[13]);
+                        i8x4_to_f16x4(v1.w, f[14], f[15]);
+                        tc::tmem_st_32x32b_x16(t_lane + static_cast<uint32_t>(kWcol0 + sw * 16), f);
+                        tc::tmem_wait_st();
+                    }
+                    tc::tc_fence_before_sync();
+                    __syncwarp();
+                    // arrive also after an abort: every barrier keeps a consistent phase
+                    if (lane == 0) tc::mbar_arrive(&wfull[sw]);
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&empty8[s8]);
+            }
+        }
+    } else if (warp >= kEpi0) {
+        // ------------------------------------------------------------ epilogue
+        // thread (quadrant qd, column half ch, lane t): weight rows
+        // 32 qd + t/4 + {0, 8, 16, 24} and activation rows 64 ch + 8 r + 2 (t % 4) + {0, 1},
+        // r = 0..7, of the tile -- the 16x256b TMEM load layout over two 16-lane halves
+        const int qd = warp & 3;
+        const int ch = (warp - kEpi0) >> 2;
+        const int m = lane & 3;
+        const int rr = lane >> 2;
+        const uint32_t t_q = tmem_base + (static_cast<uint32_t>(qd * 32) << 16);
+        uint64_t acc[4][8];  // [row k][r]: f32 pair of activation rows (2m, 2m + 1) + 8r + 64ch
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[k][r] = 0ull;
+        int gi = 0, gb = 0;
+        for (int u = u_first; u < prm.units; u += u_step) {
+            const Unit un = unit(u);
+            for (int kg = 0; kg < un.ng; ++kg, ++gi) {
+                const int sr = gi % SR;
+                const bool oks = warp_wait(&sfull[sr], (gi / SR) & 1, abort_flag, limit, lane);
+                const uint32_t wsc = sbase + kOffSc + sr * kSc;
+                const uint32_t asc = wsc + kWsc;
+#pragma unroll 1
+                for (int bb = 0; bb < GROUP; ++bb, ++gb) {
+                    const int buf = gb % kNbufD;
+                    const bool ok = oks && warp_wait(&tfull[buf], (gb / kNbufD) & 1, abort_flag, limit, lane, 32);
+                    if (ok) {
+                        tc::tc_fence_after_sync();
+                        // weight scales of the thread's four rows for block bb, as f32 pairs
+                        uint64_t w2[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int row = qd * 32 + rr + 8 * k;
+                            const float w = tc::lds32f(wsc + (prm.ws_rowmajor ? row * GROUP + bb : bb * TW + row) * 4);
+                            w2[k] = f2_pack(__float_as_uint(w), __float_as_uint(w));
+                        }
+                        // activation scales of the thread's rows of 16-column chunk c:
+                        // [bb][ch][c][m][4] order, one 16-byte load per chunk, the four
+                        // threads m of a chunk reading 64 contiguous bytes
+                        const uint32_t as0 = asc + ((bb * 2 + ch) * 64 + m * 4) * 4;
+                        // The block's 64 columns in four chunks of 16 (two 16-lane halves,
+                        // 16 registers), double-buffered: the next chunk's TMEM load is in
+                        // flight while the current one is scaled into the accumulators, and the
+                        // buffer is handed back to the MMA as soon as its last load has landed.
+                        const uint32_t col0 = t_q + static_cast<uint32_t>(buf * TA + ch * 64);
+                        uint32_t sa0[8], sa1[8], sb0[8], sb1[8];
+                        auto load = [&](int c, uint32_t(&h0)[8], uint32_t(&h1)[8]) {
+                            tc::TmemLd16x256bX2::load(col0 + c * 16, h0);
+                            tc::TmemLd16x256bX2::load(col0 + (16u << 16) + c * 16, h1);
+                        };
+                        auto scale = [&](int c, const uint32_t(&h0)[8], const uint32_t(&h1)[8]) {
+                            const float4 av = tc::lds128f(as0 + c * 64);
+#pragma unroll
+                            for (int rl = 0; rl < 2; ++rl) {
+                                const int r = 2 * c + rl;
+                                const uint64_t a2 = rl ? f2_pack(__float_as_uint(av.z), __float_as_uint(av.w))
+                                                       : f2_pack(__float_as_uint(av.x), __float_as_uint(av.y));
+                                acc[0][r] = f2_fma(w2[0], f2_mul(a2, f2_pack(h0[4 * rl], h0[4 * rl + 1])), acc[0][r]);
+                                acc[1][r] = f2_fma(w2[1], f2_mul(a2, f2_pack(h0[4 * rl + 2], h0[4 * rl + 3])), acc[1][r]);
+                                acc[2][r] = f2_fma(w2[2], f2_mul(a2, f2_pack(h1[4 * rl], h1[4 * rl + 1])), acc[2][r]);
+                                acc[3][r] = f2_fma(w2[3], f2_mul(a2, f2_pack(h1[4 * rl + 2], h1[4 * rl + 3])), acc[3][r]);
+                            }
+                        };
+                        load(0, sa0, sa1);
+                        tc::tmem_wait_ld2x8(sa0, sa1);
+                        load(1, sb0, sb1);
+                        scale(0, sa0, sa1);
+                        tc::tmem_wait_ld2x8(sb0, sb1);
+                        load(2, sa0, sa1);
+                        scale(1, sb0, sb1);
+                        tc::tmem_wait_ld2x8(sa0, sa1);
+                        load(3, sb0, sb1);
+                        scale(2, sa0, sa1);
+                        tc::tmem_wait_ld2x8(sb0, sb1);
+                        // every load of this buffer has landed: hand it back before the last chunk
+                        tc::tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&tempty[buf]);
+                        scale(3, sb0, sb1);
+                    } else {
+                        tc::tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&tempty[buf]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&sempty[sr]);
+            }
+            // the unit's tile (or K split of it) goes to C
+            if (*abort_flag == 0) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int64_t j = un.j0 + qd * 32 + rr + 8 * k;
+                    if (j < prm.N) {
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+#pragma unroll
+                            for (int c = 0; c < 2; ++c) {
+                                const int64_t i = un.i0 + ch * 64 + 8 * r + 2 * m + c;
+                                const float v = __uint_as_float(c ? static_cast<uint32_t>(acc[k][r] >> 32)
+                                                                  : static_cast<uint32_t>(acc[k][r]));
+                                if (i < prm.M) {
+                                    float* dst = prm.C + i * prm.N + j;
+                                    if (prm.atomic)
+                                        atomicAdd(dst, v);
+                                    else
+                                        *dst = v;
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int r = 0; r < 8; ++r) acc[k][r] = 0ull;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after_sync();
+        tc::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// Converts the activations A [M, K] (with AS [M, K/32]) once per call into the
+// layouts the kernel above copies into shared memory.  One CTA per (128-row
+// activation tile, scale group of 128 K):
+//   * two f16 stages of 64 K: row r of the tile at r * 128 bytes, its 16-byte
+//     chunk c (K elements 8c .. 8c + 7) at ((c ^ (r & 7)) << 4) -- the UMMA
+//     K-major 128-byte-swizzle layout of the MMA's B operand;
+//   * the group's activation scales ordered [block b][column half h][chunk q]
+//     [m][e] for activation row 64 h + 8 (2 q + e / 2) + 2 m + e % 2: an epilogue
+//     thread (m = lane % 4) reads the four rows of its chunk q with one 16-byte
+//     load, the four threads m together 64 contiguous bytes.
+// Rows past M are zero (their results are never stored).
+__global__ void __launch_bounds__(256)
+tile_act_kernel(const int8_t* __restrict__ A, const float* __restrict__ AS, uint8_t* __restrict__ act,
+                float* __restrict__ asc, int64_t M, int64_t K) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t ngroups = K / 128;
+    const int64_t KB = K / 32;
+    const int64_t tile = blockIdx.x / ngroups, g = blockIdx.x % ngroups;
+    uint8_t* out = act + static_cast<int64_t>(blockIdx.x) * 2 * kAct;
+    for (int i = threadIdx.x; i < 2 * TA * 8; i += blockDim.x) {
+        const int h = i / (TA * 8);
+        const int r = (i >> 3) % TA, c = i & 7;
+        const int64_t row = tile * TA + r;
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (row < M) {
+            const uint2 b = *reinterpret_cast<const uint2*>(A + row * K + g * 128 + h * 64 + c * 8);
+            i8x4_to_f16x4(b.x, o.x, o.y);
+            i8x4_to_f16x4(b.y, o.z, o.w);
+        }
+        *reinterpret_cast<uint4*>(out + h * kAct + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+    }
+    float* s = asc + static_cast<int64_t>(blockIdx.x) * (kAsc / 4);
+    for (int i = threadIdx.x; i < GROUP * TA; i += blockDim.x) {
+        // i = (((b * 2 + h) * 4 + q) * 4 + m) * 4 + e: chunk q of 16 columns, element e = 2 rl + c
+        // of thread m, i.e. activation row 64 h + 8 (2 q + rl) + 2 m + c
+        const int b = i / TA, rem = i % TA;
+        const int h = rem / 64, q = (rem / 16) % 4, m = (rem / 4) % 4, e = rem % 4;
+        const int r = 2 * q + e / 2, c = e % 2;
+        const int64_t row = tile * TA + 64 * h + 8 * r + 2 * m + c;
+        s[i] = row < M ? AS[row * KB + g * GROUP + b] : 0.0f;
+    }
+}
+
+// Zeroes C before a split-K contraction adds its partial tiles (a kernel, so
+// that it takes part in the programmatic dependent launches).
+__global__ void __launch_bounds__(256) zero_c_kernel(float* __restrict__ p, int64_t n) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = 0.0f;
+}
+
+// ---------------------------------------------------------------------- host
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+using TcwKernel = void (*)(CUtensorMap, CUtensorMap, TcwParams);
+
+// The build of qdot_tcw_kernel with the most registers a thread whose 448
+// threads the device admits in one block (the per-block register file is the
+// limit; the device, not the arithmetic, decides which one fits), with its
+// shared-memory size set; null if none.  Chosen once per device.
+TcwKernel pick_kernel(int dev) {
+    static std::mutex mu;
+    static TcwKernel chosen[64] = {};
+    static bool have[64] = {};
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!have[dev]) {
+        have[dev] = true;
+        const TcwKernel cands[3] = {qdot_tcw_kernel<144>, qdot_tcw_kernel<136>, qdot_tcw_kernel<128>};
+        for (TcwKernel k : cands) {
+            cudaFuncAttributes fa{};
+            if (cudaFuncGetAttributes(&fa, k) != cudaSuccess || fa.maxThreadsPerBlock < kThreads) continue;
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) continue;
+            chosen[dev] = k;
+            break;
+        }
+        cudaGetLastError();  // a declined candidate leaves no sticky error behind
+    }
+    return chosen[dev];
+}
+
+int g_skip = -1;
+unsigned long long g_timeout = 4000000000ull;  // ~2 s at 2 GHz
+
+}  // namespace
+
+// Prompt shapes (M > 64) of qdot_t, block-scaled output only.
+// cudaErrorNotSupported when the shape or the operands do not suit this kernel
+// (K % 128 != 0, scale planes that TMA cannot load, not sm_103) or when the
+// call may not allocate its activation workspace; the caller then takes the
+// other tensor-core kernel.
+cudaError_t launch_qdot_tcw(const QdotArgs& a, cudaStream_t stream) {
+    if (a.S != nullptr || a.no_alloc || a.M <= 64 || a.K % 128 != 0) return cudaErrorNotSupported;
+    if (a.K > 0x7fffffffLL || a.M > 0x7fffffffLL || a.N > 0x7fffffffLL) return cudaErrorNotSupported;
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNotSupported;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3 || sms <= 0) return cudaErrorNotSupported;
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    if ((reinterpret_cast<uintptr_t>(a.W) & 15u) != 0 || (reinterpret_cast<uintptr_t>(a.WS) & 15u) != 0)
+        return cudaErrorNotSupported;
+    const int64_t KB = a.K / 32;
+    const bool rowmajor = a.ws_layout == PQ_WS_N_KB;
+    if (!rowmajor && (a.N * 4) % 16 != 0) return cudaErrorNotSupported;
+
+    TcwParams prm{};
+    prm.C = a.C;
+    prm.M = a.M;
+    prm.N = a.N;
+    prm.K = a.K;
+    prm.ngroups = static_cast<int>(a.K / 128);
+    prm.ws_rowmajor = rowmajor ? 1 : 0;
+    prm.inject_skip_stage = g_skip;
+    prm.timeout_cycles = g_timeout;
+    const int64_t ta = (a.M + TA - 1) / TA;
+    const int64_t tw = (a.N + TW - 1) / TW;
+    const int64_t tiles = ta * tw;
+    // K is split when the tiles are too few for the SMs: the smallest split
+    // count whose units spread evenly (the busiest SM within ~5% of the mean),
+    // each split keeping at least two scale groups
+    int splits = 1;
+    if (tiles < 4 * sms) {
+        for (int s = 1; s <= std::max(1, prm.ngroups / 2); ++s) {
+            const int64_t units = tiles * s;
+            const double per_sm = static_cast<double>(units) / sms;
+            const int64_t busiest = (units + sms - 1) / sms;
+            splits = s;
+            if (units >= sms && busiest <= per_sm * 1.05 + 1e-9) break;
+        }
+    }
+    prm.groups_per_split = (prm.ngroups + splits - 1) / splits;
+    splits = (prm.ngroups + prm.groups_per_split - 1) / prm.groups_per_split;
+    if (tiles * splits > 0x7fffffffLL || ta * prm.ngroups > 0x7fffffffLL) return cudaErrorNotSupported;
+    prm.splits = splits;
+    prm.tiles_a = static_cast<int>(ta);
+    prm.units = static_cast<int>(tiles * splits);
+    prm.atomic = splits > 1 ? 1 : 0;
+
+    CUtensorMap maps[2];
+    {
+        // int8 W [N, K]: box {128 bytes of K, 128 rows}, 128-byte swizzle, zero fill past N
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K)};
+        const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(TW)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (fn(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(a.W), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorNotSupported;
+    }
+    {
+        // WS: [N, KB] box {4 blocks, 128 rows}, or [KB, N] box {128 rows, 4 blocks}; zero fill past N
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rowmajor ? KB : a.N),
+                                    static_cast<cuuint64_t>(rowmajor ? a.N : KB)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>((rowmajor ? KB : a.N) * 4)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(rowmajor ? GROUP : TW),
+                                   static_cast<cuuint32_t>(rowmajor ? TW : GROUP)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (fn(&maps[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(a.WS), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorNotSupported;
+    }
+    // the activation workspace of this stream: f16 stages, then the scales
+    const size_t act_bytes = static_cast<size_t>(ta * prm.ngroups) * 2 * kAct;
+    const size_t asc_bytes = static_cast<size_t>(ta * prm.ngroups) * kAsc;
+    void* ws = nullptr;
+    if (stream_workspace(stream, act_bytes + asc_bytes, &ws) != cudaSuccess) return cudaErrorNotSupported;
+    prm.act = static_cast<const uint8_t*>(ws);
+    prm.asc = static_cast<const uint8_t*>(ws) + act_bytes;
+    cudaError_t e = launch_pdl(tile_act_kernel, dim3(static_cast<unsigned>(ta * prm.ngroups)), dim3(256), 0, stream,
+                               a.A, a.AS, static_cast<uint8_t*>(ws),
+                               reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + act_bytes), a.M, a.K);
+    if (e != cudaSuccess) return e;
+    if (prm.atomic) {
+        const int64_t n = a.M * a.N;
+        const int64_t blocks = std::min<int64_t>((n + 1023) / 1024, 2 * static_cast<int64_t>(sms));
+        e = launch_pdl(zero_c_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, a.C, n);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t grid = std::min<int64_t>(prm.units, sms);
+    auto kern = pick_kernel(dev);
+    if (!kern) return cudaErrorNotSupported;
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), static_cast<size_t>(kSmem), stream,
+                      maps[0], maps[1], prm);
+}
+
+cudaError_t read_and_clear_status_w(unsigned* status) {
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_pq_status_w, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_pq_status_w, &zero, sizeof(unsigned));
+}
+
+int tcw_kernel_regs() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const TcwKernel k = pick_kernel(dev);
+    if (!k) return 0;
+    cudaFuncAttributes fa{};
+    return cudaFuncGetAttributes(&fa, k) == cudaSuccess ? fa.numRegs : 0;
+}
+
+void set_tcw_test_hooks(int inject_skip_group, unsigned long long timeout_cycles) {
+    g_skip = inject_skip_group;
+    g_timeout = timeout_cycles ? timeout_cycles : 4000000000ull;
+}
+
+}  // namespace pq

@@ -288,6 +288,14 @@ const char* pq_strerror(int code);
    for 9..16 rows in pq_quantize_qdot_q8_0). */
 int pq_version(void);
 
+/*
+ * The CUDA runtime error (a cudaError_t value) behind the last PQ_ERR_CUDA or
+ * PQ_ERR_UNSUPPORTED that an entry point returned on the calling thread, or 0
+ * if there was none.  For diagnostics only; it is not reset by later calls
+ * that succeed.
+ */
+int pq_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,14 +14,35 @@ extern "C" {
 
 /*
  * Makes the next tensor-core qdot launches (PQ_PATH_TC) skip pipeline stage
- * `skip_stage` in the producer (-1 turns it off), so that every consumer's
- * bounded wait gives up after `timeout_cycles` SM clock cycles (0 restores the
+ * `skip_stage` in the producer (-1 turns it off; in the prompt-shape kernel
+ * that holds the weights in tensor memory a stage is one scale group of 128
+ * K), so that every consumer's bounded wait gives up after `timeout_cycles`
+ * SM clock cycles (0 restores the
  * default limit of about two seconds).  The kernel then drains its copies and
  * MMAs in flight, frees its tensor memory and returns without writing C; the
  * next pq_check_device returns PQ_ERR_TIMEOUT.  Host state, process-wide, not
  * thread-safe; returns PQ_ERR_INVALID_ARG for skip_stage < -1.
  */
 int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles);
+
+/*
+ * Chooses the tensor-core kernel of the prompt shapes (M > 64): 0 (the
+ * default) the kernel that stages both operands in shared memory (the one
+ * that also serves small batches, block sums, Q5_0 weights and the
+ * allocation-free entry), 1 the kernel that holds the weight tiles in tensor
+ * memory.  Both compute the same qdot_t within its tolerance; the hook lets
+ * the tests and measurements run either.  Host state, process-wide, not
+ * thread-safe; PQ_ERR_INVALID_ARG for any other value.
+ */
+int pq_debug_set_prompt_kernel(int which);
+
+/*
+ * Registers a thread of the build of the tensor-memory prompt kernel that the
+ * current device admits with its 448 threads (several builds with different
+ * register limits exist; the largest that fits is used), or 0 if the device
+ * admits none and the prompt shapes run the shared-memory kernel.
+ */
+int pq_debug_prompt_kernel_regs(void);
 
 #ifdef __cplusplus
 }

@@ -22,10 +22,14 @@ def lib():
     return binding.load()
 
 
-def declared_functions():
-    text = open(os.path.join(ROOT, "include", "pq.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pq_\w+)\s*\(", text, flags=re.M)))
+def declared_functions(headers=None):
+    inc = os.path.join(ROOT, "include")
+    names = set()
+    for h in headers or sorted(f for f in os.listdir(inc) if f.endswith(".h")):
+        text = open(os.path.join(inc, h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pq_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_abi():
@@ -37,9 +41,19 @@ def test_header_declares_the_abi():
 
 
 def test_library_exports_every_declared_symbol(lib):
-    for n in declared_functions():
-        assert hasattr(lib, n), f"{n} declared in include/pq.h but not exported"
-    assert set(binding.EXPORTS) <= set(declared_functions())
+    names = declared_functions()
+    assert "pq_debug_set_tc_fault" in names and "pq_debug_set_prompt_kernel" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(binding.EXPORTS) <= set(declared_functions(["pq.h"]))
+
+
+def test_debug_hooks_reject_bad_values(lib):
+    lib.pq_debug_set_prompt_kernel.argtypes = [ctypes.c_int]
+    lib.pq_debug_set_tc_fault.argtypes = [ctypes.c_int, ctypes.c_ulonglong]
+    assert lib.pq_debug_set_prompt_kernel(2) == binding.PQ_ERR_INVALID_ARG
+    assert lib.pq_debug_set_prompt_kernel(-1) == binding.PQ_ERR_INVALID_ARG
+    assert lib.pq_debug_set_tc_fault(-2, 0) == binding.PQ_ERR_INVALID_ARG
 
 
 def test_version_and_strerror(lib):

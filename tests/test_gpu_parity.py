@@ -297,6 +297,62 @@ def test_qdot_tc_small(pq, M, N, K, layout):
     assert_within_bound(C, out, bound, f"tc M={M} N={N} K={K} layout={layout}")
 
 
+def _set_prompt_kernel(pq, which):
+    import ctypes
+    lib = pq.load()
+    lib.pq_debug_set_prompt_kernel.argtypes = [ctypes.c_int]
+    lib.pq_debug_set_prompt_kernel.restype = ctypes.c_int
+    assert lib.pq_debug_set_prompt_kernel(which) == 0
+
+
+PROMPT_SHAPES = [(65, 64, 256), (130, 200, 128), (256, 384, 1024), (300, 129, 256), (384, 2048, 1024),
+                 # few output tiles: K split over the CTAs, partial tiles added into C
+                 (128, 256, 4096), (200, 64, 2048), (96, 130, 512)]
+
+
+@pytest.mark.parametrize("which", [0, 1], ids=["smem_operands", "weights_in_tmem"])
+@pytest.mark.parametrize("M,N,K", PROMPT_SHAPES)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_prompt_kernels(pq, which, M, N, K, layout):
+    """Both tensor-core kernels of the prompt shapes (M > 64) against the oracle: the one
+    staging both operands in shared memory (the default) and the one holding the weight
+    tiles in tensor memory; ragged M and N, both scale layouts, split K."""
+    a, a_s, w, w_s = rand_operands(M * 7 + N * 3 + K + layout + 1000 * which, M, N, K)
+    out, bound = oracle.qdot(a, a_s, w, w_s, omp=True)
+    ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+    path = pq.PATH_TC if (layout == 0 or N % 4 == 0) else pq.PATH_AUTO
+    try:
+        _set_prompt_kernel(pq, which)
+        C = pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(ws), ws_layout=layout, path=path)
+        pq.check_device()
+    finally:
+        _set_prompt_kernel(pq, 0)
+    assert_within_bound(C, out, bound, f"kernel {which} M={M} N={N} K={K} layout={layout}")
+
+
+def test_weights_in_tmem_kernel_at_full_size(pq):
+    """The tensor-memory prompt kernel at the benchmark's full size (M = 512, K = 4096,
+    N = 14336) on one complete row per 128-row band and one column per 128-column band."""
+    name = "prompt_m512_k4096_n14336"
+    x, w, qa, sa, qw, sw = quantized_workload(name)
+    A, AS = pq.quantize_q8_0(dev(x))
+    W, WS = pq.quantize_q8_0(dev(w))
+    try:
+        _set_prompt_kernel(pq, 1)
+        C = host(pq.qdot_q8_0(A, AS, W, WS))
+        pq.check_device()
+    finally:
+        _set_prompt_kernel(pq, 0)
+    M, N = qa.shape[0], qw.shape[0]
+    rng = np.random.default_rng(3)
+    rows = np.array([b + rng.integers(0, min(128, M - b)) for b in range(0, M, 128)])
+    cols = np.array([b + rng.integers(0, min(128, N - b)) for b in range(0, N, 128)])
+    out, bound = oracle.qdot(qa[rows], sa[rows], qw, sw, omp=True)
+    assert_within_bound(C[rows], out, bound, "rows")
+    out, bound = oracle.qdot(qa, sa, qw[cols], sw[cols], omp=True)
+    assert_within_bound(C[:, cols], out, bound, "columns")
+
+
 def test_qdot_tc_unaligned_scales_fall_back(pq):
     """Scale planes 4- but not 16-byte aligned: auto path still correct (dp4a kernel)."""
     M, N, K = 40, 96, 256

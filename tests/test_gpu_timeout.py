@@ -25,9 +25,17 @@ def _hook(lib, stage, cycles):
     assert lib.pq_debug_set_tc_fault(stage, cycles) == 0
 
 
-@pytest.mark.parametrize("M", [16, 256])
-def test_tc_bounded_wait_gives_up_and_recovers(pq, M):
+def _prompt_kernel(lib, which):
+    lib.pq_debug_set_prompt_kernel.argtypes = [ctypes.c_int]
+    lib.pq_debug_set_prompt_kernel.restype = ctypes.c_int
+    assert lib.pq_debug_set_prompt_kernel(which) == 0
+
+
+@pytest.mark.parametrize("M,kernel", [(16, 0), (256, 0), (256, 1)],
+                         ids=["narrow_tiles", "prompt_smem_operands", "prompt_weights_in_tmem"])
+def test_tc_bounded_wait_gives_up_and_recovers(pq, M, kernel):
     lib = pq.load()
+    _prompt_kernel(lib, kernel)
     rng = np.random.default_rng(M)
     N, K = 256, 512
     a = workloads.random_int8(rng, (M, K))
@@ -46,7 +54,10 @@ def test_tc_bounded_wait_gives_up_and_recovers(pq, M):
     finally:
         _hook(lib, -1, 0)
     # the context is still usable and the next launch is correct
-    C = pq.qdot_q8_0_ex(A, AS, W, WS, path=pq.PATH_TC)
-    pq.check_device()
+    try:
+        C = pq.qdot_q8_0_ex(A, AS, W, WS, path=pq.PATH_TC)
+        pq.check_device()
+    finally:
+        _prompt_kernel(lib, 0)
     out, bound = oracle.qdot(a, a_s, w, w_s)
     assert np.all(np.abs(C.cpu().numpy().astype(np.float64) - out) <= bound)
