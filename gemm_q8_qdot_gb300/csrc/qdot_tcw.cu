@@ -1,5 +1,6 @@
-// qdot_t for prompt-sized M on the sm_103a tensor cores, with the weights held
-// in tensor memory as the MMA's A operand.
+// qdot_t for prompt-sized M on the sm_103a tensor cores, with the scales
+// applied in f32 registers (no scale-product MMA) and two Q8_0 blocks per
+// hand-off between the roles.
 //
 // What it computes ("Quantized built-ins and formats", section "Q8_0"; the
 // integer-tensor-core variant qmma_t in "Phobos Language Spec" section 10):
@@ -9,43 +10,41 @@
 // Engine.  As in the other tensor-core kernel: int8 values are exact in f16,
 // and every partial sum of one 32-element block (|S| <= 2^19 < 2^24) is exact
 // in the f32 accumulator, so two K = 16 kind::f16 MMAs into a fresh TMEM
-// buffer give the block sums S exactly.  The scales are applied by the
-// epilogue warps in f32 registers: acc[j, i] += w_scale[j] * (a_scale[i] * S).
+// buffer give the block sums S exactly.  The epilogue warps apply the scales
+// in f32 registers: acc[j, i] += w_scale[j] * (a_scale[i] * S).
 //
 // Orientation.  The MMA's 128-row side (TMEM lanes) is a tile of 128 weight
-// rows j; its N = 128 side is a tile of 128 activation rows i.  The weights are
-// converted int8 -> f16 by four converter warps, which read the TMA-loaded
-// int8 tile from shared memory and write the f16 rows straight into tensor
-// memory (tcgen05.st), where the MMA reads them as its A operand.  The
-// activations were converted once per call into f16 MMA tiles by a small
-// kernel (tile_act_kernel) and arrive by bulk copy.  So the only shared-memory
-// traffic per block is the activation tile (written once, read once by the
-// MMA), the int8 weight tile (written once, read once) and the scales: the
-// 128 x 128 x 16 f16 MMA alone would take the whole shared-memory bandwidth
-// if both operands came from there.
+// rows j; its N = 128 side is a tile of 128 activation rows i.  So a weight
+// scale is one value per TMEM lane (per epilogue thread row) and an
+// activation scale one value per column, and the activation scales can be laid
+// out in the order the epilogue threads read them.  The weights are widened
+// int8 -> f16 by four converter warps from the TMA-loaded int8 tile into the
+// f16 stage; the activations were converted once per call into f16 MMA tiles
+// by a small kernel (tile_act_kernel) and arrive by bulk copy.
 //
-// Tensor memory (512 columns): three 128-column accumulator buffers (one Q8_0
-// block each) and a ring of eight weight slots of 16 columns (one block of
-// 32 K f16 each).
+// Hand-offs.  One f16 stage holds 64 K (two Q8_0 blocks) of both operands,
+// and one accumulator buffer of 256 TMEM columns holds the block sums of those
+// two blocks (two buffers fill the 512 columns): the MMA issuer waits twice and
+// commits twice per two blocks.  (A version with one block per hand-off and the
+// weights in tensor memory was bound by the latency of its per-block hand-offs.)
 //
-// Warps (448 threads, one persistent CTA per SM over (activation tile, weight
+// Warps (704 threads, one persistent CTA per SM over (activation tile, weight
 // tile, K split) units, the activation tile fastest, so the CTAs running at
 // the same time share weight tiles in L2):
 //   warp 0      producer: per scale group (128 K) the int8 weight tile and
 //               the weight-scale box (TMA), the group's activation scales,
-//               and two 64-K f16 activation stages (bulk copies);
+//               and the activation tiles of two f16 stages (bulk copies);
 //   warp 1      MMA issuer (one thread), TMEM allocation;
-//   warps 2..5  converters, one per TMEM lane quadrant (warp % 4; 32 weight
-//               rows each);
-//   warps 6..13 epilogue: four lane quadrants x two column halves, each
-//               thread holding 4 weight rows x 16 activation rows of the
+//   warps 2..5  converters, 32 weight rows each;
+//   warps 6..21 epilogue: four TMEM lane quadrants x four column quarters,
+//               each thread holding 4 weight rows x 8 activation rows of the
 //               accumulator tile in registers; the unit's end stores C.
 //
 // Safety.  Every mbarrier wait is bounded (a clock64 limit).  A wait that
 // gives up sets this file's device status word and a CTA-wide abort flag;
 // every role then runs out its loops without waiting or working, copies and
 // MMAs in flight are drained with bounded waits, TMEM is freed and the kernel
-// returns.  The host reads the status through read_and_clear_status.
+// returns.  The host reads the status through read_and_clear_status_w.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -67,30 +66,31 @@ namespace {
 constexpr int TW = 128;                  // weight rows per tile (MMA M, TMEM lanes)
 constexpr int TA = 128;                  // activation rows per tile (MMA N)
 constexpr int GROUP = 4;                 // Q8_0 blocks per scale group (128 K)
-constexpr int kNbufD = 3;                // accumulator buffers, one block each
-constexpr int kWcol0 = kNbufD * TA;      // first TMEM column of the weight ring (384)
-constexpr int kWslots = 8;               // weight ring slots (one block = 16 columns)
-constexpr int kAct = TA * 64 * 2;        // one f16 activation stage: 128 rows x 64 K (16 KB)
+constexpr int kNbufD = 2;                // accumulator buffers of two blocks each (256 columns)
+constexpr int kAct = TA * 64 * 2;        // f16 activation tile of one stage: 128 rows x 64 K (16 KB)
+constexpr int kWt = TW * 64 * 2;         // f16 weight tile of one stage: 128 rows x 64 K (16 KB)
+constexpr int kStage = kAct + kWt;       // one f16 stage: two Q8_0 blocks of both operands
 constexpr int kAsc = GROUP * TA * 4;     // activation scales of one group (2 KB)
 constexpr int kW8 = TW * 128;            // int8 weight tile of one group (16 KB)
 constexpr int kWsc = TW * GROUP * 4;     // weight scales of one group (2 KB)
-constexpr int S16 = 6;                   // f16 activation stages
-constexpr int S8 = 4;                    // int8 weight stages (groups)
-constexpr int SR = 6;                    // scale slots (groups)
-constexpr int kOffAct = 0;
-constexpr int kOffW8 = kOffAct + S16 * kAct;
+constexpr int S16 = 4;                   // f16 stages
+constexpr int S8 = 3;                    // int8 weight stages (groups)
+constexpr int SR = 4;                    // scale slots (groups)
+constexpr int kOffSt = 0;
+constexpr int kOffW8 = kOffSt + S16 * kStage;
 constexpr int kOffSc = kOffW8 + S8 * kW8;          // slot: weight scales, then activation scales
 constexpr int kSc = kWsc + kAsc;
 constexpr int kOffBar = kOffSc + SR * kSc;
-constexpr int kNumBars = 2 * S16 + 2 * S8 + 2 * SR + 2 * kWslots + 2 * kNbufD + 1;
+constexpr int kNumBars = 2 * S16 + 2 * S8 + 2 * SR + 2 * kNbufD + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmem = kOffMisc + 16 + 1024;        // + alignment slack
-constexpr int kThreads = 448;            // 14 warps of 144 registers
+constexpr int kThreads = 704;            // 22 warps
 constexpr int kConv0 = 2;                // first converter warp
-constexpr int kEpi0 = 6;                 // first epilogue warp
+constexpr int kEpi0 = 6;                 // first epilogue warp (16 of them)
+constexpr int kNepi = 16;
 constexpr unsigned kBackoff = 64;        // ns between failed barrier tests of the waiting roles
 static_assert(kSmem <= 227 * 1024, "shared memory");
-static_assert(kAct % 1024 == 0 && kW8 % 1024 == 0 && kSc % 1024 == 0, "1024-byte aligned tiles");
+static_assert(kAct % 1024 == 0 && kWt % 1024 == 0 && kW8 % 1024 == 0 && kSc % 1024 == 0, "1024-byte aligned tiles");
 
 struct TcwParams {
     float* C;                  // C[i * N + j], [M, N] row-major
@@ -158,7 +158,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // NREG registers a thread (the launcher takes the largest build the device
-// admits with 448 threads)
+// admits with 704 threads)
 template <int NREG>
 __global__ void __maxnreg__(NREG)
 qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWS,
@@ -166,16 +166,14 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    uint64_t* full16 = bars;                  // f16 activation stage landed (producer, tx)
+    uint64_t* full16 = bars;                  // f16 stage ready: activations landed (tx) + 4 converter warps
     uint64_t* empty16 = full16 + S16;         // its MMAs completed (commit)
     uint64_t* full8 = empty16 + S16;          // int8 weight tile landed (producer, tx)
     uint64_t* empty8 = full8 + S8;            // converted (4 converter warps)
     uint64_t* sfull = empty8 + S8;            // scales of a group landed (producer, tx)
-    uint64_t* sempty = sfull + SR;            // read (8 epilogue warps)
-    uint64_t* wfull = sempty + SR;            // weight slot written to TMEM (4 converter warps)
-    uint64_t* wempty = wfull + kWslots;       // its MMAs completed (commit)
-    uint64_t* tfull = wempty + kWslots;       // block sums in an accumulator buffer (commit)
-    uint64_t* tempty = tfull + kNbufD;        // read (8 epilogue warps)
+    uint64_t* sempty = sfull + SR;            // read (16 epilogue warps)
+    uint64_t* tfull = sempty + SR;            // block sums of a pair of blocks in an accumulator buffer (commit)
+    uint64_t* tempty = tfull + kNbufD;        // read (16 epilogue warps)
     uint64_t* drain = tempty + kNbufD;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
@@ -208,7 +206,7 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     pdl_trigger();
     if (threadIdx.x == 0) {
         for (int i = 0; i < S16; ++i) {
-            tc::mbar_init(&full16[i], 1);
+            tc::mbar_init(&full16[i], 1 + 4);
             tc::mbar_init(&empty16[i], 1);
         }
         for (int i = 0; i < S8; ++i) {
@@ -217,15 +215,11 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         }
         for (int i = 0; i < SR; ++i) {
             tc::mbar_init(&sfull[i], 1);
-            tc::mbar_init(&sempty[i], 8);
-        }
-        for (int i = 0; i < kWslots; ++i) {
-            tc::mbar_init(&wfull[i], 4);
-            tc::mbar_init(&wempty[i], 1);  // the first kWslots / 2 are used: one per slot pair
+            tc::mbar_init(&sempty[i], kNepi);
         }
         for (int i = 0; i < kNbufD; ++i) {
             tc::mbar_init(&tfull[i], 1);
-            tc::mbar_init(&tempty[i], 8);
+            tc::mbar_init(&tempty[i], kNepi);
         }
         tc::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -275,7 +269,7 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
                                           prm.asc + (static_cast<int64_t>(un.a_tile) * prm.ngroups + g) * kAsc, kAsc,
                                           &sfull[sr]);
                     }
-                    // the group's two f16 activation stages
+                    // the activation tiles of the group's two f16 stages
 #pragma unroll 1
                     for (int h = 0; h < 2; ++h) {
                         const int si = 2 * gi + h;
@@ -283,14 +277,17 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
                         if (!bounded_wait(&empty16[s16], ((si / S16) & 1) ^ 1, abort_flag, limit, kBackoff)) continue;
                         issued16 = si + 1;
                         tc::mbar_arrive_expect_tx(&full16[s16], kAct);
-                        tc::bulk_copy_g2s(smem + kOffAct + s16 * kAct,
+                        tc::bulk_copy_g2s(smem + kOffSt + s16 * kStage,
                                           prm.act + (static_cast<int64_t>(un.a_tile) * (2 * prm.ngroups) + 2 * g + h) *
                                                         kAct,
                                           kAct, &full16[s16]);
                     }
                 }
             }
-            // copies in flight land before the CTA may exit (the skipped test group excepted)
+            // copies in flight land before the CTA may exit (the skipped test group excepted;
+            // an f16 stage also waits for the converters, whose arrivals are not awaited here,
+            // so the drain of the f16 ring waits for the bytes alone: a bounded wait that may
+            // report a timeout only after an abort)
             for (int i = max(0, issued8 - S8); i < issued8; ++i)
                 if (i != prm.inject_skip_stage) drain_wait(&full8[i % S8], (i / S8) & 1, limit);
             for (int i = max(0, issuedS - SR); i < issuedS; ++i)
@@ -300,38 +297,36 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // one f16 stage = two Q8_0 blocks = one hand-off: four K = 16 MMAs into the
+        // two 128-column halves of one accumulator buffer, one commit for the epilogue
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_f16_f32(TW, TA);
-            int gb = 0;  // blocks over all units of this CTA
+            int si = 0;  // f16 stages over all units of this CTA
             for (int u = u_first; u < prm.units; u += u_step) {
-                const int nblk = unit(u).ng * GROUP;
-                for (int k = 0; k < nblk; ++k, ++gb) {
-                    const int sw = gb % kWslots;
-                    const int si = gb >> 1;
+                const int nst = unit(u).ng * 2;
+                for (int k = 0; k < nst; ++k, ++si) {
                     const int s16 = si % S16;
-                    const int buf = gb % kNbufD;
-                    bool ok = bounded_wait(&wfull[sw], (gb / kWslots) & 1, abort_flag, limit, kBackoff);
-                    if ((gb & 1) == 0)
-                        ok = ok && bounded_wait(&full16[s16], (si / S16) & 1, abort_flag, limit, kBackoff);
-                    ok = ok && bounded_wait(&tempty[buf], ((gb / kNbufD) & 1) ^ 1, abort_flag, limit, kBackoff);
+                    const int buf = si % kNbufD;
+                    bool ok = bounded_wait(&full16[s16], (si / S16) & 1, abort_flag, limit, kBackoff);
+                    ok = ok && bounded_wait(&tempty[buf], ((si / kNbufD) & 1) ^ 1, abort_flag, limit, kBackoff);
                     if (ok) {
                         tc::tc_fence_after_sync();
-                        const uint32_t b0 = sbase + kOffAct + s16 * kAct;
+                        const uint32_t a0 = sbase + kOffSt + s16 * kStage;  // activations: the MMA's B
+                        const uint32_t w0 = a0 + kAct;                      // weights: the MMA's A
 #pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            const uint32_t koff = static_cast<uint32_t>(((gb & 1) * 2 + kk) * 32);  // 16 f16 = 32 B
-                            tc::umma_f16_tmem_a(tmem_base + static_cast<uint32_t>(buf * TA),
-                                                tmem_base + static_cast<uint32_t>(kWcol0 + sw * 16 + kk * 8),
-                                                tc::sw128_kmajor_desc(b0 + koff), idesc, kk);
-                        }
+                        for (int bb = 0; bb < 2; ++bb)
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                const uint32_t koff = static_cast<uint32_t>((bb * 2 + kk) * 32);  // 16 f16 = 32 B
+                                tc::umma_f16(tmem_base + static_cast<uint32_t>(buf * 2 * TA + bb * TA),
+                                             tc::sw128_kmajor_desc(w0 + koff), tc::sw128_kmajor_desc(a0 + koff),
+                                             idesc, kk);
+                            }
                     }
                     // the commits arrive also after an abort, so that every barrier
                     // keeps a consistent phase for the drains
                     tc::umma_commit(&tfull[buf]);
-                    if (gb & 1) {  // both blocks of the f16 stage and of the weight-slot pair done
-                        tc::umma_commit(&wempty[sw >> 1]);
-                        tc::umma_commit(&empty16[s16]);
-                    }
+                    tc::umma_commit(&empty16[s16]);
                 }
             }
             tc::umma_commit(drain);  // arrives when every MMA issued above has completed
@@ -339,12 +334,11 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         }
     } else if (warp >= kConv0 && warp < kEpi0) {
         // ------------------------------------------------------------ converters
-        // warp w converts weight rows 32 (w % 4) .. + 31 of the tile, one row per
-        // lane, into the TMEM lanes of the same numbers
-        const int quad = warp & 3;
-        const int row = quad * 32 + lane;
-        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-        int gi = 0, gb = 0;
+        // warp cw widens weight rows 32 cw .. 32 cw + 31 of the group's int8 tile, one row
+        // per lane, into the f16 weight tiles of the group's two stages (UMMA K-major
+        // 128-byte swizzle: row r at r * 128 bytes, 16-byte chunk c at (c ^ (r & 7)) << 4)
+        const int row = (warp - kConv0) * 32 + lane;
+        int gi = 0;
         for (int u = u_first; u < prm.units; u += u_step) {
             const int ng = unit(u).ng;
             for (int k = 0; k < ng; ++k, ++gi) {
@@ -352,31 +346,31 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
                 const bool ok8 = warp_wait(&full8[s8], (gi / S8) & 1, abort_flag, limit, lane, kBackoff);
                 const uint32_t w8 = sbase + kOffW8 + s8 * kW8 + row * 128;
 #pragma unroll 1
-                for (int bb = 0; bb < GROUP; ++bb, ++gb) {
-                    const int sw = gb % kWslots;
-                    // slots are released in pairs (the MMA's blocks 2p and 2p + 1)
-                    const bool ok = ok8 && ((gb & 1) || warp_wait(&wempty[sw >> 1], ((gb / kWslots) & 1) ^ 1, abort_flag,
-                                                                  limit, lane, kBackoff));
+                for (int h = 0; h < 2; ++h) {
+                    const int si = 2 * gi + h;
+                    const int s16 = si % S16;
+                    const bool ok = ok8 && warp_wait(&empty16[s16], ((si / S16) & 1) ^ 1, abort_flag, limit, lane,
+                                                     kBackoff);
                     if (ok) {
-                        // block bb = 16-byte chunks 2bb, 2bb + 1 of the row (128-byte swizzle)
-                        const uint4 v0 = tc::lds128(w8 + (((2 * bb) ^ (row & 7)) << 4));
-                        const uint4 v1 = tc::lds128(w8 + (((2 * bb + 1) ^ (row & 7)) << 4));
-                        uint32_t f[16];
-                        i8x4_to_f16x4(v0.x, f[0], f[1]);
-                        i8x4_to_f16x4(v0.y, f[2], f[3]);
-                        i8x4_to_f16x4(v0.z, f[4], f[5]);
-                        i8x4_to_f16x4(v0.w, f[6], f[7]);
-                        i8x4_to_f16x4(v1.x, f[8], f[9]);
-                        i8x4_to_f16x4(v1.y, f[10], f[11]);
-                        i8x4_to_f16x4(v1.z, f[12], f[13]);
-                        i8x4_to_f16x4(v1.w, f[14], f[15]);
-                        tc::tmem_st_32x32b_x16(t_lane + static_cast<uint32_t>(kWcol0 + sw * 16), f);
-                        tc::tmem_wait_st();
+                        const uint32_t w16 = sbase + kOffSt + s16 * kStage + kAct + row * 128;
+                        uint4 v[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) v[c] = tc::lds128(w8 + (((h * 4 + c) ^ (row & 7)) << 4));
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint4 o0, o1;
+                            i8x4_to_f16x4(v[c].x, o0.x, o0.y);
+                            i8x4_to_f16x4(v[c].y, o0.z, o0.w);
+                            i8x4_to_f16x4(v[c].z, o1.x, o1.y);
+                            i8x4_to_f16x4(v[c].w, o1.z, o1.w);
+                            tc::sts128(w16 + (((2 * c) ^ (row & 7)) << 4), o0);
+                            tc::sts128(w16 + (((2 * c + 1) ^ (row & 7)) << 4), o1);
+                        }
+                        tc::fence_proxy_async_smem();
                     }
-                    tc::tc_fence_before_sync();
                     __syncwarp();
                     // arrive also after an abort: every barrier keeps a consistent phase
-                    if (lane == 0) tc::mbar_arrive(&wfull[sw]);
+                    if (lane == 0) tc::mbar_arrive(&full16[s16]);
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&empty8[s8]);
@@ -384,20 +378,20 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         }
     } else if (warp >= kEpi0) {
         // ------------------------------------------------------------ epilogue
-        // thread (quadrant qd, column half ch, lane t): weight rows
-        // 32 qd + t/4 + {0, 8, 16, 24} and activation rows 64 ch + 8 r + 2 (t % 4) + {0, 1},
-        // r = 0..7, of the tile -- the 16x256b TMEM load layout over two 16-lane halves
+        // thread (quadrant qd, column quarter cq, lane t): weight rows
+        // 32 qd + t/4 + {0, 8, 16, 24} and activation rows 32 cq + 8 r + 2 (t % 4) + {0, 1},
+        // r = 0..3, of the tile -- the 16x256b TMEM load layout over two 16-lane halves
         const int qd = warp & 3;
-        const int ch = (warp - kEpi0) >> 2;
+        const int cq = (warp - kEpi0) >> 2;
         const int m = lane & 3;
         const int rr = lane >> 2;
         const uint32_t t_q = tmem_base + (static_cast<uint32_t>(qd * 32) << 16);
-        uint64_t acc[4][8];  // [row k][r]: f32 pair of activation rows (2m, 2m + 1) + 8r + 64ch
+        uint64_t acc[4][4];  // [row k][r]: f32 pair of activation rows (2m, 2m + 1) + 8r + 32cq
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
-            for (int r = 0; r < 8; ++r) acc[k][r] = 0ull;
-        int gi = 0, gb = 0;
+            for (int r = 0; r < 4; ++r) acc[k][r] = 0ull;
+        int gi = 0, si = 0;
         for (int u = u_first; u < prm.units; u += u_step) {
             const Unit un = unit(u);
             for (int kg = 0; kg < un.ng; ++kg, ++gi) {
@@ -406,62 +400,53 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
                 const uint32_t wsc = sbase + kOffSc + sr * kSc;
                 const uint32_t asc = wsc + kWsc;
 #pragma unroll 1
-                for (int bb = 0; bb < GROUP; ++bb, ++gb) {
-                    const int buf = gb % kNbufD;
-                    const bool ok = oks && warp_wait(&tfull[buf], (gb / kNbufD) & 1, abort_flag, limit, lane, 32);
+                for (int h = 0; h < 2; ++h, ++si) {
+                    const int buf = si % kNbufD;
+                    const bool ok = oks && warp_wait(&tfull[buf], (si / kNbufD) & 1, abort_flag, limit, lane, 32);
                     if (ok) {
                         tc::tc_fence_after_sync();
-                        // weight scales of the thread's four rows for block bb, as f32 pairs
-                        uint64_t w2[4];
+#pragma unroll 1
+                        for (int bl = 0; bl < 2; ++bl) {
+                            const int bb = h * 2 + bl;  // block within the group
+                            // weight scales of the thread's four rows for block bb, as f32 pairs
+                            uint64_t w2[4];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int row = qd * 32 + rr + 8 * k;
-                            const float w = tc::lds32f(wsc + (prm.ws_rowmajor ? row * GROUP + bb : bb * TW + row) * 4);
-                            w2[k] = f2_pack(__float_as_uint(w), __float_as_uint(w));
-                        }
-                        // activation scales of the thread's rows of 16-column chunk c:
-                        // [bb][ch][c][m][4] order, one 16-byte load per chunk, the four
-                        // threads m of a chunk reading 64 contiguous bytes
-                        const uint32_t as0 = asc + ((bb * 2 + ch) * 64 + m * 4) * 4;
-                        // The block's 64 columns in four chunks of 16 (two 16-lane halves,
-                        // 16 registers), double-buffered: the next chunk's TMEM load is in
-                        // flight while the current one is scaled into the accumulators, and the
-                        // buffer is handed back to the MMA as soon as its last load has landed.
-                        const uint32_t col0 = t_q + static_cast<uint32_t>(buf * TA + ch * 64);
-                        uint32_t sa0[8], sa1[8], sb0[8], sb1[8];
-                        auto load = [&](int c, uint32_t(&h0)[8], uint32_t(&h1)[8]) {
-                            tc::TmemLd16x256bX2::load(col0 + c * 16, h0);
-                            tc::TmemLd16x256bX2::load(col0 + (16u << 16) + c * 16, h1);
-                        };
-                        auto scale = [&](int c, const uint32_t(&h0)[8], const uint32_t(&h1)[8]) {
-                            const float4 av = tc::lds128f(as0 + c * 64);
-#pragma unroll
-                            for (int rl = 0; rl < 2; ++rl) {
-                                const int r = 2 * c + rl;
-                                const uint64_t a2 = rl ? f2_pack(__float_as_uint(av.z), __float_as_uint(av.w))
-                                                       : f2_pack(__float_as_uint(av.x), __float_as_uint(av.y));
-                                acc[0][r] = f2_fma(w2[0], f2_mul(a2, f2_pack(h0[4 * rl], h0[4 * rl + 1])), acc[0][r]);
-                                acc[1][r] = f2_fma(w2[1], f2_mul(a2, f2_pack(h0[4 * rl + 2], h0[4 * rl + 3])), acc[1][r]);
-                                acc[2][r] = f2_fma(w2[2], f2_mul(a2, f2_pack(h1[4 * rl], h1[4 * rl + 1])), acc[2][r]);
-                                acc[3][r] = f2_fma(w2[3], f2_mul(a2, f2_pack(h1[4 * rl + 2], h1[4 * rl + 3])), acc[3][r]);
+                            for (int k = 0; k < 4; ++k) {
+                                const int row = qd * 32 + rr + 8 * k;
+                                const float w =
+                                    tc::lds32f(wsc + (prm.ws_rowmajor ? row * GROUP + bb : bb * TW + row) * 4);
+                                w2[k] = f2_pack(__float_as_uint(w), __float_as_uint(w));
                             }
-                        };
-                        load(0, sa0, sa1);
-                        tc::tmem_wait_ld2x8(sa0, sa1);
-                        load(1, sb0, sb1);
-                        scale(0, sa0, sa1);
-                        tc::tmem_wait_ld2x8(sb0, sb1);
-                        load(2, sa0, sa1);
-                        scale(1, sb0, sb1);
-                        tc::tmem_wait_ld2x8(sa0, sa1);
-                        load(3, sb0, sb1);
-                        scale(2, sa0, sa1);
-                        tc::tmem_wait_ld2x8(sb0, sb1);
-                        // every load of this buffer has landed: hand it back before the last chunk
-                        tc::tc_fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&tempty[buf]);
-                        scale(3, sb0, sb1);
+                            // activation scales of the thread's rows of 16-column chunk c:
+                            // [bb][cq][c][m][4] order, one 16-byte load per chunk, the four
+                            // threads m of a chunk reading 64 contiguous bytes
+                            const uint32_t as0 = asc + ((bb * 4 + cq) * 32 + m * 4) * 4;
+                            const uint32_t col0 = t_q + static_cast<uint32_t>(buf * 2 * TA + bl * TA + cq * 32);
+#pragma unroll
+                            for (int c = 0; c < 2; ++c) {
+                                uint32_t h0[8], h1[8];  // lanes + 0..15 and + 16..31 of the quadrant
+                                tc::TmemLd16x256bX2::load(col0 + c * 16, h0);
+                                tc::TmemLd16x256bX2::load(col0 + (16u << 16) + c * 16, h1);
+                                const float4 av = tc::lds128f(as0 + c * 64);
+                                tc::tmem_wait_ld2x8(h0, h1);
+                                if (bl == 1 && c == 1) {
+                                    // every load of this buffer has landed: hand it back
+                                    tc::tc_fence_before_sync();
+                                    __syncwarp();
+                                    if (lane == 0) tc::mbar_arrive(&tempty[buf]);
+                                }
+#pragma unroll
+                                for (int rl = 0; rl < 2; ++rl) {
+                                    const int r = 2 * c + rl;
+                                    const uint64_t a2 = rl ? f2_pack(__float_as_uint(av.z), __float_as_uint(av.w))
+                                                           : f2_pack(__float_as_uint(av.x), __float_as_uint(av.y));
+                                    acc[0][r] = f2_fma(w2[0], f2_mul(a2, f2_pack(h0[4 * rl], h0[4 * rl + 1])), acc[0][r]);
+                                    acc[1][r] = f2_fma(w2[1], f2_mul(a2, f2_pack(h0[4 * rl + 2], h0[4 * rl + 3])), acc[1][r]);
+                                    acc[2][r] = f2_fma(w2[2], f2_mul(a2, f2_pack(h1[4 * rl], h1[4 * rl + 1])), acc[2][r]);
+                                    acc[3][r] = f2_fma(w2[3], f2_mul(a2, f2_pack(h1[4 * rl + 2], h1[4 * rl + 3])), acc[3][r]);
+                                }
+                            }
+                        }
                     } else {
                         tc::tc_fence_before_sync();
                         __syncwarp();
@@ -478,10 +463,10 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
                     const int64_t j = un.j0 + qd * 32 + rr + 8 * k;
                     if (j < prm.N) {
 #pragma unroll
-                        for (int r = 0; r < 8; ++r) {
+                        for (int r = 0; r < 4; ++r) {
 #pragma unroll
                             for (int c = 0; c < 2; ++c) {
-                                const int64_t i = un.i0 + ch * 64 + 8 * r + 2 * m + c;
+                                const int64_t i = un.i0 + cq * 32 + 8 * r + 2 * m + c;
                                 const float v = __uint_as_float(c ? static_cast<uint32_t>(acc[k][r] >> 32)
                                                                   : static_cast<uint32_t>(acc[k][r]));
                                 if (i < prm.M) {
@@ -499,7 +484,7 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 #pragma unroll
             for (int k = 0; k < 4; ++k)
 #pragma unroll
-                for (int r = 0; r < 8; ++r) acc[k][r] = 0ull;
+                for (int r = 0; r < 4; ++r) acc[k][r] = 0ull;
         }
     }
 
@@ -516,10 +501,10 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 //   * two f16 stages of 64 K: row r of the tile at r * 128 bytes, its 16-byte
 //     chunk c (K elements 8c .. 8c + 7) at ((c ^ (r & 7)) << 4) -- the UMMA
 //     K-major 128-byte-swizzle layout of the MMA's B operand;
-//   * the group's activation scales ordered [block b][column half h][chunk q]
-//     [m][e] for activation row 64 h + 8 (2 q + e / 2) + 2 m + e % 2: an epilogue
-//     thread (m = lane % 4) reads the four rows of its chunk q with one 16-byte
-//     load, the four threads m together 64 contiguous bytes.
+//   * the group's activation scales ordered [block b][column quarter cq][chunk q]
+//     [m][e] for activation row 32 cq + 8 (2 q + e / 2) + 2 m + e % 2: an
+//     epilogue thread (m = lane % 4) reads the four rows of its chunk q with one
+//     16-byte load, the four threads m together 64 contiguous bytes.
 // Rows past M are zero (their results are never stored).
 __global__ void __launch_bounds__(256)
 tile_act_kernel(const int8_t* __restrict__ A, const float* __restrict__ AS, uint8_t* __restrict__ act,
@@ -544,12 +529,13 @@ tile_act_kernel(const int8_t* __restrict__ A, const float* __restrict__ AS, uint
     }
     float* s = asc + static_cast<int64_t>(blockIdx.x) * (kAsc / 4);
     for (int i = threadIdx.x; i < GROUP * TA; i += blockDim.x) {
-        // i = (((b * 2 + h) * 4 + q) * 4 + m) * 4 + e: chunk q of 16 columns, element e = 2 rl + c
-        // of thread m, i.e. activation row 64 h + 8 (2 q + rl) + 2 m + c
+        // i = (((b * 4 + cq) * 2 + q) * 4 + m) * 4 + e: column quarter cq, chunk q of 16
+        // columns, element e = 2 rl + c of thread m, i.e. activation row
+        // 32 cq + 8 (2 q + rl) + 2 m + c
         const int b = i / TA, rem = i % TA;
-        const int h = rem / 64, q = (rem / 16) % 4, m = (rem / 4) % 4, e = rem % 4;
+        const int cq = rem / 32, q = (rem / 16) % 2, m = (rem / 4) % 4, e = rem % 4;
         const int r = 2 * q + e / 2, c = e % 2;
-        const int64_t row = tile * TA + 64 * h + 8 * r + 2 * m + c;
+        const int64_t row = tile * TA + 32 * cq + 8 * r + 2 * m + c;
         s[i] = row < M ? AS[row * KB + g * GROUP + b] : 0.0f;
     }
 }
@@ -585,7 +571,7 @@ EncodeTiledFn encode_fn() {
 
 using TcwKernel = void (*)(CUtensorMap, CUtensorMap, TcwParams);
 
-// The build of qdot_tcw_kernel with the most registers a thread whose 448
+// The build of qdot_tcw_kernel with the most registers a thread whose 704
 // threads the device admits in one block (the per-block register file is the
 // limit; the device, not the arithmetic, decides which one fits), with its
 // shared-memory size set; null if none.  Chosen once per device.
@@ -597,7 +583,7 @@ TcwKernel pick_kernel(int dev) {
     std::lock_guard<std::mutex> lk(mu);
     if (!have[dev]) {
         have[dev] = true;
-        const TcwKernel cands[3] = {qdot_tcw_kernel<144>, qdot_tcw_kernel<136>, qdot_tcw_kernel<128>};
+        const TcwKernel cands[3] = {qdot_tcw_kernel<88>, qdot_tcw_kernel<80>, qdot_tcw_kernel<72>};
         for (TcwKernel k : cands) {
             cudaFuncAttributes fa{};
             if (cudaFuncGetAttributes(&fa, k) != cudaSuccess || fa.maxThreadsPerBlock < kThreads) continue;
@@ -615,7 +601,8 @@ unsigned long long g_timeout = 4000000000ull;  // ~2 s at 2 GHz
 
 }  // namespace
 
-// Prompt shapes (M > 64) of qdot_t, block-scaled output only.
+// Prompt shapes (M > 64) of qdot_t, block-scaled output only (the launch
+// order: tile_act_kernel, the zeroing of C for split K, qdot_tcw_kernel).
 // cudaErrorNotSupported when the shape or the operands do not suit this kernel
 // (K % 128 != 0, scale planes that TMA cannot load, not sm_103) or when the
 // call may not allocate its activation workspace; the caller then takes the

@@ -27,20 +27,21 @@ int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles);
 
 /*
  * Chooses the tensor-core kernel of the prompt shapes (M > 64): 0 (the
- * default) the kernel that stages both operands in shared memory (the one
- * that also serves small batches, block sums, Q5_0 weights and the
- * allocation-free entry), 1 the kernel that holds the weight tiles in tensor
- * memory.  Both compute the same qdot_t within its tolerance; the hook lets
+ * default) the kernel with the scale-product MMA (the one that also serves
+ * small batches, block sums, Q5_0 weights and the allocation-free entry), 1
+ * the kernel that applies the scales in registers and hands two Q8_0 blocks
+ * at a time between its roles.  Both compute the same qdot_t within its tolerance; the hook lets
  * the tests and measurements run either.  Host state, process-wide, not
  * thread-safe; PQ_ERR_INVALID_ARG for any other value.
  */
 int pq_debug_set_prompt_kernel(int which);
 
 /*
- * Registers a thread of the build of the tensor-memory prompt kernel that the
- * current device admits with its 448 threads (several builds with different
- * register limits exist; the largest that fits is used), or 0 if the device
- * admits none and the prompt shapes run the shared-memory kernel.
+ * Registers a thread of the build of the second prompt kernel (see
+ * pq_debug_set_prompt_kernel) that the current device admits with its 704
+ * threads (several builds with different register limits exist; the largest
+ * that fits is used), or 0 if the device admits none and the prompt shapes
+ * run the first kernel.
  */
 int pq_debug_prompt_kernel_regs(void);
 

@@ -310,13 +310,13 @@ PROMPT_SHAPES = [(65, 64, 256), (130, 200, 128), (256, 384, 1024), (300, 129, 25
                  (128, 256, 4096), (200, 64, 2048), (96, 130, 512)]
 
 
-@pytest.mark.parametrize("which", [0, 1], ids=["smem_operands", "weights_in_tmem"])
+@pytest.mark.parametrize("which", [0, 1], ids=["scale_product_mma", "scales_in_registers"])
 @pytest.mark.parametrize("M,N,K", PROMPT_SHAPES)
 @pytest.mark.parametrize("layout", [0, 1])
 def test_prompt_kernels(pq, which, M, N, K, layout):
     """Both tensor-core kernels of the prompt shapes (M > 64) against the oracle: the one
-    staging both operands in shared memory (the default) and the one holding the weight
-    tiles in tensor memory; ragged M and N, both scale layouts, split K."""
+    with the scale-product MMA (the default) and the one applying the scales in registers;
+    ragged M and N, both scale layouts, split K."""
     a, a_s, w, w_s = rand_operands(M * 7 + N * 3 + K + layout + 1000 * which, M, N, K)
     out, bound = oracle.qdot(a, a_s, w, w_s, omp=True)
     ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
@@ -330,9 +330,10 @@ def test_prompt_kernels(pq, which, M, N, K, layout):
     assert_within_bound(C, out, bound, f"kernel {which} M={M} N={N} K={K} layout={layout}")
 
 
-def test_weights_in_tmem_kernel_at_full_size(pq):
-    """The tensor-memory prompt kernel at the benchmark's full size (M = 512, K = 4096,
-    N = 14336) on one complete row per 128-row band and one column per 128-column band."""
+def test_second_prompt_kernel_at_full_size(pq):
+    """The second prompt kernel (scales in registers) at the benchmark's full size (M = 512,
+    K = 4096, N = 14336) on one complete row per 128-row band and one column per 128-column
+    band."""
     name = "prompt_m512_k4096_n14336"
     x, w, qa, sa, qw, sw = quantized_workload(name)
     A, AS = pq.quantize_q8_0(dev(x))

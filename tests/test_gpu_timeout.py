@@ -4,7 +4,7 @@ The tensor-core kernel's producer is told (test hook, include/pq_debug.h) to
 skip one pipeline stage, so the consumers' waits on that stage never complete.
 Every wait is bounded: the kernel must give up within its limit, record the
 timeout in the library's status word, drain its work in flight, free its
-tensor memory and return.  The test checks the reported status and that the
+tensor memory and return.  Both prompt-shape kernels are covered.  The test checks the reported status and that the
 context stays usable (a normal launch afterwards gives correct results).
 """
 import ctypes
@@ -32,7 +32,7 @@ def _prompt_kernel(lib, which):
 
 
 @pytest.mark.parametrize("M,kernel", [(16, 0), (256, 0), (256, 1)],
-                         ids=["narrow_tiles", "prompt_smem_operands", "prompt_weights_in_tmem"])
+                         ids=["narrow_tiles", "prompt_first_kernel", "prompt_second_kernel"])
 def test_tc_bounded_wait_gives_up_and_recovers(pq, M, kernel):
     lib = pq.load()
     _prompt_kernel(lib, kernel)
