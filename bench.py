@@ -401,6 +401,27 @@ def time_graph(prob: Problem, steps: int, warmup: int, world: int, sampler=None)
     return ms, quant_ms, qdot_ms, qdot_only_ms, (t0, t1)
 
 
+def time_reader(prob: Problem, steps: int, early: bool) -> float:
+    """Mean time of the test-only streaming reader (the one-row step's weight traffic without
+    its arithmetic) over the same rotating weight copies, K launches in one graph (ms)."""
+    import torch
+    out = torch.empty((prob.wl.N,), dtype=torch.float32, device=prob.x.device)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for t in range(2):
+            prob.pq.debug_stream_read(prob.W[t % prob.copies], prob.WS[t % prob.copies], out, early=early)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for t in range(steps):
+            prob.pq.debug_stream_read(prob.W[t % prob.copies], prob.WS[t % prob.copies], out, early=early)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    return _replay_ms(g, stream) / steps
+
+
 def time_e2e(prob: Problem, steps: int, warmup: int):
     """Through the public API with host buffers, per step: the H2D copy of x from pinned host
     memory, the decode step, the D2H copy of C into pinned host memory (for Q8_0 weights one
@@ -496,6 +517,10 @@ def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sample
            "kernel_ms": kernel_ms,
            "roofline": roofline_for(prob, dom_ms, peaks, peak_src, one_kernel), "weight_copies": prob.copies,
            "window": window}
+    if wl.M == 1 and not prob.q50 and split[1] == 1:
+        # the floor launch chaining sets: the same weight traffic with no arithmetic
+        res["stream_reader_ms"] = {"chained": round(time_reader(prob, steps, False), 5),
+                                   "early": round(time_reader(prob, steps, True), 5)}
     if prob.fused and split[1] == 1:
         # the same step as two calls (quantizer, then qdot_t), for comparison
         two = Problem(pq, wl, device, fused=False)
@@ -706,6 +731,12 @@ def final_line(head: dict, others: dict, cpus: dict, args, world: int, clocks: d
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
     if args.workload in cpus:
         line["cpu_baseline"] = cpus[args.workload]
+    variants = {}
+    if "stream_reader_ms" in head:
+        variants["reader_chained_ms"] = head["stream_reader_ms"]["chained"]
+        variants["reader_early_ms"] = head["stream_reader_ms"]["early"]
+    if variants:
+        line["step_variants"] = variants
     prompt = head if args.workload == PROMPT else others.get(PROMPT)
     if prompt and "roofline" in prompt:
         rl = {k: prompt["roofline"][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}

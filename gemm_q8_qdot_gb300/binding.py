@@ -27,6 +27,7 @@ PATH_AUTO, PATH_SIMT, PATH_TC, PATH_MMA = 0, 1, 2, 3
 WS_N_KB, WS_KB_N = 0, 1
 
 EXPORTS = ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
+           "pq_last_cuda_error",
            "pq_quantize_qdot_q8_0_noalloc", "pq_quantize_qdot_q8_0_host", "pq_qdot_q8_0_blocksums", "pq_q50_qdot",
            "pq_quantize_q50_qdot", "pq_q50_blocksums", "pq_check_device", "pq_strerror", "pq_version")
 
@@ -57,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pq_qdot_q8_0.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp]
     lib.pq_qdot_q8_0_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp]
     lib.pq_quantize_qdot_q8_0.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
+    lib.pq_last_cuda_error.argtypes = []
+    lib.pq_debug_stream_read.argtypes = [vp, vp, i64, i64, vp, i32, vp]
     lib.pq_quantize_qdot_q8_0_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_quantize_qdot_q8_0_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.pq_qdot_q8_0_blocksums.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
@@ -68,6 +71,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pq_strerror.restype = ctypes.c_char_p
     lib.pq_version.argtypes = []
     for fn in ("pq_quantize_q8_0", "pq_qdot_q8_0", "pq_qdot_q8_0_ex", "pq_quantize_qdot_q8_0",
+               "pq_last_cuda_error", "pq_debug_stream_read",
                "pq_quantize_qdot_q8_0_noalloc", "pq_quantize_qdot_q8_0_host", "pq_qdot_q8_0_blocksums",
                "pq_q50_qdot", "pq_quantize_q50_qdot", "pq_q50_blocksums", "pq_check_device", "pq_version"):
         getattr(lib, fn).restype = ctypes.c_int
@@ -162,6 +166,17 @@ def quantize_qdot_q8_0(x, W, WS, C=None, A=None, AS=None, ws_layout: int = WS_N_
     _check(load().pq_quantize_qdot_q8_0(_ptr(x), _ptr(A), _ptr(AS), _ptr(W), _ptr(WS), _ptr(C), M, N, K,
                                         int(ws_layout), _stream(stream)), "pq_quantize_qdot_q8_0")
     return C
+
+
+def debug_stream_read(W, WS, out=None, early: bool = False, stream=None):
+    """Test-only: the decode step's weight stream without its arithmetic (pq_debug_stream_read);
+    out[row] receives a checksum of the row."""
+    rows, K = W.shape
+    if out is None:
+        out = torch.empty((rows,), dtype=torch.float32, device=W.device)
+    _check(load().pq_debug_stream_read(_ptr(W), _ptr(WS), rows, K, _ptr(out), int(early), _stream(stream)),
+           "pq_debug_stream_read")
+    return out
 
 
 def quantize_qdot_q8_0_host(x_host, W, WS, C_host, ws_layout: int = WS_N_KB, stream=None):

@@ -345,6 +345,14 @@ int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles) {
 
 int pq_debug_prompt_kernel_regs(void) { return pq::tcw_kernel_regs(); }
 
+int pq_debug_stream_read(const int8_t* W, const float* WS, int64_t rows, int64_t K, float* out, int early,
+                         cudaStream_t stream) {
+    if (!W || !WS || !out || rows <= 0 || K < 32 || K % 32 != 0 || (early != 0 && early != 1))
+        return PQ_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W) & 31u) != 0 || !aligned(WS, 4) || !aligned(out, 4)) return PQ_ERR_ALIGN;
+    return map_cuda(pq::launch_stream_read(W, WS, rows, K, out, early, stream));
+}
+
 int pq_debug_set_prompt_kernel(int which) {
     if (which != 0 && which != 1) return PQ_ERR_INVALID_ARG;
     pq::set_prompt_kernel(which);

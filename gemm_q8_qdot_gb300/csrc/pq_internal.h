@@ -61,6 +61,13 @@ cudaError_t launch_qdot_simt(const QdotArgs& a, cudaStream_t stream);
 // quantized row does not fit a CTA's shared memory).
 cudaError_t launch_qdot_fused(const FusedArgs& a, cudaStream_t stream);
 
+// Test-only streaming reader: reads `rows` weight rows of K bytes and their
+// K/32 f32 scales exactly as the fused decode step does (same grid, loads and
+// launch chaining), computes nothing but a checksum per row (out[row]).
+// early = 1 issues the first round of loads before griddepcontrol.wait.
+cudaError_t launch_stream_read(const int8_t* W, const float* WS, int64_t rows, int64_t K, float* out, int early,
+                               cudaStream_t stream);
+
 // dp4a kernel for Q5_0 weights (q50_qdot_t): a.W points at the 20-byte Q5_0
 // blocks, [N, K/32 * 20] bytes; any M.
 cudaError_t launch_qdot_q50(const QdotArgs& a, cudaStream_t stream);

@@ -367,6 +367,82 @@ cudaError_t launch_qdot_fused(const FusedArgs& a, cudaStream_t stream) {
                             : launch_fused<4, 1, kFusedWarps>(a, v8, sms, stream);
 }
 
+namespace {
+
+// Test-only streaming reader: the fused decode step's memory traffic without
+// its arithmetic.  One warp per weight row (kFusedWarps rows per CTA, at most
+// one CTA per SM), the same L2 prefetch before griddepcontrol.wait, the same
+// 256-bit evict-first loads of U blocks per lane and of their scales; the
+// loaded words are folded into a checksum per row so that no load is dead.
+template <bool EARLY>
+__global__ void __launch_bounds__(kFusedWarps * 32)
+stream_read_kernel(const int8_t* __restrict__ W, const float* __restrict__ WS, int64_t rows, int64_t K,
+                   float* __restrict__ out) {
+    constexpr int U = 4;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t KB = K >> 5;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * kFusedWarps + warp;
+    const bool jv = j < rows;
+    const int8_t* wrow = W + (jv ? j : 0) * K;
+    if (lane == 0 && jv) {
+        const int64_t kb = K < kPrefetchBytes ? K : kPrefetchBytes;
+        prefetch_l2(wrow, static_cast<uint32_t>(kb));
+        if ((reinterpret_cast<uintptr_t>(WS + j * KB) & 15) == 0 && (kb / 32 * 4) % 16 == 0)
+            prefetch_l2(WS + j * KB, static_cast<uint32_t>(kb / 32 * 4));
+    }
+    const uint64_t wpol = l2_weight_policy(true);
+    u32x8 wv[U];
+    float wsv[U];
+    auto load_round = [&](int64_t bb) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t b = bb + u * 32 + lane;
+            if (jv && b < KB) {
+                wv[u] = ld_wblock<true>(wrow + b * 32, wpol);
+                wsv[u] = ld_wscale(WS + j * KB + b, wpol);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) wv[u].v[t] = 0u;
+                wsv[u] = 0.0f;
+            }
+        }
+    };
+    if constexpr (EARLY) load_round(0);
+    pdl_wait();
+    pdl_trigger();
+    if constexpr (!EARLY) load_round(0);
+    uint32_t h = 0;
+    float s = 0.0f;
+    for (int64_t bb = 0; bb < KB; bb += 32 * U) {
+        if (bb > 0) load_round(bb);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) h += wv[u].v[t];
+            s += wsv[u];
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        h += __shfl_xor_sync(0xffffffffu, h, o);
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+    }
+    if (lane == 0 && jv) out[j] = s + static_cast<float>(h & 0xffu);
+}
+
+}  // namespace
+
+cudaError_t launch_stream_read(const int8_t* W, const float* WS, int64_t rows, int64_t K, float* out, int early,
+                               cudaStream_t stream) {
+    if ((reinterpret_cast<uintptr_t>(W) & 31u) != 0 || K % 32 != 0 || rows <= 0) return cudaErrorInvalidValue;
+    const int64_t grid = (rows + kFusedWarps - 1) / kFusedWarps;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    return early ? launch_pdl(stream_read_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kFusedWarps * 32), 0,
+                              stream, W, WS, rows, K, out)
+                 : launch_pdl(stream_read_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kFusedWarps * 32), 0,
+                              stream, W, WS, rows, K, out);
+}
+
 cudaError_t launch_qdot_simt(const QdotArgs& a, cudaStream_t stream) {
     // 256-bit loads need 32-byte aligned blocks: every row starts at a multiple
     // of 32 bytes from its base (K % 32 == 0), so only the bases decide.

@@ -8,6 +8,9 @@
 #ifndef PQ_DEBUG_H
 #define PQ_DEBUG_H
 
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -44,6 +47,22 @@ int pq_debug_set_prompt_kernel(int which);
  * run the first kernel.
  */
 int pq_debug_prompt_kernel_regs(void);
+
+/*
+ * A streaming reader with the memory traffic of the one-row decode step and
+ * none of its arithmetic, for measuring the floor that launch chaining and the
+ * weight stream set on that step: `rows` weight rows W [rows, K] int8
+ * (32-byte aligned base) and their scales WS [rows, K/32] f32 are read with
+ * the step's grid (32 rows per CTA), L2 prefetch, 256-bit evict-first loads and
+ * programmatic launch chaining; out[row] receives a checksum of the row (so no
+ * load can be dropped).  early = 1 issues the first round of loads before the
+ * wait for the preceding kernel (valid here because the reader's inputs are
+ * never written while it runs).  Device
+ * pointers; asynchronous on `stream`; PQ_ERR_INVALID_ARG / PQ_ERR_ALIGN on bad
+ * arguments.
+ */
+int pq_debug_stream_read(const int8_t* W, const float* WS, int64_t rows, int64_t K, float* out, int early,
+                         cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -206,3 +206,13 @@ def test_noalloc_rejects_the_shapes_the_allocating_step_rejects(lib):
     assert noalloc(lib, M=1 << 20, K=4096) == binding.PQ_ERR_SCRATCH
     assert noalloc(lib, x=None) == binding.PQ_ERR_INVALID_ARG
     assert noalloc(lib, layout=2) == binding.PQ_ERR_INVALID_ARG
+
+
+def test_stream_reader_entry_checks(lib):
+    """pq_debug_stream_read rejects bad arguments before anything is launched."""
+    d = lib.pq_debug_stream_read
+    assert d(P16, P16, 0, 32, P16, 0, None) == binding.PQ_ERR_INVALID_ARG
+    assert d(P16, P16, 4, 40, P16, 0, None) == binding.PQ_ERR_INVALID_ARG
+    assert d(P16, P16, 4, 32, P16, 2, None) == binding.PQ_ERR_INVALID_ARG
+    assert d(P16 + 16, P16, 4, 32, P16, 0, None) == binding.PQ_ERR_ALIGN  # W must be 32-byte aligned
+    assert d(P16, P2, 4, 32, P16, 0, None) == binding.PQ_ERR_ALIGN

@@ -467,6 +467,21 @@ def test_quantize_qdot_fused(pq, M, N, K, layout):
     assert_within_bound(C2, out, bound, "fused, no A/AS")
 
 
+def test_stream_reader_checksums(pq):
+    """The test-only streaming reader reads every weight row: its per-row checksum (the
+    32-bit word sum's low byte plus the sum of the row's scales) matches the host's."""
+    rng = np.random.default_rng(4)
+    for rows, K in ((4096, 4096), (100, 14336), (33, 128)):
+        w = workloads.random_int8(rng, (rows, K))
+        ws = workloads.random_scales(rng, (rows, K // 32))
+        words = w.view(np.uint32).astype(np.uint64).reshape(rows, -1).sum(axis=1)
+        ref = ws.astype(np.float64).sum(axis=1) + (words & 0xff).astype(np.float64)
+        for early in (False, True):
+            out = host(pq.debug_stream_read(dev(w), dev(ws), early=early))
+            torch.cuda.synchronize()
+            assert np.allclose(out, ref, rtol=1e-5, atol=1e-3), (rows, K, early)
+
+
 def test_quantize_qdot_large_m(pq):
     """M > 1 runs the quantizer and qdot_t as two kernels, into A / AS or the workspace."""
     M, N, K = 40, 96, 256
