@@ -445,6 +445,15 @@ def time_e2e(prob: Problem, steps: int, warmup: int):
     return dt, prob.x_host.numel() * 4, prob.C_host.numel() * 4
 
 
+def set_host_path(pq, which: int) -> None:
+    """Test hook of the host-buffer step: 0 host buffers in place (default), 1 copies."""
+    lib = pq.load()
+    lib.pq_debug_set_host_path.argtypes = [ctypes.c_int]
+    lib.pq_debug_set_host_path.restype = ctypes.c_int
+    if lib.pq_debug_set_host_path(int(which)) != 0:
+        raise RuntimeError("pq_debug_set_host_path failed")
+
+
 def fused_is_one_kernel(prob: Problem) -> bool:
     """Whether the one-call step runs as a single fused kernel for this shape:
     pq_quantize_qdot_q8_0 for one row (any N, its CTAs take further columns beyond
@@ -531,8 +540,17 @@ def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sample
     if e2e:
         dt, h2d, d2h = time_e2e(prob, steps, warmup)
         ev, _ = aggregate(units, dt, world, device)
+        # x is copied in, C written in place into page-locked host memory over the
+        # chip-to-chip link; the bytes still cross between host and device
         res["e2e"] = {"value": round(ev / scale, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h}
+        if not prob.q50 and prob.world == 1:
+            set_host_path(pq, 1)
+            try:
+                dt2, _, _ = time_e2e(prob, steps, warmup)
+            finally:
+                set_host_path(pq, 0)
+            res["e2e_copies"] = {"value": round(units / dt2 / scale, 3), "unit": unit}
     del prob
     import torch
     torch.cuda.empty_cache()
@@ -735,6 +753,8 @@ def final_line(head: dict, others: dict, cpus: dict, args, world: int, clocks: d
     if "stream_reader_ms" in head:
         variants["reader_chained_ms"] = head["stream_reader_ms"]["chained"]
         variants["reader_early_ms"] = head["stream_reader_ms"]["early"]
+    if "e2e_copies" in head:
+        variants["e2e_with_copies"] = head["e2e_copies"]["value"]
     if variants:
         line["step_variants"] = variants
     prompt = head if args.workload == PROMPT else others.get(PROMPT)

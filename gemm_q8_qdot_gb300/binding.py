@@ -181,8 +181,8 @@ def debug_stream_read(W, WS, out=None, early: bool = False, stream=None):
 
 def quantize_qdot_q8_0_host(x_host, W, WS, C_host, ws_layout: int = WS_N_KB, stream=None):
     """pq_quantize_qdot_q8_0_host: one decode step from host x_host [M, K] f32 into host C_host
-    [M, N] f32 (both page-locked CPU tensors); enqueued on the stream, which the caller
-    synchronizes before reading C_host."""
+    [M, N] f32 (a page-locked C_host is written in place by the kernels, a pageable one through
+    a copy); enqueued on the stream, which the caller synchronizes before reading C_host."""
     if x_host.dtype != torch.float32 or C_host.dtype != torch.float32:
         raise TypeError("x_host and C_host must be float32")
     if x_host.is_cuda or C_host.is_cuda:

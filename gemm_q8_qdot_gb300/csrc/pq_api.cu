@@ -91,6 +91,23 @@ bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p
 // The CUDA error behind this thread's last PQ_ERR_CUDA / PQ_ERR_UNSUPPORTED.
 thread_local int g_last_cuda_error = 0;
 
+// 0: host buffers the device can address are used in place; 1: always copied
+// (test hook, pq_debug_set_host_path).
+int g_host_path = 0;
+
+// The device address of a page-locked host buffer that the device can access
+// (registered or allocated with cudaHostAlloc, mapped), or null for any other
+// pointer (pageable or device memory); leaves no CUDA error behind.
+void* device_view(const void* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+    return at.devicePointer;
+}
+
 int map_cuda(cudaError_t e) {
     if (e == cudaSuccess) return PQ_OK;
     g_last_cuda_error = static_cast<int>(e);
@@ -221,6 +238,22 @@ int pq_quantize_qdot_q8_0_host(const float* x_host, const int8_t* W, const float
     if (M == 0 || N == 0) return PQ_OK;
     if (!x_host || !W || !WS || !C_host) return PQ_ERR_INVALID_ARG;
     if (!aligned(W, 16) || !aligned(WS, 4)) return PQ_ERR_ALIGN;
+    // C in page-locked host memory the device can address (on GB300 host memory
+    // is reached over the coherent chip-to-chip link): the step writes it there
+    // itself, with no device-to-host copy.  x is still copied in (one copy into
+    // this stream's workspace): read in place, every CTA of the step would pull
+    // the whole row over the link.
+    float* cd = g_host_path == 0 ? static_cast<float*>(device_view(C_host)) : nullptr;
+    if (cd && aligned(cd, 4)) {
+        const size_t xbytes = static_cast<size_t>(M * K) * sizeof(float);
+        void* ws = nullptr;
+        cudaError_t e = pq::stream_workspace(stream, xbytes, &ws, 1);
+        if (e != cudaSuccess) return map_cuda(e);
+        e = cudaMemcpyAsync(ws, x_host, xbytes, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return map_cuda(e);
+        return pq_quantize_qdot_q8_0(static_cast<const float*>(ws), nullptr, nullptr, W, WS, cd, M, N, K, ws_layout,
+                                     stream);
+    }
     // device copies of x and C in this stream's staging workspace
     const size_t xbytes = static_cast<size_t>(M * K) * sizeof(float);
     const size_t cbytes = static_cast<size_t>(M * N) * sizeof(float);
@@ -344,6 +377,12 @@ int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles) {
 }
 
 int pq_debug_prompt_kernel_regs(void) { return pq::tcw_kernel_regs(); }
+
+int pq_debug_set_host_path(int which) {
+    if (which != 0 && which != 1) return PQ_ERR_INVALID_ARG;
+    g_host_path = which;
+    return PQ_OK;
+}
 
 int pq_debug_stream_read(const int8_t* W, const float* WS, int64_t rows, int64_t K, float* out, int early,
                          cudaStream_t stream) {

@@ -165,17 +165,22 @@ int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W,
                           float* C, int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);
 
 /*
- * One decode step with the activations and the result in host memory: the
- * host-to-device copy of x_host [M, K] f32, pq_quantize_qdot_q8_0 on that copy
- * (A = AS = NULL), and the device-to-host copy of the result into C_host
- * [M, N] f32, all enqueued on `stream` in that order.  The call returns once
- * they are enqueued: synchronize the stream before reading C_host.  x_host and
- * C_host should be page-locked (cudaHostAlloc or cudaHostRegister) for the
- * copies to run asynchronously.  The device copies of x and C live in a
- * workspace of this (device, stream) pair, allocated on the first call on the
- * stream and grown when a larger one arrives (that call must not be inside a
- * stream capture; see the top of this header).  W, WS and the rules of the contraction
- * as for pq_quantize_qdot_q8_0.
+ * One decode step with the activations and the result in host memory:
+ * x_host [M, K] f32 in, C_host [M, N] f32 out, the rules of the contraction as
+ * for pq_quantize_qdot_q8_0 (A = AS = NULL).  The call returns once the work is
+ * enqueued on `stream`: synchronize the stream before reading C_host.
+ *   - When C_host is page-locked host memory that the device can address
+ *     (cudaHostAlloc / cudaHostRegister, mapped: on GB300 the host memory is
+ *     reached over the coherent chip-to-chip link), the host-to-device copy of
+ *     x and the step are enqueued, and the step's kernels write C into C_host
+ *     directly (no device-to-host copy).
+ *   - Otherwise (pageable C_host) the host-to-device copy of x, the step, and
+ *     the device-to-host copy of C are enqueued in that order.
+ * The device copies of x (and of C) live in a workspace of this (device,
+ * stream) pair, allocated on the first such call on the stream and grown when a
+ * larger one arrives (that call must not be inside a stream capture; see the
+ * top of this header).  Pageable buffers make the copies synchronous.
+ * W and WS as for pq_quantize_qdot_q8_0.
  */
 int pq_quantize_qdot_q8_0_host(const float* x_host, const int8_t* W, const float* WS, float* C_host,
                                int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);

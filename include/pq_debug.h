@@ -64,6 +64,15 @@ int pq_debug_prompt_kernel_regs(void);
 int pq_debug_stream_read(const int8_t* W, const float* WS, int64_t rows, int64_t K, float* out, int early,
                          cudaStream_t stream);
 
+/*
+ * How pq_quantize_qdot_q8_0_host reaches its result buffer: 0 (the default)
+ * the kernels write C_host in place when it is page-locked host memory the
+ * device can address, else through a copy; 1 always through a copy.  Both give the same results; the
+ * hook lets the tests and measurements run either.  Host state, process-wide,
+ * not thread-safe; PQ_ERR_INVALID_ARG for any other value.
+ */
+int pq_debug_set_host_path(int which);
+
 #ifdef __cplusplus
 }
 #endif

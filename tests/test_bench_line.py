@@ -25,7 +25,8 @@ def _fake(name):
           "kernel": "qdot_tc", "peak_source": "measured hbm_gbs", "algorithmic_bytes": 123456789}
     if tensor:
         rl.update(int8_library_tops=155.5, frac_of_int8_library=2.034)
-    extra = {} if tensor else {"stream_reader_ms": {"chained": 0.0047612, "early": 0.0040123}}
+    extra = {} if tensor else {"stream_reader_ms": {"chained": 0.0047612, "early": 0.0040123},
+                               "e2e_copies": {"value": 604.123, "unit": "GB/s"}}
     return {**extra, "value": 12345.678, "unit": "TOPS" if tensor else "GB/s", "ms_per_step": 0.1234567,
             "step": "pq_quantize_q8_0 + pq_qdot_q8_0", "roofline": rl, "weight_copies": 15,
             "kernel_ms": {"dominant": 0.12345}, "e2e": {"value": 604.123, "unit": "GB/s",
@@ -69,7 +70,7 @@ def test_final_line_holds_every_workload_at_its_end():
         assert k in line, k
     for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
         assert k in line["roofline"] and k in line["prompt"]["roofline"], k
-    assert set(line["step_variants"]) == {"reader_chained_ms", "reader_early_ms"}
+    assert set(line["step_variants"]) == {"reader_chained_ms", "reader_early_ms", "e2e_with_copies"}
 
 
 def test_compact_keeps_errors_short():

@@ -519,12 +519,48 @@ def test_quantize_qdot_workload_full(pq, name):
 
 # ------------------------------------------------------------------ host-buffer decode step
 
+def _host_path(pq, which):
+    import ctypes
+    lib = pq.load()
+    lib.pq_debug_set_host_path.argtypes = [ctypes.c_int]
+    lib.pq_debug_set_host_path.restype = ctypes.c_int
+    assert lib.pq_debug_set_host_path(which) == 0
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (1, 9800, 256), (4, 300, 1024), (1, 64, 256), (12, 500, 1024)])
 @pytest.mark.parametrize("layout", [0, 1])
-def test_quantize_qdot_host_buffers(pq, M, N, K, layout):
-    """x and C in page-locked host memory: the copies and the step enqueued by one call;
-    the result matches the oracle on the quantized rows, and a second call of another
-    size on the same stream (workspace regrown) is correct too."""
+@pytest.mark.parametrize("copies", [False, True], ids=["in_place", "copies"])
+def test_quantize_qdot_host_buffers(pq, M, N, K, layout, copies):
+    """x and C in page-locked host memory: x copied in, C written in place by the step's
+    kernels (the default), or C copied out too (forced by the test hook); the result
+    matches the oracle on the quantized rows, and a second call of another size on the
+    same stream (workspace regrown) is correct too."""
+    _host_path(pq, 1 if copies else 0)
+    try:
+        _host_buffers_case(pq, M, N, K, layout)
+    finally:
+        _host_path(pq, 0)
+
+
+def test_quantize_qdot_pageable_host_buffers(pq):
+    """Pageable (not page-locked) host buffers take the copy path: same results."""
+    M, N, K = 1, 512, 1024
+    rng = np.random.default_rng(77)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    _, _, w, w_s = rand_operands(78, 1, N, K)
+    qa, sa = oracle.quantize_q8_0(x)
+    out, bound = oracle.qdot(qa, sa, w, w_s)
+    x_host = torch.from_numpy(x.copy())
+    C_host = torch.full((M, N), float("nan"), dtype=torch.float32)
+    assert not x_host.is_pinned() and not C_host.is_pinned()
+    stream = torch.cuda.Stream()
+    pq.quantize_qdot_q8_0_host(x_host, dev(w), dev(w_s), C_host, stream=stream)
+    stream.synchronize()
+    pq.check_device()
+    assert_within_bound(C_host.numpy(), out, bound, "pageable host buffers")
+
+
+def _host_buffers_case(pq, M, N, K, layout):
     rng = np.random.default_rng(M * 7 + N + K + layout)
     x = (rng.standard_normal((M, K)) * np.exp(rng.uniform(-3, 3, size=(M, 1)))).astype(np.float32)
     _, _, w, w_s = rand_operands(N + 5 * K, 1, N, K)
