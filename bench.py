@@ -77,6 +77,8 @@ KERNEL_SOURCES = {
     "qdot_q50": ["gemm_q8_qdot_gb300/csrc/qdot_q50.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
     "qdot_mma": ["gemm_q8_qdot_gb300/csrc/qdot_mma.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
     "qdot_q50_fused": ["gemm_q8_qdot_gb300/csrc/qdot_q50.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
+    "qdot_tcw": ["gemm_q8_qdot_gb300/csrc/qdot_tcw.cu", "gemm_q8_qdot_gb300/csrc/tc_ptx.cuh",
+                 "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
 }
 
 
