@@ -76,6 +76,8 @@ KERNEL_SOURCES = {
     "qdot_fused": ["gemm_q8_qdot_gb300/csrc/qdot_simt.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
     "qdot_q50": ["gemm_q8_qdot_gb300/csrc/qdot_q50.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
     "qdot_mma": ["gemm_q8_qdot_gb300/csrc/qdot_mma.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
+    "qdot_mmt": ["gemm_q8_qdot_gb300/csrc/qdot_mmt.cu", "gemm_q8_qdot_gb300/csrc/tc_ptx.cuh",
+                 "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
     "qdot_q50_fused": ["gemm_q8_qdot_gb300/csrc/qdot_q50.cu", "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
     "qdot_tcw": ["gemm_q8_qdot_gb300/csrc/qdot_tcw.cu", "gemm_q8_qdot_gb300/csrc/tc_ptx.cuh",
                  "gemm_q8_qdot_gb300/csrc/pq_device.cuh"],
@@ -476,10 +478,10 @@ def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str, one_kernel
         achieved = nbytes / (qdot_ms * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])
         # the kernel the automatic path runs for this M (pq_api.cu: dp4a up to 8
-        # rows, the warp-level MMA for 9..16, tcgen05 above)
+        # rows, the TMA-fed warp-level MMA kernel for 9..16, tcgen05 above)
         kernel = ("qdot_q50_fused" if one_kernel else "qdot_q50") if prob.q50 else \
             ("qdot_fused" if one_kernel else "qdot_simt") if wl.M <= 8 else \
-            "qdot_mma" if wl.M <= 16 else "qdot_tc"
+            "qdot_mmt" if wl.M <= 16 else "qdot_tc"
         traffic = recorded_traffic(kernel, wl.name)
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,

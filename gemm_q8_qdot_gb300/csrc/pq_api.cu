@@ -154,12 +154,14 @@ int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS
     if (path == PQ_PATH_TC) return map_cuda(pq::launch_qdot_tc(a, stream));
     if (path == PQ_PATH_MMA) return map_cuda(pq::launch_qdot_mma(a, stream));
     // automatic, by M (measured on GB300 at K = 4096, N = 11008, graphs of
-    // back-to-back calls): the dp4a streaming kernel up to 8 rows (12.3 us at
-    // M = 4, 17.3 us at M = 8), the warp-level MMA kernel for 9..16 rows (24.7 us
-    // at M = 16, against 31.8 us for dp4a and 28.6 us for tcgen05), the tcgen05
-    // kernel above (30.6 us at M = 32, 39.6 us at M = 64); a shape a kernel
-    // declines (K % 128 != 0 for tcgen05) goes to the dp4a kernel, which takes
-    // every shape
+    // back-to-back calls): the dp4a streaming kernel up to 8 rows (12.6 us at
+    // M = 4, 17.3 us at M = 8, against 19.1 us for the TMA-fed warp-level MMA
+    // kernel), the warp-level MMA path for 9..16 rows (19.1 us at M = 16 with
+    // its TMA-fed kernel, against 31.9 us for dp4a and 29.2 us for tcgen05),
+    // the tcgen05 kernel above (30.8 us at M = 32, 34.2 us at M = 64, against
+    // 32.8 and 47.5 us for the TMA-fed kernel); a shape a kernel declines
+    // (K % 128 != 0 for tcgen05) goes to the dp4a kernel, which takes every
+    // shape
     cudaError_t e = cudaErrorNotSupported;
     if (M > 16) e = pq::launch_qdot_tc(a, stream);
     else if (M > 8) e = pq::launch_qdot_mma(a, stream);
@@ -345,10 +347,11 @@ int pq_q50_blocksums(const int8_t* A, const uint8_t* W5, int32_t* S, int64_t M, 
 
 int pq_check_device(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return PQ_ERR_CUDA;
-    unsigned status = 0, status_w = 0;
+    unsigned status = 0, status_w = 0, status_m = 0;
     if (pq::read_and_clear_status(&status) != cudaSuccess) return PQ_ERR_CUDA;
     if (pq::read_and_clear_status_w(&status_w) != cudaSuccess) return PQ_ERR_CUDA;
-    return (status | status_w) ? PQ_ERR_TIMEOUT : PQ_OK;
+    if (pq::read_and_clear_status_mmt(&status_m) != cudaSuccess) return PQ_ERR_CUDA;
+    return (status | status_w | status_m) ? PQ_ERR_TIMEOUT : PQ_OK;
 }
 
 const char* pq_strerror(int code) {
@@ -373,6 +376,13 @@ int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles) {
     if (skip_stage < -1) return PQ_ERR_INVALID_ARG;
     pq::set_tc_test_hooks(skip_stage, timeout_cycles);
     pq::set_tcw_test_hooks(skip_stage, timeout_cycles);
+    pq::set_mmt_test_hooks(skip_stage, timeout_cycles);
+    return PQ_OK;
+}
+
+int pq_debug_set_small_kernel(int which) {
+    if (which != 0 && which != 1) return PQ_ERR_INVALID_ARG;
+    pq::set_small_kernel(which);
     return PQ_OK;
 }
 

@@ -100,6 +100,18 @@ cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream);
 // quantized rows.  cudaErrorNotSupported as for launch_qdot_mma.
 cudaError_t launch_qdot_mma_fused(const FusedArgs& a, cudaStream_t stream);
 
+// Warp-level MMA kernel fed by TMA (qdot_mmt.cu) for 1 <= M <= 64, scaled
+// output only: weights streamed into a shared-memory ring by a producer warp,
+// K split over a thread-block cluster.  With X non-null it quantizes X [M, K]
+// itself (a.A / a.AS unused; Aq / ASq, when non-null, receive the quantized
+// rows).  cudaErrorNotSupported for shapes or alignments it does not take
+// (block-sum mode, K < 128, N < 32, bases of W / WS / A / X not 16-byte
+// aligned, K/32 % 4 != 0 with WS [N, K/32], N % 4 != 0 with WS [K/32, N],
+// shared memory too small for the K chunk) and when set_small_kernel(0)
+// selected the register-fed kernel of qdot_mma.cu.
+cudaError_t launch_qdot_mmt(const QdotArgs& a, const float* X, int8_t* Aq, float* ASq, cudaStream_t stream);
+void set_small_kernel(int which);
+
 // A workspace of at least `bytes` for work enqueued on `stream` of the current
 // device (one per device, stream and kind, so calls on different streams never
 // share it; allocated stream-ordered on first use, replaced by one at least
@@ -121,12 +133,14 @@ int qdot_noalloc(const int8_t* A, const float* AS, const int8_t* W, const float*
 // a bounded wait that gave up).
 cudaError_t read_and_clear_status(unsigned* status);
 cudaError_t read_and_clear_status_w(unsigned* status);
+cudaError_t read_and_clear_status_mmt(unsigned* status);
 
 // Test hooks of the tensor-core kernel: skip one producer stage so that the
 // consumers' bounded waits give up (-1: off), and the wait limit in SM clock
 // cycles (0: the default of about two seconds).
 void set_tc_test_hooks(int inject_skip_stage, unsigned long long timeout_cycles);
 void set_tcw_test_hooks(int inject_skip_group, unsigned long long timeout_cycles);
+void set_mmt_test_hooks(int inject_skip_stage, unsigned long long timeout_cycles);
 // Registers a thread of the prompt kernel build chosen for the current device
 // (0: the device admits none, the shared-memory kernel runs instead).
 int tcw_kernel_regs();

@@ -508,6 +508,11 @@ cudaError_t launch_mma(MmaParams p, bool sums, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream) {
+    // the TMA-fed kernel where it applies, else this file's
+    if (a.S == nullptr) {
+        const cudaError_t e = launch_qdot_mmt(a, nullptr, nullptr, nullptr, stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
     MmaParams p{};
     p.A = a.A;
     p.AS = a.AS;
@@ -524,6 +529,11 @@ cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_qdot_mma_fused(const FusedArgs& f, cudaStream_t stream) {
+    {
+        const QdotArgs a{nullptr, nullptr, f.W, f.WS, f.C, nullptr, f.M, f.N, f.K, f.ws_layout};
+        const cudaError_t e = launch_qdot_mmt(a, f.x, f.A, f.AS, stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
     MmaParams p{};
     p.X = f.x;
     p.Aq = f.A;

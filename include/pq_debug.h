@@ -16,15 +16,18 @@ extern "C" {
 #endif
 
 /*
- * Makes the next tensor-core qdot launches (PQ_PATH_TC) skip pipeline stage
- * `skip_stage` in the producer (-1 turns it off; in the prompt-shape kernel
- * that holds the weights in tensor memory a stage is one scale group of 128
- * K), so that every consumer's bounded wait gives up after `timeout_cycles`
- * SM clock cycles (0 restores the
- * default limit of about two seconds).  The kernel then drains its copies and
- * MMAs in flight, frees its tensor memory and returns without writing C; the
- * next pq_check_device returns PQ_ERR_TIMEOUT.  Host state, process-wide, not
- * thread-safe; returns PQ_ERR_INVALID_ARG for skip_stage < -1.
+ * Makes the next launches of the pipelined kernels skip pipeline stage
+ * `skip_stage` in the producer (-1 turns it off): the tensor-core kernels
+ * (PQ_PATH_TC; in the prompt-shape kernel that holds the weights in tensor
+ * memory a stage is one scale group of 128 K) and the TMA-fed warp-level MMA
+ * kernel of few rows (PQ_PATH_MMA, and the automatic path where it runs that
+ * kernel; a stage is 128 weight rows x 4 blocks of one CTA's K chunk), so
+ * that every consumer's bounded wait gives up after `timeout_cycles` SM clock
+ * cycles (0 restores the default limit of about two seconds).  The kernel
+ * then drains its copies and MMAs in flight, frees its tensor memory and
+ * returns; C is left undefined.  The next pq_check_device returns
+ * PQ_ERR_TIMEOUT.  Host state, process-wide, not thread-safe; returns
+ * PQ_ERR_INVALID_ARG for skip_stage < -1.
  */
 int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles);
 
@@ -38,6 +41,18 @@ int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles);
  * thread-safe; PQ_ERR_INVALID_ARG for any other value.
  */
 int pq_debug_set_prompt_kernel(int which);
+
+/*
+ * Chooses the warp-level MMA kernel of few rows (PQ_PATH_MMA, 1 <= M <= 64,
+ * and the automatic paths that use it): 1 (the default) the kernel whose
+ * producer warp streams the weights into shared memory by TMA, with K split
+ * over a thread-block cluster, wherever it takes the shape; 0 the kernel whose
+ * computing warps load their own weight bytes.  Both compute the same qdot_t
+ * within its tolerance; the hook lets the tests and measurements run either.
+ * Host state, process-wide, not thread-safe; PQ_ERR_INVALID_ARG for any other
+ * value.
+ */
+int pq_debug_set_small_kernel(int which);
 
 /*
  * Registers a thread of the build of the second prompt kernel (see

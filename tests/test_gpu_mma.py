@@ -5,7 +5,12 @@ Same bars as the other paths: outputs within |C - out| <= 1e-5 * sum_b |t_b| +
 one to four 16-row m-tiles, ragged weight-row tiles (N not a multiple of 8 or
 64), single-block K, K split over clusters of CTAs (including a short last
 split), both weight-scale layouts, graph capture, and the full-size workloads.
+The path has two kernels (include/pq_debug.h, pq_debug_set_small_kernel): the
+TMA-fed one (the default, wherever it takes the shape) and the register-fed
+one; the shape tests run both.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -24,9 +29,23 @@ MMA_SHAPES = [(1, 1, 32), (1, 64, 128), (2, 7, 32), (3, 65, 256), (5, 130, 1056)
               (4, 8, 128), (8, 100, 512), (12, 333, 2048), (16, 1000, 4096), (16, 5000, 1024)]
 
 
+def set_small_kernel(pq, which):
+    lib = pq.load()
+    lib.pq_debug_set_small_kernel.argtypes = [ctypes.c_int]
+    lib.pq_debug_set_small_kernel.restype = ctypes.c_int
+    assert lib.pq_debug_set_small_kernel(which) == 0
+
+
+@pytest.fixture(params=[1, 0], ids=["tma_fed", "register_fed"])
+def small_kernel(pq, request):
+    set_small_kernel(pq, request.param)
+    yield request.param
+    set_small_kernel(pq, 1)
+
+
 @pytest.mark.parametrize("M,N,K", MMA_SHAPES)
 @pytest.mark.parametrize("layout", [0, 1])
-def test_qdot_mma(pq, M, N, K, layout):
+def test_qdot_mma(pq, small_kernel, M, N, K, layout):
     a, a_s, w, w_s = rand_operands(M * 131 + N * 7 + K + layout, M, N, K)
     out, bound = oracle.qdot(a, a_s, w, w_s)
     ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
@@ -112,7 +131,7 @@ def test_qdot_mma_workload_full(pq, name):
 # ------------------------------------------------------------------ fused step, 9..16 rows
 
 @pytest.mark.parametrize("M,N,K", [(9, 300, 1024), (12, 1000, 4096), (16, 129, 96), (14, 700, 14336)])
-def test_fused_step_equals_quantizer_then_mma(pq, M, N, K):
+def test_fused_step_equals_quantizer_then_mma(pq, small_kernel, M, N, K):
     """pq_quantize_qdot_q8_0 at 9..16 rows quantizes inside the MMA kernel: its rows,
     scales and C are bit-identical to the quantizer followed by this path's qdot_t."""
     rng = np.random.default_rng(M * 17 + N + K)
@@ -160,3 +179,48 @@ def test_fused_step_in_a_graph(pq, M):
         assert np.array_equal(host(A), qa) and np.array_equal(host(AS).view(np.uint32), sa.view(np.uint32))
         out, bound = oracle.qdot(qa, sa, w, w_s)
         assert_within_bound(C, out, bound, "graph replay")
+
+
+# ------------------------------------------------------------------ the TMA-fed kernel
+
+@pytest.mark.parametrize("M", [1, 16, 17, 33, 64])
+def test_tma_kernel_block_sums_exact(pq, M):
+    """Weights widened to 1152 + w with the MMA started at -1152 * sum(a): with unit
+    scales and four blocks per row, C is the exact integer sum of four block sums
+    (each up to 32 * 128 * 128 in magnitude), equal to the oracle's int64 sums."""
+    N, K = 200, 128
+    rng = np.random.default_rng(M)
+    a = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+    w = rng.integers(-128, 128, size=(N, K), dtype=np.int8)
+    a[0, :32] = -128
+    w[:, :32] = -128            # block 0 of row 0: +32 * 2^14
+    w[1::2, 32:64] = 127
+    a[:, 32:64] = -128          # block 1: -32 * 128 * 127 on odd weight rows
+    ones_a = np.ones((M, K // 32), dtype=np.float32)
+    ones_w = np.ones((N, K // 32), dtype=np.float32)
+    exact = oracle.blocksums(a, w).sum(axis=2)
+    for layout in (0, 1):
+        ws = ones_w if layout == 0 else np.ascontiguousarray(ones_w.T)
+        C = pq.qdot_q8_0_ex(dev(a), dev(ones_a), dev(w), dev(ws), ws_layout=layout, path=pq.PATH_MMA)
+        pq.check_device()
+        assert np.array_equal(host(C).astype(np.int64), exact), f"layout {layout}"
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 32, 128), (3, 33, 4224), (16, 11008, 4096), (20, 4100, 14336),
+                                   (40, 999, 2560), (64, 4096, 4096), (16, 100, 480)])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_tma_kernel_chunks_and_passes(pq, M, N, K, layout):
+    """K chunks of whole four-block stages with a short last chunk (K = 4224, 2560,
+    480), clusters owning ragged tile ranges and several 128-row passes, rows past N
+    in the last TMA box (zero-filled), against the oracle on sampled columns."""
+    a, a_s, w, w_s = rand_operands(M + N + K + layout, M, N, K)
+    ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+    C = pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(ws), ws_layout=layout, path=pq.PATH_MMA)
+    pq.check_device()
+    rng = np.random.default_rng(K)
+    cols = np.unique(np.concatenate([rng.choice(N, min(N, 300), replace=False), np.arange(min(N, 40)),
+                                     np.arange(max(0, N - 40), N)]))
+    out, bound = oracle.qdot(a, a_s, w[cols], w_s[cols])
+    got = host(C)[:, cols].astype(np.float64)
+    bad = np.abs(got - out) > bound
+    assert not bad.any(), f"{int(bad.sum())} elements out of bound, M={M} N={N} K={K}"

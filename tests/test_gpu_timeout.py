@@ -1,10 +1,12 @@
 """Failure detection on the GPU without a fault: a bounded wait is made to run out.
 
-The tensor-core kernel's producer is told (test hook, include/pq_debug.h) to
+The producer of a pipelined kernel is told (test hook, include/pq_debug.h) to
 skip one pipeline stage, so the consumers' waits on that stage never complete.
 Every wait is bounded: the kernel must give up within its limit, record the
 timeout in the library's status word, drain its work in flight, free its
-tensor memory and return.  Both prompt-shape kernels are covered.  The test checks the reported status and that the
+tensor memory and return.  Covered: the tcgen05 kernel (narrow tiles and both
+prompt-shape kernels) and the TMA-fed warp-level MMA kernel, whose CTAs also
+wait on one another across their cluster.  The test checks the reported status and that the
 context stays usable (a normal launch afterwards gives correct results).
 """
 import ctypes
@@ -31,13 +33,16 @@ def _prompt_kernel(lib, which):
     assert lib.pq_debug_set_prompt_kernel(which) == 0
 
 
-@pytest.mark.parametrize("M,kernel", [(16, 0), (256, 0), (256, 1)],
-                         ids=["narrow_tiles", "prompt_first_kernel", "prompt_second_kernel"])
-def test_tc_bounded_wait_gives_up_and_recovers(pq, M, kernel):
+@pytest.mark.parametrize("M,kernel,path", [(16, 0, "tc"), (256, 0, "tc"), (256, 1, "tc"), (16, 0, "mma"),
+                                           (48, 0, "mma")],
+                         ids=["narrow_tiles", "prompt_first_kernel", "prompt_second_kernel", "tma_fed_mma",
+                              "tma_fed_mma_two_groups"])
+def test_tc_bounded_wait_gives_up_and_recovers(pq, M, kernel, path):
     lib = pq.load()
     _prompt_kernel(lib, kernel)
+    path = pq.PATH_TC if path == "tc" else pq.PATH_MMA
     rng = np.random.default_rng(M)
-    N, K = 256, 512
+    N, K = 256, 2048
     a = workloads.random_int8(rng, (M, K))
     w = workloads.random_int8(rng, (N, K))
     a_s = workloads.random_scales(rng, (M, K // 32))
@@ -47,7 +52,7 @@ def test_tc_bounded_wait_gives_up_and_recovers(pq, M, kernel):
     try:
         _hook(lib, 1, 20_000_000)  # ~10 ms at 2 GHz
         C = torch.full((M, N), 123.0, device="cuda")
-        pq.qdot_q8_0_ex(A, AS, W, WS, C, path=pq.PATH_TC)
+        pq.qdot_q8_0_ex(A, AS, W, WS, C, path=path)
         with pytest.raises(pq.PQError) as ei:
             pq.check_device()
         assert ei.value.code == pq.PQ_ERR_TIMEOUT
@@ -55,7 +60,7 @@ def test_tc_bounded_wait_gives_up_and_recovers(pq, M, kernel):
         _hook(lib, -1, 0)
     # the context is still usable and the next launch is correct
     try:
-        C = pq.qdot_q8_0_ex(A, AS, W, WS, path=pq.PATH_TC)
+        C = pq.qdot_q8_0_ex(A, AS, W, WS, path=path)
         pq.check_device()
     finally:
         _prompt_kernel(lib, 0)
