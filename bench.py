@@ -461,13 +461,14 @@ def set_host_path(pq, which: int) -> None:
 def fused_is_one_kernel(prob: Problem) -> bool:
     """Whether the one-call step runs as a single fused kernel for this shape:
     pq_quantize_qdot_q8_0 for one row (any N, its CTAs take further columns beyond
-    one per SM) and for 9..16 rows (the warp-level MMA kernel quantizes the rows
-    itself); pq_quantize_q50_qdot for one row (32 columns per CTA, at most two waves)."""
+    one per SM; 9..16 rows are the quantizer and the TMA-fed warp-level MMA
+    kernel); pq_quantize_q50_qdot for one row (32 columns per CTA, at most two
+    waves)."""
     import torch
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     if prob.q50:
         return prob.wl.M == 1 and -(-prob.wl.N // 32) <= 2 * sms
-    return prob.wl.M == 1 or 9 <= prob.wl.M <= 16
+    return prob.wl.M == 1
 
 
 def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str, one_kernel: bool = False):
@@ -514,7 +515,7 @@ def run_workload(pq, name, steps, warmup, world, device, peaks, peak_src, sample
     else:
         kernel_ms.update({"quantize": round(quant_ms, 5), "qdot": round(qdot_ms, 5)})
     # duration of the dominant kernel: a step that is one kernel (the fused decode
-    # step, or the fused step of 9..16 rows) is timed exactly by the step time;
+    # step) is timed exactly by the step time;
     # otherwise the mean launch of a graph
     # of that kernel alone (event-record nodes between kernels add their own
     # latency, so the in-graph event figure is an upper bound, reported beside it)

@@ -73,11 +73,13 @@ extern "C" int pq_quantize_qdot_q8_0_noalloc(const float* x, const int8_t* W, co
     if (!x || !W || !WS || !C) return PQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(W, 16) || !aligned(WS, 4) || !aligned(C, 4)) return PQ_ERR_ALIGN;
 
-    // one kernel where the one-call step has one (one row; 9..16 rows): its CTAs
-    // quantize the rows themselves and the scratch is not touched
+    // one kernel where the one-call step has one (one row; 9..16 rows with the
+    // register-fed warp-level MMA kernel selected): its CTAs quantize the rows
+    // themselves and the scratch is not touched
     const pq::FusedArgs f{x, nullptr, nullptr, W, WS, C, M, N, K, ws_layout};
     cudaError_t e = pq::launch_qdot_fused(f, stream);
-    if (e == cudaErrorNotSupported && M > 8 && M <= 16) e = pq::launch_qdot_mma_fused(f, stream);
+    if (e == cudaErrorNotSupported && M > 8 && M <= 16 && pq::small_kernel() == 0)
+        e = pq::launch_qdot_mma_fused(f, stream);
     if (e != cudaErrorNotSupported)
         return e == cudaSuccess ? PQ_OK : e == cudaErrorInvalidConfiguration ? PQ_ERR_UNSUPPORTED : PQ_ERR_CUDA;
 

@@ -211,9 +211,13 @@ int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W,
     pq::FusedArgs f{x, A, AS, W, WS, C, M, N, K, ws_layout};
     cudaError_t e = pq::launch_qdot_fused(f, stream);
     if (e != cudaErrorNotSupported) return map_cuda(e);
-    // 9..16 rows (the warp-level MMA path of qdot_t): one kernel as well, whose
-    // CTAs quantize the rows of their K ranges themselves
-    if (M > 8 && M <= 16) {
+    // 9..16 rows with the register-fed warp-level MMA kernel selected
+    // (pq_debug_set_small_kernel(0)): one kernel as well, whose CTAs quantize
+    // the rows of their K ranges themselves.  With the TMA-fed kernel (the
+    // default) the quantizer followed by qdot_t is faster (21.0 against 25.0
+    // us at K = 4096, N = 11008: every CTA of a one-kernel step quantizes its
+    // K chunk of all rows again)
+    if (M > 8 && M <= 16 && pq::small_kernel() == 0) {
         e = pq::launch_qdot_mma_fused(f, stream);
         if (e != cudaErrorNotSupported) return map_cuda(e);
     }

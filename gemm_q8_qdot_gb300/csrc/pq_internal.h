@@ -102,15 +102,15 @@ cudaError_t launch_qdot_mma_fused(const FusedArgs& a, cudaStream_t stream);
 
 // Warp-level MMA kernel fed by TMA (qdot_mmt.cu) for 1 <= M <= 64, scaled
 // output only: weights streamed into a shared-memory ring by a producer warp,
-// K split over a thread-block cluster.  With X non-null it quantizes X [M, K]
-// itself (a.A / a.AS unused; Aq / ASq, when non-null, receive the quantized
-// rows).  cudaErrorNotSupported for shapes or alignments it does not take
-// (block-sum mode, K < 128, N < 32, bases of W / WS / A / X not 16-byte
-// aligned, K/32 % 4 != 0 with WS [N, K/32], N % 4 != 0 with WS [K/32, N],
-// shared memory too small for the K chunk) and when set_small_kernel(0)
-// selected the register-fed kernel of qdot_mma.cu.
-cudaError_t launch_qdot_mmt(const QdotArgs& a, const float* X, int8_t* Aq, float* ASq, cudaStream_t stream);
+// K split over a thread-block cluster.  cudaErrorNotSupported for shapes or
+// alignments it does not take (block-sum mode, K < 128, N < 32, W or WS not
+// 16-byte aligned, K/32 % 4 != 0 with WS [N, K/32], N % 4 != 0 with WS
+// [K/32, N], shared memory too small for the K chunk) and when
+// set_small_kernel(0) selected the register-fed kernel of qdot_mma.cu.
+// small_kernel() returns the selection (1: this kernel where it applies).
+cudaError_t launch_qdot_mmt(const QdotArgs& a, cudaStream_t stream);
 void set_small_kernel(int which);
+int small_kernel();
 
 // A workspace of at least `bytes` for work enqueued on `stream` of the current
 // device (one per device, stream and kind, so calls on different streams never

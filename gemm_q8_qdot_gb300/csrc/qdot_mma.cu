@@ -510,7 +510,7 @@ cudaError_t launch_mma(MmaParams p, bool sums, cudaStream_t stream) {
 cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream) {
     // the TMA-fed kernel where it applies, else this file's
     if (a.S == nullptr) {
-        const cudaError_t e = launch_qdot_mmt(a, nullptr, nullptr, nullptr, stream);
+        const cudaError_t e = launch_qdot_mmt(a, stream);
         if (e != cudaErrorNotSupported) return e;
     }
     MmaParams p{};
@@ -529,11 +529,6 @@ cudaError_t launch_qdot_mma(const QdotArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_qdot_mma_fused(const FusedArgs& f, cudaStream_t stream) {
-    {
-        const QdotArgs a{nullptr, nullptr, f.W, f.WS, f.C, nullptr, f.M, f.N, f.K, f.ws_layout};
-        const cudaError_t e = launch_qdot_mmt(a, f.x, f.A, f.AS, stream);
-        if (e != cudaErrorNotSupported) return e;
-    }
     MmaParams p{};
     p.X = f.x;
     p.Aq = f.A;

@@ -111,11 +111,8 @@ struct MmtCfg {
 };
 
 struct MmtParams {
-    const int8_t* A;    // [M, K] (null in the fused step)
+    const int8_t* A;    // [M, K]
     const float* AS;    // [M, K/32]
-    const float* X;     // fused step: f32 [M, K], quantized in the staging; else null
-    int8_t* Aq;         // fused step: optional outputs, the quantized rows and their scales
-    float* ASq;
     float* C;           // [M, N]
     int64_t M, N, K;
     int KB;
@@ -432,51 +429,11 @@ __global__ void __launch_bounds__(MmtCfg<MT>::kThreads, 1)
                 live[h] = i < nunits && r < p.M && b < nbr;
                 v0[h] = v1[h] = 0u;
                 d[h] = 0.0f;
-                if (live[h] && p.X == nullptr) {
+                if (live[h]) {
                     const int8_t* src = p.A + r * p.K + static_cast<int64_t>(b0 + b) * 32 + 4 * qq;
                     v0[h] = *reinterpret_cast<const uint32_t*>(src);
                     v1[h] = *reinterpret_cast<const uint32_t*>(src + 16);
                     d[h] = p.AS[r * static_cast<int64_t>(p.KB) + b0 + b];
-                }
-            }
-            if (p.X != nullptr) {
-                // the fused step: the row quantizer's arithmetic (bytes and scales
-                // bit-identical to pq_quantize_q8_0; the block's maximum over
-                // its four threads); the first cluster also stores the
-                // quantized rows.  Every load of the batch is issued first.
-                float4 x0[kBatch], x1[kBatch];
-#pragma unroll
-                for (int h = 0; h < kBatch; ++h) {
-                    const int i = base + h * NCT + ctid;
-                    const int qq = i & 3, rb = i >> 2;
-                    const int r = rb / p.nbc, b = rb - r * p.nbc;
-                    x0[h] = x1[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (live[h]) {
-                        const float* src = p.X + r * p.K + static_cast<int64_t>(b0 + b) * 32 + 4 * qq;
-                        x0[h] = ld_stream_f4(src);
-                        x1[h] = ld_stream_f4(src + 16);
-                    }
-                }
-#pragma unroll
-                for (int h = 0; h < kBatch; ++h) {
-                    const int i = base + h * NCT + ctid;
-                    const int qq = i & 3, rb = i >> 2;
-                    const int r = rb / p.nbc, b = rb - r * p.nbc;
-                    float amax = fmaxf(amax4(x0[h]), amax4(x1[h]));
-                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                    if (live[h]) {
-                        d[h] = __fdiv_rn(amax, 127.0f);
-                        const float rc = __frcp_rn(d[h]);
-                        v0[h] = q8_pack4(x0[h], d[h], rc);
-                        v1[h] = q8_pack4(x1[h], d[h], rc);
-                        if (p.Aq != nullptr && ci == 0) {
-                            int8_t* dq = p.Aq + r * p.K + static_cast<int64_t>(b0 + b) * 32 + 4 * qq;
-                            *reinterpret_cast<uint32_t*>(dq) = v0[h];
-                            *reinterpret_cast<uint32_t*>(dq + 16) = v1[h];
-                            if (qq == 0) p.ASq[r * static_cast<int64_t>(p.KB) + b0 + b] = d[h];
-                        }
-                    }
                 }
             }
 #pragma unroll
@@ -903,7 +860,7 @@ cudaError_t launch_mt(const CUtensorMap* maps, MmtParams p, cudaStream_t stream)
 
 }  // namespace
 
-cudaError_t launch_qdot_mmt(const QdotArgs& a, const float* X, int8_t* Aq, float* ASq, cudaStream_t stream) {
+cudaError_t launch_qdot_mmt(const QdotArgs& a, cudaStream_t stream) {
     if (g_small_kernel != 1 || a.S != nullptr) return cudaErrorNotSupported;
     // (tiny planes, K < 128 or N < 32, are left to the register-fed kernel)
     if (a.M < 1 || a.M > 64 || a.N < kBoxRows || a.K < 128 || a.K % 32 != 0) return cudaErrorNotSupported;
@@ -913,10 +870,7 @@ cudaError_t launch_qdot_mmt(const QdotArgs& a, const float* X, int8_t* Aq, float
     if ((reinterpret_cast<uintptr_t>(a.W) & 15u) != 0 || (reinterpret_cast<uintptr_t>(a.WS) & 15u) != 0)
         return cudaErrorNotSupported;
     if (a.ws_layout == 0 ? (KB % 4 != 0) : (a.N % 4 != 0)) return cudaErrorNotSupported;
-    if (X == nullptr && (reinterpret_cast<uintptr_t>(a.A) & 15u) != 0) return cudaErrorNotSupported;
-    if (X != nullptr && ((reinterpret_cast<uintptr_t>(X) & 15u) != 0 ||
-                         (Aq != nullptr && (reinterpret_cast<uintptr_t>(Aq) & 15u) != 0)))
-        return cudaErrorNotSupported;
+    if ((reinterpret_cast<uintptr_t>(a.A) & 3u) != 0) return cudaErrorNotSupported;
 
     // weights and scales in boxes of a whole pass (128 rows) and of 32 rows
     CUtensorMap maps[4];
@@ -936,9 +890,6 @@ cudaError_t launch_qdot_mmt(const QdotArgs& a, const float* X, int8_t* Aq, float
     MmtParams p{};
     p.A = a.A;
     p.AS = a.AS;
-    p.X = X;
-    p.Aq = Aq;
-    p.ASq = ASq;
     p.C = a.C;
     p.M = a.M;
     p.N = a.N;
@@ -968,5 +919,6 @@ void set_mmt_test_hooks(int inject_skip_stage, unsigned long long timeout_cycles
 }
 
 void set_small_kernel(int which) { g_small_kernel = which; }
+int small_kernel() { return g_small_kernel; }
 
 }  // namespace pq

@@ -83,8 +83,10 @@ enum {
     PQ_PATH_AUTO = 0,  /* by M: dp4a up to M = 8, the warp-level MMA for 9..16, tcgen05 above */
     PQ_PATH_SIMT = 1,  /* dp4a (CUDA-core) streaming kernel, any M */
     PQ_PATH_TC = 2,    /* tcgen05 tensor-core kernel (f16 operands, exact integer block sums) */
-    PQ_PATH_MMA = 3    /* warp-level tensor-core kernel (mma.sync m16n8k16, f16 operands, exact
-                          integer block sums), M <= 64 */
+    PQ_PATH_MMA = 3    /* warp-level tensor-core path (mma.sync m16n8k16, f16 operands, exact
+                          integer block sums), M <= 64: the kernel fed by TMA through a
+                          shared-memory ring, or the one whose warps load their own weight
+                          bytes (block-sum mode; shapes the first declines) */
 };
 
 /* Layout of the weight-scale plane WS. */
@@ -149,10 +151,11 @@ int pq_qdot_q8_0_ex(const int8_t* A, const float* AS, const int8_t* W, const flo
  * row (M == 1) this is one kernel, in which every CTA quantizes x into its
  * shared memory while L2 prefetches its weight rows, then streams them (at
  * most one CTA per SM; its warps take further columns when N needs more).
- * For 9 to 16 rows it is one kernel too: the warp-level MMA kernel of qdot_t,
- * each of whose CTAs quantizes the rows of its K range itself.  Otherwise it
- * is the quantizer followed by qdot_t, launched so that the second overlaps
- * the first.  A [M, K] int8 and AS [M, K/32] f32
+ * Otherwise it is the quantizer followed by qdot_t, launched so that the
+ * second overlaps the first (for 9 to 16 rows this is faster than a one-kernel
+ * step whose every CTA quantizes its K range of the rows again; that one-kernel
+ * step remains with the register-fed warp-level MMA kernel selected by
+ * pq_debug_set_small_kernel(0)).  A [M, K] int8 and AS [M, K/32] f32
  * optionally receive the quantized rows (both null, or both non-null).  When
  * they are null and the two-kernel route is taken, the rows go to a
  * workspace of this (device, stream) pair, allocated on the first such call
@@ -198,8 +201,8 @@ int pq_quantize_qdot_q8_0_host(const float* x_host, const int8_t* W, const float
  * automatic path), but the quantized rows and their scales are kept in a
  * fixed array of PQ_NOALLOC_SCRATCH_BYTES (1 MiB) that is part of the library
  * and that every GPU which loads the library holds until the process exits.
- * Where pq_quantize_qdot_q8_0 runs one kernel (one row; 9 to 16 rows) this
- * call runs the same kernel and leaves the array alone.
+ * Where pq_quantize_qdot_q8_0 runs one kernel (one row) this call runs the
+ * same kernel and leaves the array alone.
  * The caller still passes x, W, WS and C (same layouts and alignment as
  * pq_quantize_qdot_q8_0); nothing else is allocated, by this call or by the
  * kernels it starts.

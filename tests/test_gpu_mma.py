@@ -132,8 +132,10 @@ def test_qdot_mma_workload_full(pq, name):
 
 @pytest.mark.parametrize("M,N,K", [(9, 300, 1024), (12, 1000, 4096), (16, 129, 96), (14, 700, 14336)])
 def test_fused_step_equals_quantizer_then_mma(pq, small_kernel, M, N, K):
-    """pq_quantize_qdot_q8_0 at 9..16 rows quantizes inside the MMA kernel: its rows,
-    scales and C are bit-identical to the quantizer followed by this path's qdot_t."""
+    """pq_quantize_qdot_q8_0 at 9..16 rows: with the register-fed kernel one kernel
+    that quantizes x itself, with the TMA-fed kernel the quantizer and then qdot_t;
+    either way its rows, scales and C are bit-identical to the quantizer followed by
+    this path's qdot_t."""
     rng = np.random.default_rng(M * 17 + N + K)
     x = (rng.standard_normal((M, K)) * np.exp(rng.uniform(-4, 4, size=(M, 1)))).astype(np.float32)
     x[1, :64] = 0.0  # two all-zero blocks: d = 0, q = 0

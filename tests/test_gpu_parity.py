@@ -438,7 +438,7 @@ def test_qdot_prompt_full_rows_and_columns(pq):
 
 FUSED_SHAPES = [(1, 64, 256), (1, 300, 1056), (2, 17, 128), (3, 129, 512), (4, 64, 4096), (7, 33, 96),
                 (8, 257, 256), (1, 40, 14336), (1, 4000, 64), (1, 9000, 128), (1, 96, 49152),
-                # 9..16 rows: the warp-level MMA kernel quantizes the rows itself (one split,
+                # 9..16 rows: the quantizer and the warp-level MMA path (one split,
                 # several splits, a short last split, ragged N, long K)
                 (9, 130, 512), (16, 300, 4096), (10, 5, 32), (15, 129, 96), (12, 333, 2048),
                 (13, 1000, 4096), (16, 2000, 14336), (11, 64, 1056),
