@@ -24,15 +24,17 @@
 //   half has been read).  C is written once, with no zeroing pass and no
 //   atomics, and no fence is on the path (a cluster-scope fence before a
 //   remote arrival was measured at 3-4 thousand cycles a pass).
-//   Stage: 128 weight rows x 128 bytes (four Q8_0 blocks) in one TMA box
-//   (128-byte swizzle) and their f32 weight scales in another, on one
-//   mbarrier.  The TMA unit keeps few operations in flight per SM, so the
-//   boxes are large: with four 32-row boxes and four scale boxes per stage the
-//   stream reached about a third of HBM bandwidth.  A pass of fewer than 128
-//   rows (the end of a cluster's range) takes 32-row boxes instead, as few as
-//   cover its rows.
-//   Consumer warp (box j, quarter kq): rows 32j .. 32j + 31 of the pass (four
-//   n-tiles of 8) and 4 / KQ blocks of each stage, all m-tiles of 16 rows.
+//   Stage: 128 weight rows x 256 bytes (eight Q8_0 blocks) in two TMA boxes of
+//   128 rows x 128 bytes (the 128-byte swizzle span) and their f32 weight
+//   scales in a third, on one mbarrier.  The TMA unit keeps few operations in
+//   flight per SM, so the boxes are large: with four 32-row boxes and four
+//   scale boxes per 16 KB stage the stream reached about a third of HBM
+//   bandwidth.  A pass of fewer than 128 rows (the end of a cluster's range)
+//   takes 32-row boxes instead, as few as cover its rows.  Eight blocks a
+//   stage give each consumer warp several independent blocks between two
+//   waits (a stage's time was measured to be one warp's dependency chain).
+//   Consumer warp (box j, part kq): rows 32j .. 32j + 31 of the pass (four
+//   n-tiles of 8) and 8 / KQ blocks of each stage, its m-tiles of 16 rows.
 //   B fragments come from the stage by ldmatrix; A fragments and the
 //   activation scales from the staged tile.
 //
@@ -76,10 +78,12 @@ constexpr int kBoxRows = 32;                          // weight rows per TMA box
 constexpr int kBoxes = 4;                             // boxes per stage
 constexpr int kPassRows = kBoxRows * kBoxes;          // 128 weight rows per pass
 constexpr int kPassTiles = kPassRows / 8;             // 8-row tiles per pass
-constexpr int kStageBlocks = 4;                       // Q8_0 blocks per stage (128 bytes of a row)
-constexpr int kW8Box = kBoxRows * 128;                // 4 KB
-constexpr int kW8 = kBoxes * kW8Box;                  // 16 KB of weight bytes per stage
-constexpr int kWSBox = kBoxRows * kStageBlocks * 4;   // 512 B of weight scales per box
+constexpr int kHalves = 2;                            // 128-byte column groups per stage (128B swizzle span)
+constexpr int kStageBlocks = 4 * kHalves;             // Q8_0 blocks per stage (256 bytes of a row)
+constexpr int kW8Box = kBoxRows * 128;                // 4 KB: 32 rows of one column group
+constexpr int kW8Half = kBoxes * kW8Box;              // 16 KB: the pass's rows in one column group
+constexpr int kW8 = kHalves * kW8Half;                // 32 KB of weight bytes per stage
+constexpr int kWSBox = kBoxRows * kStageBlocks * 4;   // 1 KB of weight scales per 32 rows
 constexpr int kWS = kBoxes * kWSBox;
 constexpr int kMaxStages = 8;
 constexpr int kMaxCluster = 8;
@@ -99,7 +103,7 @@ struct MmtCfg {
     // one m-tile: 2 K parts (measured at M = 16, K = 4096, N = 11008: 21.5 us
     // against 23.6 with 4 and 27 with 1; fewer parts also shrink the partials'
     // buffer, leaving room for a deeper ring)
-    static constexpr int KQ = MT <= 2 ? 2 : 1;  // consumer warps per box and m-group
+    static constexpr int KQ = MT <= 2 ? 2 : 1;  // consumer warps per box and m-group (4 or 8 blocks each)
     static constexpr int MG = MT == 4 ? 2 : 1;        // m-groups
     static constexpr int MTW = MT / MG;               // m-tiles per consumer warp
     static constexpr int BPW = kStageBlocks / KQ;     // blocks per consumer warp and stage
@@ -370,8 +374,10 @@ __global__ void __launch_bounds__(MmtCfg<MT>::kThreads, 1)
             for (int it = 0; it < min(S, total); ++it) {
                 int x, y, nbox;
                 coords(it, x, y, nbox);
-                if (nbox == kBoxes) tc::tma_prefetch_2d(&wmap, x * 32, y);
-                else for (int i = 0; i < nbox; ++i) tc::tma_prefetch_2d(&wmap32, x * 32, y + i * kBoxRows);
+                for (int h = 0; h < kHalves; ++h) {
+                    if (nbox == kBoxes) tc::tma_prefetch_2d(&wmap, x * 32 + h * 128, y);
+                    else for (int i = 0; i < nbox; ++i) tc::tma_prefetch_2d(&wmap32, x * 32 + h * 128, y + i * kBoxRows);
+                }
             }
             pdl_wait();
             int it = 0, slot = 0;
@@ -382,17 +388,21 @@ __global__ void __launch_bounds__(MmtCfg<MT>::kThreads, 1)
                 if (it == p.inject_skip) continue;
                 int x, y, nbox;
                 coords(it, x, y, nbox);
-                tc::mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nbox * (kW8Box + kWSBox)));
+                tc::mbar_arrive_expect_tx(&full[slot],
+                                          static_cast<uint32_t>(nbox * (kHalves * kW8Box + kWSBox)));
                 uint8_t* wdst = smem + slot * kW8;
                 uint8_t* sdst = smem + p.off_ws + slot * kWS;
                 if (nbox == kBoxes) {
-                    // a whole pass: one box of 128 rows each
-                    tc::tma_load_2d(wdst, &wmap, &full[slot], x * 32, y);
+                    // a whole pass: boxes of 128 rows
+                    for (int h = 0; h < kHalves; ++h)
+                        tc::tma_load_2d(wdst + h * kW8Half, &wmap, &full[slot], x * 32 + h * 128, y);
                     if (p.ws_layout == 0) tc::tma_load_2d(sdst, &smap, &full[slot], x, y);
                     else tc::tma_load_2d(sdst, &smap, &full[slot], y, x);
                 } else {
                     for (int i = 0; i < nbox; ++i) {
-                        tc::tma_load_2d(wdst + i * kW8Box, &wmap32, &full[slot], x * 32, y + i * kBoxRows);
+                        for (int h = 0; h < kHalves; ++h)
+                            tc::tma_load_2d(wdst + h * kW8Half + i * kW8Box, &wmap32, &full[slot], x * 32 + h * 128,
+                                            y + i * kBoxRows);
                         if (p.ws_layout == 0)
                             tc::tma_load_2d(sdst + i * kWSBox, &smap32, &full[slot], x, y + i * kBoxRows);
                         else tc::tma_load_2d(sdst + i * kWSBox, &smap32, &full[slot], y + i * kBoxRows, x);
@@ -459,11 +469,12 @@ __global__ void __launch_bounds__(MmtCfg<MT>::kThreads, 1)
         uint32_t ldm_off[CF::BPW][2];
 #pragma unroll
         for (int ub = 0; ub < CF::BPW; ++ub) {
-            const int u = kq * CF::BPW + ub;
+            const int u = kq * CF::BPW + ub;  // block of the stage: column group u / 4, block u % 4 in it
             const int mi = lane >> 3, i = lane & 7;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-                ldm_off[ub][h] = (8 * (2 * h + (mi >> 1)) + i) * 128 + (((2 * u + (mi & 1)) ^ i) << 4);
+                ldm_off[ub][h] = (u >> 2) * kW8Half + (8 * (2 * h + (mi >> 1)) + i) * 128 +
+                                 (((2 * (u & 3) + (mi & 1)) ^ i) << 4);
         }
         const uint32_t a_lane = sbase + p.off_a + g * p.a_rs + q * 16;
         const uint32_t asc_lane = sbase + p.off_asc + g * 32;
@@ -820,7 +831,8 @@ cudaError_t launch_mt(const CUtensorMap* maps, MmtParams p, cudaStream_t stream)
         const int64_t nstage = nbc4 / kStageBlocks;
         const int64_t t_lat = 3500 / L.stages;
         const int64_t t_whole = std::max<int64_t>((kW8 + kWS) / 23, t_lat);
-        const int64_t t_tail = std::max<int64_t>((tail * 8 + kBoxRows - 1) / kBoxRows * (kW8Box + kWSBox) / 23, t_lat);
+        const int64_t t_tail =
+            std::max<int64_t>((tail * 8 + kBoxRows - 1) / kBoxRows * (kHalves * kW8Box + kWSBox) / 23, t_lat);
         const int64_t cost = nstage * (whole * t_whole + (tail ? t_tail : 0));
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;

@@ -33,16 +33,20 @@ def _prompt_kernel(lib, which):
     assert lib.pq_debug_set_prompt_kernel(which) == 0
 
 
-@pytest.mark.parametrize("M,kernel,path", [(16, 0, "tc"), (256, 0, "tc"), (256, 1, "tc"), (16, 0, "mma"),
-                                           (48, 0, "mma")],
+# Every CTA must reach the skipped stage.  The warp-level kernel's stages are 8
+# blocks of one CTA's K chunk: K = 8192 gives two or more at any K split for one
+# m-tile; four m-tiles fit shared memory only with eight-way splits of K = 4096
+# (two stages).
+@pytest.mark.parametrize("M,kernel,path,K", [(16, 0, "tc", 2048), (256, 0, "tc", 2048), (256, 1, "tc", 2048),
+                                             (16, 0, "mma", 8192), (48, 0, "mma", 4096)],
                          ids=["narrow_tiles", "prompt_first_kernel", "prompt_second_kernel", "tma_fed_mma",
                               "tma_fed_mma_two_groups"])
-def test_tc_bounded_wait_gives_up_and_recovers(pq, M, kernel, path):
+def test_tc_bounded_wait_gives_up_and_recovers(pq, M, kernel, path, K):
     lib = pq.load()
     _prompt_kernel(lib, kernel)
     path = pq.PATH_TC if path == "tc" else pq.PATH_MMA
     rng = np.random.default_rng(M)
-    N, K = 256, 2048
+    N = 256
     a = workloads.random_int8(rng, (M, K))
     w = workloads.random_int8(rng, (N, K))
     a_s = workloads.random_scales(rng, (M, K // 32))
