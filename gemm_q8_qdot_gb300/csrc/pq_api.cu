@@ -390,6 +390,18 @@ int pq_debug_set_small_kernel(int which) {
     return PQ_OK;
 }
 
+int pq_debug_set_small_split(int ks) {
+    if (ks != 0 && ks != 1 && ks != 2 && ks != 4 && ks != 8) return PQ_ERR_INVALID_ARG;
+    pq::set_small_split(ks);
+    return PQ_OK;
+}
+
+int pq_debug_small_kernel_config(int* out4) {
+    if (!out4) return PQ_ERR_INVALID_ARG;
+    pq::small_kernel_config(out4);
+    return PQ_OK;
+}
+
 int pq_debug_prompt_kernel_regs(void) { return pq::tcw_kernel_regs(); }
 
 int pq_debug_set_host_path(int which) {

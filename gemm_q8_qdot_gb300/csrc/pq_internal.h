@@ -111,6 +111,10 @@ cudaError_t launch_qdot_mma_fused(const FusedArgs& a, cudaStream_t stream);
 cudaError_t launch_qdot_mmt(const QdotArgs& a, cudaStream_t stream);
 void set_small_kernel(int which);
 int small_kernel();
+// Test hooks: restrict the TMA-fed kernel to clusters of ks CTAs (0: its own
+// choice); the last launch's (cluster size, clusters, ring stages, K chunk).
+void set_small_split(int ks);
+void small_kernel_config(int* out4);
 
 // A workspace of at least `bytes` for work enqueued on `stream` of the current
 // device (one per device, stream and kind, so calls on different streams never

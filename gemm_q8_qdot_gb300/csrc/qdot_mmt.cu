@@ -746,6 +746,8 @@ Layout layout_for(int nbc) {
 int g_skip_stage = -1;
 unsigned long long g_timeout = 4000000000ull;  // ~2 s at 2 GHz
 int g_small_kernel = 1;                        // 1: this kernel where it applies; 0: the register-fed one
+int g_force_ks = 0;                            // test hook: only this cluster size (0: the cost model's choice)
+int g_last_cfg[4] = {0, 0, 0, 0};              // the last launch's cluster size, clusters, ring stages, K chunk
 
 struct Choice {
     int ks = 0, clusters = 0, nbc = 0;
@@ -789,10 +791,12 @@ cudaError_t launch_mt(const CUtensorMap* maps, MmtParams p, cudaStream_t stream)
     Choice best;
     int64_t best_cost = -1;
     for (int ks : {8, 4, 2, 1}) {
+        if (g_force_ks != 0 && ks != g_force_ks) continue;
         const int nbc = (p.KB + ks - 1) / ks;
         const int nbc4 = (nbc + kStageBlocks - 1) / kStageBlocks * kStageBlocks;
         const int kse = (p.KB + nbc4 - 1) / nbc4;
         if ((kse & (kse - 1)) != 0) continue;  // the partials' owner is lane % ks: a power of two
+        if (g_force_ks != 0 && kse != g_force_ks) continue;
         const Layout L = layout_for<MT>(nbc4);
         if (L.stages < 2) continue;
         static std::mutex mu;
@@ -844,6 +848,10 @@ cudaError_t launch_mt(const CUtensorMap* maps, MmtParams p, cudaStream_t stream)
     }
     if (best_cost < 0) return cudaErrorNotSupported;
 
+    g_last_cfg[0] = best.ks;
+    g_last_cfg[1] = best.clusters;
+    g_last_cfg[2] = best.L.stages;
+    g_last_cfg[3] = best.nbc;
     p.nbc = best.nbc;
     p.clusters = best.clusters;
     p.stages = best.L.stages;
@@ -931,6 +939,10 @@ void set_mmt_test_hooks(int inject_skip_stage, unsigned long long timeout_cycles
 }
 
 void set_small_kernel(int which) { g_small_kernel = which; }
+void set_small_split(int ks) { g_force_ks = ks; }
+void small_kernel_config(int* out) {
+    for (int i = 0; i < 4; ++i) out[i] = g_last_cfg[i];
+}
 int small_kernel() { return g_small_kernel; }
 
 }  // namespace pq

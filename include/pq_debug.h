@@ -55,6 +55,20 @@ int pq_debug_set_prompt_kernel(int which);
 int pq_debug_set_small_kernel(int which);
 
 /*
+ * The TMA-fed kernel of few rows splits K over a thread-block cluster whose
+ * size (1, 2, 4 or 8 CTAs) it chooses by a cost model.  pq_debug_set_small_split
+ * restricts it to clusters of `ks` CTAs (0 restores its own choice); a shape
+ * whose K chunk then does not fit shared memory, or whose chunking gives
+ * another cluster size, goes to the register-fed kernel.
+ * pq_debug_small_kernel_config writes the last launch of that kernel's cluster
+ * size, number of clusters, ring stages and K chunk in blocks to out4[0..3]
+ * (zeros before the first launch).  Host state, process-wide, not
+ * thread-safe; PQ_ERR_INVALID_ARG for another ks or a null out4.
+ */
+int pq_debug_set_small_split(int ks);
+int pq_debug_small_kernel_config(int* out4);
+
+/*
  * Registers a thread of the build of the second prompt kernel (see
  * pq_debug_set_prompt_kernel) that the current device admits with its 704
  * threads (several builds with different register limits exist; the largest

@@ -54,6 +54,18 @@ def test_debug_hooks_reject_bad_values(lib):
     assert lib.pq_debug_set_prompt_kernel(2) == binding.PQ_ERR_INVALID_ARG
     assert lib.pq_debug_set_prompt_kernel(-1) == binding.PQ_ERR_INVALID_ARG
     assert lib.pq_debug_set_tc_fault(-2, 0) == binding.PQ_ERR_INVALID_ARG
+    lib.pq_debug_set_small_kernel.argtypes = [ctypes.c_int]
+    lib.pq_debug_set_small_split.argtypes = [ctypes.c_int]
+    lib.pq_debug_small_kernel_config.argtypes = [ctypes.c_void_p]
+    for bad in (2, -1):
+        assert lib.pq_debug_set_small_kernel(bad) == binding.PQ_ERR_INVALID_ARG
+    for bad in (3, 16, -1):
+        assert lib.pq_debug_set_small_split(bad) == binding.PQ_ERR_INVALID_ARG
+    assert lib.pq_debug_small_kernel_config(None) == binding.PQ_ERR_INVALID_ARG
+    # host state only: valid values are accepted without a device
+    assert lib.pq_debug_set_small_split(0) == binding.PQ_OK
+    cfg = (ctypes.c_int * 4)()
+    assert lib.pq_debug_small_kernel_config(cfg) == binding.PQ_OK
 
 
 def test_version_and_strerror(lib):

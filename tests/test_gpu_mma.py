@@ -226,3 +226,44 @@ def test_tma_kernel_chunks_and_passes(pq, M, N, K, layout):
     got = host(C)[:, cols].astype(np.float64)
     bad = np.abs(got - out) > bound
     assert not bad.any(), f"{int(bad.sum())} elements out of bound, M={M} N={N} K={K}"
+
+
+def _split_hooks(pq):
+    lib = pq.load()
+    lib.pq_debug_set_small_split.argtypes = [ctypes.c_int]
+    lib.pq_debug_set_small_split.restype = ctypes.c_int
+    lib.pq_debug_small_kernel_config.argtypes = [ctypes.c_void_p]
+    lib.pq_debug_small_kernel_config.restype = ctypes.c_int
+    return lib
+
+
+def test_tma_kernel_every_cluster_size(pq):
+    """The cost model picks the K split by itself, so parity at the shapes above may
+    never see some cluster sizes: force each of 1, 2, 4 and 8 CTAs on shapes whose
+    chunks fit, check the launch took it (the last launch's configuration), and
+    compare with the oracle.  Every size must be exercised by some shape."""
+    lib = _split_hooks(pq)
+    shapes = [(16, 1000, 1024), (5, 333, 4096), (20, 777, 2048), (16, 300, 8192), (48, 200, 1024),
+              (64, 520, 2048), (1, 64, 512)]
+    seen = set()
+    try:
+        for ks in (1, 2, 4, 8):
+            assert lib.pq_debug_set_small_split(ks) == 0
+            for M, N, K in shapes:
+                a, a_s, w, w_s = rand_operands(ks * 7 + M + N + K, M, N, K)
+                cfg = (ctypes.c_int * 4)()
+                assert lib.pq_debug_small_kernel_config(cfg) == 0
+                before = tuple(cfg)
+                for layout in (0, 1):
+                    ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
+                    C = torch.full((M, N), float("nan"), device="cuda:0")
+                    pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(ws), C, ws_layout=layout, path=pq.PATH_MMA)
+                    pq.check_device()
+                    out, bound = oracle.qdot(a, a_s, w, w_s)
+                    assert_within_bound(C, out, bound, f"ks={ks} M={M} N={N} K={K} layout={layout}")
+                assert lib.pq_debug_small_kernel_config(cfg) == 0
+                if tuple(cfg) != before and cfg[0] == ks:
+                    seen.add(ks)
+    finally:
+        lib.pq_debug_set_small_split(0)
+    assert seen == {1, 2, 4, 8}, f"cluster sizes exercised: {sorted(seen)}"
