@@ -135,7 +135,7 @@ using pq::check_qdot_shape;
 
 int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS, float* C,
               int32_t* S, int64_t M, int64_t N, int64_t K, int ws_layout, int path,
-              cudaStream_t stream, int no_alloc = 0) {
+              cudaStream_t stream, int no_alloc = 0, int early_weights = 0) {
     if (path != PQ_PATH_AUTO && path != PQ_PATH_SIMT && path != PQ_PATH_TC && path != PQ_PATH_MMA)
         return PQ_ERR_INVALID_ARG;
     if (ws_layout != PQ_WS_N_KB && ws_layout != PQ_WS_KB_N) return PQ_ERR_INVALID_ARG;
@@ -149,7 +149,7 @@ int qdot_impl(const int8_t* A, const float* AS, const int8_t* W, const float* WS
     if (sums && !aligned(S, 4)) return PQ_ERR_ALIGN;
     if (!sums && (!aligned(AS, 4) || !aligned(WS, 4) || !aligned(C, 4))) return PQ_ERR_ALIGN;
 
-    pq::QdotArgs a{A, AS, W, WS, C, S, M, N, K, ws_layout, no_alloc};
+    pq::QdotArgs a{A, AS, W, WS, C, S, M, N, K, ws_layout, no_alloc, early_weights};
     if (path == PQ_PATH_SIMT) return map_cuda(pq::launch_qdot_simt(a, stream));
     if (path == PQ_PATH_TC) return map_cuda(pq::launch_qdot_tc(a, stream));
     if (path == PQ_PATH_MMA) return map_cuda(pq::launch_qdot_mma(a, stream));
@@ -231,9 +231,14 @@ int pq_quantize_qdot_q8_0(const float* x, int8_t* A, float* AS, const int8_t* W,
         A = static_cast<int8_t*>(ws);
         AS = reinterpret_cast<float*>(static_cast<char*>(ws) + qbytes);
     }
-    st = pq_quantize_q8_0(x, A, AS, M, K, stream);
-    if (st != PQ_OK) return st;
-    return qdot_impl(A, AS, W, WS, C, nullptr, M, N, K, ws_layout, PQ_PATH_AUTO, stream);
+    // 9..16 rows on the TMA-fed kernel: the quantizer lets qdot_t in only
+    // after its own wait, and qdot_t then streams its first weight stages
+    // while the quantizer runs
+    const bool early = M > 8 && M <= 16 && pq::small_kernel() == 1;
+    if (!aligned(A, 16) || !aligned(AS, 4)) return PQ_ERR_ALIGN;
+    e = pq::launch_quantize(x, A, AS, M, K, stream, early);
+    if (e != cudaSuccess) return map_cuda(e);
+    return qdot_impl(A, AS, W, WS, C, nullptr, M, N, K, ws_layout, PQ_PATH_AUTO, stream, 0, early ? 1 : 0);
 }
 
 int pq_quantize_qdot_q8_0_host(const float* x_host, const int8_t* W, const float* WS, float* C_host, int64_t M,

@@ -16,6 +16,11 @@ struct QdotArgs {
     int64_t M, N, K;
     int ws_layout;   // 0: WS [N, K/32]; 1: WS [K/32, N]
     int no_alloc = 0;  // 1: the call must not allocate device memory (no workspace)
+    // 1: the kernel just before this launch on the stream is this library's
+    // quantizer launched with late_trigger, so every kernel before that one
+    // has completed when this one starts and W, WS may be read before
+    // griddepcontrol.wait (the TMA-fed kernel then streams its first stages)
+    int early_weights = 0;
 };
 
 struct FusedArgs {
@@ -49,8 +54,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// late_trigger: the next kernel on the stream is let in only after this one
+// has waited for its own predecessor (see QdotArgs::early_weights).
 cudaError_t launch_quantize(const float* x, int8_t* q, float* s, int64_t rows, int64_t K,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool late_trigger = false);
 
 // dp4a streaming kernel: any M; returns cudaErrorInvalidConfiguration when the
 // grid would exceed the device limits.

@@ -127,6 +127,7 @@ struct MmtParams {
     int ws_layout;      // 0: WS [N, K/32]; 1: WS [K/32, N]
     int vec2;           // C 8-byte aligned and N even: float2 stores
     int inject_skip;    // test hook: the producer never fills this stage (-1: off)
+    int early_weights;  // W / WS may be read before griddepcontrol.wait (QdotArgs::early_weights)
     unsigned long long timeout_cycles;
     uint32_t off_ws, off_a, off_asc, off_red, off_bar;  // shared-memory regions
     uint32_t a_rs;      // bytes per row of the staged activation tile (nbc * 64 + 64)
@@ -369,20 +370,27 @@ __global__ void __launch_bounds__(MmtCfg<MT>::kThreads, 1)
                 nbox = min(kBoxes, ((t1 - tile0) * 8 + kBoxRows - 1) / kBoxRows);
                 x = b0 + s * kStageBlocks;
             };
-            // the weights do not depend on the preceding kernel: ask L2 for the
-            // first stages before waiting on it (a hint; the loads come after)
-            for (int it = 0; it < min(S, total); ++it) {
-                int x, y, nbox;
-                coords(it, x, y, nbox);
-                for (int h = 0; h < kHalves; ++h) {
-                    if (nbox == kBoxes) tc::tma_prefetch_2d(&wmap, x * 32 + h * 128, y);
-                    else for (int i = 0; i < nbox; ++i) tc::tma_prefetch_2d(&wmap32, x * 32 + h * 128, y + i * kBoxRows);
+            // Before waiting on the preceding kernel: with early_weights (the
+            // preceding kernel is the library's quantizer, which let this one in
+            // only once every kernel before it had completed) the first stages
+            // are loaded; otherwise L2 is asked for them (a hint that cannot
+            // return stale data; the loads come after the wait).
+            const int first = min(S, total);
+            if (!p.early_weights) {
+                for (int it = 0; it < first; ++it) {
+                    int x, y, nbox;
+                    coords(it, x, y, nbox);
+                    for (int h = 0; h < kHalves; ++h) {
+                        if (nbox == kBoxes) tc::tma_prefetch_2d(&wmap, x * 32 + h * 128, y);
+                        else for (int i = 0; i < nbox; ++i) tc::tma_prefetch_2d(&wmap32, x * 32 + h * 128, y + i * kBoxRows);
+                    }
                 }
+                pdl_wait();
             }
-            pdl_wait();
             int it = 0, slot = 0;
             uint32_t phase = 0;  // (it / S) & 1
             for (; it < total; ++it, slot = slot + 1 == S ? 0 : slot + 1, phase ^= slot == 0 ? 1u : 0u) {
+                if (p.early_weights && it == first) pdl_wait();
                 if (it >= S && (abort_get(abort_flag) || !bounded_wait<false>(&empty[slot], phase ^ 1, abort_flag, limit)))
                     break;
                 if (it == p.inject_skip) continue;
@@ -409,6 +417,7 @@ __global__ void __launch_bounds__(MmtCfg<MT>::kThreads, 1)
                     }
                 }
             }
+            if (p.early_weights && it <= first) pdl_wait();  // (no stage past the first ring, or an early end)
             // loads still in flight land before the CTA may exit
             for (int j = max(0, it - S); j < it; ++j)
                 if (j != p.inject_skip) drain_wait(&full[j % S], (j / S) & 1, limit);
@@ -919,6 +928,7 @@ cudaError_t launch_qdot_mmt(const QdotArgs& a, cudaStream_t stream) {
     p.ws_layout = a.ws_layout;
     p.vec2 = (reinterpret_cast<uintptr_t>(a.C) & 7u) == 0 && a.N % 2 == 0;
     p.inject_skip = g_skip_stage;
+    p.early_weights = a.early_weights;
     p.timeout_cycles = g_timeout;
     const int MT = static_cast<int>((a.M + 15) / 16);
     if (MT == 1) return launch_mt<1>(maps, p, stream);

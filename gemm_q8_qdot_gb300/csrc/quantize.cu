@@ -23,14 +23,19 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBlocksPerCta = kThreads / 4;
 
+// LATE: let the next kernel in only after this one has waited for its own
+// predecessor, so that once the next kernel runs, every kernel before this one
+// has completed (the one-call step's qdot_t then reads the weights before its
+// own wait).  Otherwise let it in at once, so that it can prefetch its weights
+// into L2 while this one runs.
+template <bool LATE>
 __global__ void __launch_bounds__(kThreads)
 quantize_q8_0_kernel(const float* __restrict__ x, int8_t* __restrict__ q, float* __restrict__ s,
                      int64_t nblocks) {
-    // Let the next kernel (typically qdot_t) be scheduled now, so that it can
-    // stream its weights while this one runs; then wait for whatever wrote x
-    // (and read q, s) before us.
-    pdl_trigger();
+    // wait for whatever wrote x (and read q, s) before us
+    if constexpr (!LATE) pdl_trigger();
     pdl_wait();
+    if constexpr (LATE) pdl_trigger();
     const int64_t g = static_cast<int64_t>(blockIdx.x) * kBlocksPerCta + (threadIdx.x >> 2);
     const int sub = threadIdx.x & 3;
     const bool live = g < nblocks;
@@ -50,11 +55,14 @@ quantize_q8_0_kernel(const float* __restrict__ x, int8_t* __restrict__ q, float*
 }  // namespace
 
 cudaError_t launch_quantize(const float* x, int8_t* q, float* s, int64_t rows, int64_t K,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool late_trigger) {
     const int64_t nblocks = rows * (K / 32);
     const int64_t grid = (nblocks + kBlocksPerCta - 1) / kBlocksPerCta;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    return launch_pdl(quantize_q8_0_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, stream,
+    if (late_trigger)
+        return launch_pdl(quantize_q8_0_kernel<true>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, stream,
+                          x, q, s, nblocks);
+    return launch_pdl(quantize_q8_0_kernel<false>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, stream,
                       x, q, s, nblocks);
 }
 

@@ -267,3 +267,31 @@ def test_tma_kernel_every_cluster_size(pq):
     finally:
         lib.pq_debug_set_small_split(0)
     assert seen == {1, 2, 4, 8}, f"cluster sizes exercised: {sorted(seen)}"
+
+
+@pytest.mark.parametrize("M", [12, 16])
+def test_step_sees_weights_written_just_before(pq, M):
+    """The one-call step at 9..16 rows lets qdot_t stream its first weight stages
+    before its own wait on the quantizer (which lets it in only once every kernel
+    before the quantizer has completed).  Weights rewritten by a kernel just before
+    each step, on the same stream and with no synchronization, must be the ones used."""
+    N, K = 2000, 4096
+    rng = np.random.default_rng(M)
+    x = (rng.standard_normal((M, K)) * 2.0).astype(np.float32)
+    X = dev(x)
+    W = torch.empty((N, K), dtype=torch.int8, device="cuda:0")
+    WS = torch.empty((N, K // 32), dtype=torch.float32, device="cuda:0")
+    sets = [rand_operands(100 * M + i, 1, N, K)[2:] for i in range(3)]
+    srcs = [(dev(w), dev(ws)) for w, ws in sets]
+    qa, sa = oracle.quantize_q8_0(x)
+    torch.cuda.synchronize()
+    outs = []
+    for w_d, ws_d in srcs:
+        W.copy_(w_d)        # a kernel on the current stream, right before the step
+        WS.copy_(ws_d)
+        outs.append(pq.quantize_qdot_q8_0(X, W, WS))
+    torch.cuda.synchronize()
+    pq.check_device()
+    for (w, ws), C in zip(sets, outs):
+        out, bound = oracle.qdot(qa, sa, w, ws)
+        assert_within_bound(C, out, bound, f"weights rewritten before the step, M={M}")
