@@ -269,12 +269,13 @@ def test_tma_kernel_every_cluster_size(pq):
     assert seen == {1, 2, 4, 8}, f"cluster sizes exercised: {sorted(seen)}"
 
 
-@pytest.mark.parametrize("M", [12, 16])
+@pytest.mark.parametrize("M", [3, 8, 12, 16])
 def test_step_sees_weights_written_just_before(pq, M):
     """The one-call step at 9..16 rows lets qdot_t stream its first weight stages
     before its own wait on the quantizer (which lets it in only once every kernel
-    before the quantizer has completed).  Weights rewritten by a kernel just before
-    each step, on the same stream and with no synchronization, must be the ones used."""
+    before the quantizer has completed); at 2..8 rows the dp4a kernel only prefetches
+    into L2 before its wait.  Weights rewritten by a kernel just before each step, on
+    the same stream and with no synchronization, must be the ones used."""
     N, K = 2000, 4096
     rng = np.random.default_rng(M)
     x = (rng.standard_normal((M, K)) * 2.0).astype(np.float32)
