@@ -356,11 +356,12 @@ int pq_q50_blocksums(const int8_t* A, const uint8_t* W5, int32_t* S, int64_t M, 
 
 int pq_check_device(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return PQ_ERR_CUDA;
-    unsigned status = 0, status_w = 0, status_m = 0;
+    unsigned status = 0, status_w = 0, status_m = 0, status_s = 0;
     if (pq::read_and_clear_status(&status) != cudaSuccess) return PQ_ERR_CUDA;
     if (pq::read_and_clear_status_w(&status_w) != cudaSuccess) return PQ_ERR_CUDA;
     if (pq::read_and_clear_status_mmt(&status_m) != cudaSuccess) return PQ_ERR_CUDA;
-    return (status | status_w | status_m) ? PQ_ERR_TIMEOUT : PQ_OK;
+    if (pq::read_and_clear_status_simt(&status_s) != cudaSuccess) return PQ_ERR_CUDA;
+    return (status | status_w | status_m | status_s) ? PQ_ERR_TIMEOUT : PQ_OK;
 }
 
 const char* pq_strerror(int code) {

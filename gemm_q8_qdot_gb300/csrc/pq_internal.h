@@ -145,6 +145,7 @@ int qdot_noalloc(const int8_t* A, const float* AS, const int8_t* W, const float*
 cudaError_t read_and_clear_status(unsigned* status);
 cudaError_t read_and_clear_status_w(unsigned* status);
 cudaError_t read_and_clear_status_mmt(unsigned* status);
+cudaError_t read_and_clear_status_simt(unsigned* status);
 
 // Test hooks of the tensor-core kernel: skip one producer stage so that the
 // consumers' bounded waits give up (-1: off), and the wait limit in SM clock

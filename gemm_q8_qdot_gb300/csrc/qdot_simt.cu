@@ -38,6 +38,17 @@
 #include "pq_device.cuh"
 
 namespace pq {
+
+// Nonzero after the fused step's bounded wait for its copy of x gave up.
+__device__ unsigned g_pq_status_simt;
+
+cudaError_t read_and_clear_status_simt(unsigned* status) {
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_pq_status_simt, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_pq_status_simt, &zero, sizeof(unsigned));
+}
+
 namespace {
 
 constexpr int kWarps = 8;
@@ -211,7 +222,15 @@ cudaError_t launch_by_m(const QdotArgs& a, bool v8, cudaStream_t stream) {
 // MULTI: N exceeds the grid (one CTA per SM), so each warp takes further
 // columns; otherwise one column per warp (the loop costs the single-column
 // grids ~3 %, measured).
-template <int U, bool V8, int WSL, int NW, bool MULTI>
+// XB: x arrives by one bulk copy into shared memory (the async proxy) and the
+// first weight round is issued at once, before x is there; otherwise x is
+// loaded by the threads and the first weight round follows its quantization
+// (issuing it earlier delayed x's loads behind the weights').  Measured on
+// GB300 (graphs of back-to-back steps): XB takes K = 4096, N = 14336 from
+// 11.90 to 11.24 us and K = 14336, N = 4096 from 13.27 to 12.32 us, but
+// K = N = 4096 (one column per warp) from 4.75 to 4.83 us, so it serves long
+// rows and several columns per warp.
+template <int U, bool V8, int WSL, int NW, bool MULTI, bool XB>
 __global__ void __launch_bounds__(NW * 32)
 qdot_fused_kernel(FusedArgs p) {
     extern __shared__ __align__(16) uint8_t fsm[];
@@ -220,6 +239,17 @@ qdot_fused_kernel(FusedArgs p) {
     const int64_t N = p.N, K = p.K, KB = K >> 5;
     int8_t* a_s = reinterpret_cast<int8_t*>(fsm);           // [K]
     float* as_s = reinterpret_cast<float*>(fsm + K);        // [KB]
+    // XB: x as f32 [K] after them, 16-byte aligned
+    float* x_s = reinterpret_cast<float*>(fsm + ((K + KB * 4 + 15) & ~int64_t(15)));
+    __shared__ __align__(8) uint64_t xbar;
+    const uint32_t xbar_a = static_cast<uint32_t>(__cvta_generic_to_shared(&xbar));
+    if constexpr (XB) {
+        if (threadIdx.x == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(xbar_a) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+    }
     // the warp's columns: j0, j0 + jstride, ... (one each unless N exceeds the grid)
     const int64_t j0 = static_cast<int64_t>(blockIdx.x) * NW + warp;
     const int64_t jstride = static_cast<int64_t>(gridDim.x) * NW;
@@ -238,6 +268,15 @@ qdot_fused_kernel(FusedArgs p) {
         }
     }
     pdl_wait();
+    if constexpr (XB) {
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(K * 4);
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(xbar_a), "r"(bytes) : "memory");
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                         ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(x_s))), "l"(p.x), "r"(bytes), "r"(xbar_a)
+                         : "memory");
+        }
+    }
 
     // weights of round `bb`: U blocks per lane, read once per launch
     const uint64_t wpol = l2_weight_policy(true);
@@ -264,18 +303,38 @@ qdot_fused_kernel(FusedArgs p) {
     const int64_t nthr = KB * 8;    // one float4 of x per thread and round
     constexpr int64_t kRound = NW * 32;
     const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 xv = threadIdx.x < nthr ? ld_stream_f4(p.x + threadIdx.x * 4) : zero4;
+    float4 xv;
+    if constexpr (XB) {
+        load_round(0);
+        // bounded wait for the copy of x (about a second at 2 GHz; giving up
+        // records the failure in this file's status word, C is then undefined)
+        uint32_t ok = 0;
+        const long long t0 = clock64();
+        for (uint32_t n = 0; !ok; ++n) {
+            asm volatile("{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], 0;\n\t"
+                         "selp.b32 %0, 1, 0, q;\n\t}"
+                         : "=r"(ok) : "r"(xbar_a) : "memory");
+            if (!ok && (n & 15) == 15 && clock64() - t0 > 2000000000LL) {
+                atomicOr(&g_pq_status_simt, 1u);
+                break;
+            }
+        }
+        xv = threadIdx.x < nthr ? reinterpret_cast<const float4*>(x_s)[threadIdx.x] : zero4;
+    } else {
+        xv = threadIdx.x < nthr ? ld_stream_f4(p.x + threadIdx.x * 4) : zero4;
+    }
     for (int64_t base = 0; base < nthr; base += kRound) {  // CTA-uniform
         const int64_t t = base + threadIdx.x;
         const int64_t tn = t + kRound;
-        const float4 xn = tn < nthr ? ld_stream_f4(p.x + tn * 4) : zero4;
+        const float4 xn = tn < nthr ? (XB ? reinterpret_cast<const float4*>(x_s)[tn] : ld_stream_f4(p.x + tn * 4))
+                                    : zero4;
         const float d = q8_scale_of<8>(amax4(xv));  // every lane of the warp takes part
         if (t < nthr) {
             *reinterpret_cast<uint32_t*>(a_s + t * 4) = q8_pack4(xv, d, __frcp_rn(d));
             if ((threadIdx.x & 7) == 0) as_s[t >> 3] = d;
         }
         xv = xn;
-        if (base == 0) load_round(0);
+        if (!XB && base == 0) load_round(0);
     }
     __syncthreads();
     pdl_trigger();
@@ -314,24 +373,33 @@ qdot_fused_kernel(FusedArgs p) {
     }
 }
 
+template <int U, int WSL, int NW, bool MULTI, bool XB>
+auto fused_kernel_for(bool v8) {
+    return v8 ? qdot_fused_kernel<U, true, WSL, NW, MULTI, XB> : qdot_fused_kernel<U, false, WSL, NW, MULTI, XB>;
+}
+
 template <int U, int WSL, int NW>
-cudaError_t launch_fused(const FusedArgs& a, bool v8, int sms, cudaStream_t stream) {
-    const size_t smem = static_cast<size_t>(a.K) + static_cast<size_t>(a.K / 32) * 4;
-    if (smem > 200 * 1024) return cudaErrorNotSupported;
+cudaError_t launch_fused(const FusedArgs& a, bool v8, int sms, bool long_rows, cudaStream_t stream) {
+    const size_t smem0 = static_cast<size_t>(a.K) + static_cast<size_t>(a.K / 32) * 4;
+    if (smem0 > 200 * 1024) return cudaErrorNotSupported;
     // one output column per warp; NW warps per CTA quantize x once for NW columns
     // one CTA per SM at most (its 1024 or 896 threads hold the SM's registers);
     // beyond that each warp takes further columns
     const int64_t grid = std::min<int64_t>((a.N + NW - 1) / NW, sms);
     const bool multi = (a.N + NW - 1) / NW > sms;
-    auto kern = v8 ? (multi ? qdot_fused_kernel<U, true, WSL, NW, true> : qdot_fused_kernel<U, true, WSL, NW, false>)
-                   : (multi ? qdot_fused_kernel<U, false, WSL, NW, true> : qdot_fused_kernel<U, false, WSL, NW, false>);
+    // x by bulk copy for long rows and several columns per warp, where it fits
+    const size_t smem_xb = ((smem0 + 15) & ~size_t(15)) + static_cast<size_t>(a.K) * 4;
+    const bool xb = (multi || long_rows) && smem_xb <= 200 * 1024;
+    const size_t smem = xb ? smem_xb : smem0;
+    auto kern = multi ? (xb ? fused_kernel_for<U, WSL, NW, true, true>(v8) : fused_kernel_for<U, WSL, NW, true, false>(v8))
+                      : (xb ? fused_kernel_for<U, WSL, NW, false, true>(v8) : fused_kernel_for<U, WSL, NW, false, false>(v8));
     // beyond the default 48 KB of dynamic shared memory (K > 43690) the kernel's
     // limit is raised once for the largest size met (it is per function, not per call)
     if (smem > 48 * 1024) {
-        static std::atomic<int> raised[64][4];  // per device (the attribute is set in its context) and kernel
+        static std::atomic<int> raised[64][8];  // per device (the attribute is set in its context) and kernel
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorNotSupported;
-        std::atomic<int>& r = raised[dev][(v8 ? 1 : 0) + (multi ? 2 : 0)];
+        std::atomic<int>& r = raised[dev][(v8 ? 1 : 0) + (multi ? 2 : 0) + (xb ? 4 : 0)];
         if (static_cast<int>(smem) > r.load()) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));
@@ -361,10 +429,10 @@ cudaError_t launch_qdot_fused(const FusedArgs& a, cudaStream_t stream) {
     const bool long_rows = a.K >= kLongRowK;
     const bool v8 = (reinterpret_cast<uintptr_t>(a.W) & 31u) == 0;
     if (long_rows)
-        return a.ws_layout == 0 ? launch_fused<4, 0, kFusedWarpsLongRows>(a, v8, sms, stream)
-                                : launch_fused<4, 1, kFusedWarpsLongRows>(a, v8, sms, stream);
-    return a.ws_layout == 0 ? launch_fused<4, 0, kFusedWarps>(a, v8, sms, stream)
-                            : launch_fused<4, 1, kFusedWarps>(a, v8, sms, stream);
+        return a.ws_layout == 0 ? launch_fused<4, 0, kFusedWarpsLongRows>(a, v8, sms, true, stream)
+                                : launch_fused<4, 1, kFusedWarpsLongRows>(a, v8, sms, true, stream);
+    return a.ws_layout == 0 ? launch_fused<4, 0, kFusedWarps>(a, v8, sms, false, stream)
+                            : launch_fused<4, 1, kFusedWarps>(a, v8, sms, false, stream);
 }
 
 namespace {
