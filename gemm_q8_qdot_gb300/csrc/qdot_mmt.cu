@@ -13,7 +13,7 @@
 // the consumer warps only compute.
 //
 // Work layout.
-//   Cluster: KS CTAs (one per SM) that split K into chunks of whole 4-block
+//   Cluster: KS CTAs (one per SM) that split K into chunks of whole 8-block
 //   stages; the cluster owns a contiguous range of 8-row weight tiles and walks
 //   it in passes of 128 rows.  Each CTA stages the activation rows of its K
 //   chunk once, as f16 in shared memory, and keeps them for every pass.  After
@@ -56,8 +56,9 @@
 // gives up sets this file's device status word and a CTA-wide abort flag;
 // every role then runs out its loops without waiting or working, TMA loads in
 // flight are drained with bounded waits, and every thread of every CTA meets
-// at one last cluster barrier, so no CTA leaves while another may still read
-// its shared memory.  No trap, no unbounded spin.
+// at one last cluster barrier (after waiting, bounded, for the other CTAs'
+// last arrivals on its barriers), so no CTA leaves while another may still
+// write to its shared memory.  No trap, no unbounded spin.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
