@@ -343,10 +343,18 @@ def _capture(prob: Problem, first: int, steps: int, stream, events=None, only_qd
     return g
 
 
+# Cycles of a spin kernel enqueued ahead of a timed graph (~50 us at 2 GHz):
+# it holds the stream until the graph launch has been submitted, so the timed
+# region (start event to end event) holds the graph's K steps and not the
+# host's launch latency, and the GPU does not idle meanwhile.
+HOLD_CYCLES = 100_000
+
+
 def _replay_ms(g, stream) -> float:
     import torch
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        torch.cuda._sleep(HOLD_CYCLES)
         start.record(stream)
         g.replay()
         end.record(stream)
