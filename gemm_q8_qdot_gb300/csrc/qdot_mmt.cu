@@ -62,6 +62,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pq_device.cuh"
@@ -757,7 +758,7 @@ int g_skip_stage = -1;
 unsigned long long g_timeout = 4000000000ull;  // ~2 s at 2 GHz
 int g_small_kernel = 1;                        // 1: this kernel where it applies; 0: the register-fed one
 int g_force_ks = 0;                            // test hook: only this cluster size (0: the cost model's choice)
-int g_last_cfg[4] = {0, 0, 0, 0};              // the last launch's cluster size, clusters, ring stages, K chunk
+std::atomic<int> g_last_cfg[4];                // the last launch's cluster size, clusters, ring stages, K chunk
 
 struct Choice {
     int ks = 0, clusters = 0, nbc = 0;
@@ -796,18 +797,18 @@ cudaError_t launch_mt(const CUtensorMap* maps, MmtParams p, cudaStream_t stream)
     if (sms <= 0) return cudaErrorNotSupported;
 
     // K split: for each cluster size the chunk (whole stages), the ring that
-    // fits and how many clusters the device runs at once; take the one with
-    // the fewest weight bytes per CTA (rows of the busiest cluster x chunk)
+    // fits and how many clusters the device runs at once; take the one whose
+    // busiest CTA the time model below puts first
     Choice best;
     int64_t best_cost = -1;
     for (int ks : {8, 4, 2, 1}) {
         if (g_force_ks != 0 && ks != g_force_ks) continue;
         const int nbc = (p.KB + ks - 1) / ks;
-        const int nbc4 = (nbc + kStageBlocks - 1) / kStageBlocks * kStageBlocks;
-        const int kse = (p.KB + nbc4 - 1) / nbc4;
+        const int chunk = (nbc + kStageBlocks - 1) / kStageBlocks * kStageBlocks;
+        const int kse = (p.KB + chunk - 1) / chunk;
         if ((kse & (kse - 1)) != 0) continue;  // the partials' owner is lane % ks: a power of two
         if (g_force_ks != 0 && kse != g_force_ks) continue;
-        const Layout L = layout_for<MT>(nbc4);
+        const Layout L = layout_for<MT>(chunk);
         if (L.stages < 2) continue;
         static std::mutex mu;
         static int cache[64][4][kMaxCluster + 1];  // [device][MT index][ks] -> clusters + 1 (0: unknown)
@@ -842,7 +843,7 @@ cudaError_t launch_mt(const CUtensorMap* maps, MmtParams p, cudaStream_t stream)
         // latency under load (~3500 cycles) over the ring depth
         const int64_t tiles = (p.ntiles + nclu - 1) / nclu;
         const int64_t whole = tiles / kPassTiles, tail = tiles % kPassTiles;
-        const int64_t nstage = nbc4 / kStageBlocks;
+        const int64_t nstage = chunk / kStageBlocks;
         const int64_t t_lat = 3500 / L.stages;
         const int64_t t_whole = std::max<int64_t>((kW8 + kWS) / 23, t_lat);
         const int64_t t_tail =
@@ -852,16 +853,16 @@ cudaError_t launch_mt(const CUtensorMap* maps, MmtParams p, cudaStream_t stream)
             best_cost = cost;
             best.ks = kse;
             best.clusters = nclu;
-            best.nbc = nbc4;
+            best.nbc = chunk;
             best.L = L;
         }
     }
     if (best_cost < 0) return cudaErrorNotSupported;
 
-    g_last_cfg[0] = best.ks;
-    g_last_cfg[1] = best.clusters;
-    g_last_cfg[2] = best.L.stages;
-    g_last_cfg[3] = best.nbc;
+    g_last_cfg[0].store(best.ks, std::memory_order_relaxed);
+    g_last_cfg[1].store(best.clusters, std::memory_order_relaxed);
+    g_last_cfg[2].store(best.L.stages, std::memory_order_relaxed);
+    g_last_cfg[3].store(best.nbc, std::memory_order_relaxed);
     p.nbc = best.nbc;
     p.clusters = best.clusters;
     p.stages = best.L.stages;
@@ -952,7 +953,7 @@ void set_mmt_test_hooks(int inject_skip_stage, unsigned long long timeout_cycles
 void set_small_kernel(int which) { g_small_kernel = which; }
 void set_small_split(int ks) { g_force_ks = ks; }
 void small_kernel_config(int* out) {
-    for (int i = 0; i < 4; ++i) out[i] = g_last_cfg[i];
+    for (int i = 0; i < 4; ++i) out[i] = g_last_cfg[i].load(std::memory_order_relaxed);
 }
 int small_kernel() { return g_small_kernel; }
 
