@@ -90,10 +90,10 @@ cudaError_t launch_qdot_q50_fused(const FusedArgs& a, cudaStream_t stream);
 cudaError_t launch_qdot_tc_q50(const QdotArgs& a, cudaStream_t stream);
 
 // tcgen05 tensor-core kernels.  cudaErrorNotSupported if the device is not
-// sm_103.  Every shape runs the kernel of qdot_tc.cu (launch_qdot_tc) unless
-// set_prompt_kernel(1) asks for the kernel of qdot_tcw.cu (scales applied in
-// registers, two blocks per hand-off) for the prompt shapes it takes (M > 64,
-// scaled output, a call that may allocate).
+// sm_103.  The prompt shapes that the kernel of qdot_tcw.cu takes (M > 64,
+// scaled output, K % 128 == 0, a call that may allocate) run it (scales applied
+// in registers, two blocks per hand-off) unless set_prompt_kernel(0) asks for
+// the kernel of qdot_tc.cu, which runs every other shape.
 cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream);
 cudaError_t launch_qdot_tcw(const QdotArgs& a, cudaStream_t stream);
 void set_prompt_kernel(int which);

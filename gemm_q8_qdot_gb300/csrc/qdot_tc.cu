@@ -1095,7 +1095,7 @@ cudaError_t launch_tc(const QdotArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-int g_prompt_kernel = 0;  // 0: this file's kernel; 1: the tensor-memory kernel where it applies
+int g_prompt_kernel = 1;  // 1: the kernel of qdot_tcw.cu where it applies; 0: this file's kernel
 
 void set_prompt_kernel(int which) { g_prompt_kernel = which; }
 

@@ -157,9 +157,53 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+__device__ __forceinline__ void tmem_wait_ld8(uint32_t (&r)[8]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+                 :
+                 : "memory");
+}
+
+// The epilogue's wait: every lane tests the barrier (no branch to lane 0 and no
+// broadcast); the result is made warp-uniform before the warp-collective TMEM
+// loads it guards.  The abort flag is read from shared memory by its address.
+__device__ __forceinline__ uint32_t abort_get(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ bool epi_wait(uint64_t* bar, uint32_t parity, uint32_t abort_a, unsigned long long limit) {
+    bool ok = abort_get(abort_a) == 0;
+    if (ok && !tc::mbar_try_wait(bar, parity)) {
+        const long long t0 = clock64();
+        for (uint32_t n = 1;; ++n) {
+            if (tc::mbar_try_wait(bar, parity)) break;
+            if ((n & 31) == 0) {
+                if (abort_get(abort_a)) {
+                    ok = false;
+                    break;
+                }
+                if (static_cast<unsigned long long>(clock64() - t0) > limit) {
+                    set_abort(reinterpret_cast<volatile int*>(__cvta_shared_to_generic(abort_a)));
+                    ok = false;
+                    break;
+                }
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Arrival on a barrier by lane 0 of the warp, as one predicated instruction.
+__device__ __forceinline__ void arrive_lane0(uint64_t* bar, int lane) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %1, 0;\n\t"
+                 "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}"
+                 ::"r"(tc::smem_u32(bar)), "r"(lane) : "memory");
+}
+
 // NREG registers a thread (the launcher takes the largest build the device
-// admits with 704 threads)
-template <int NREG>
+// admits with 704 threads); WSR: weight scales [N, K/32] (else [K/32, N])
+template <int NREG, bool WSR>
 __global__ void __maxnreg__(NREG)
 qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWS,
                 const TcwParams prm) {
@@ -380,84 +424,102 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         // ------------------------------------------------------------ epilogue
         // thread (quadrant qd, column quarter cq, lane t): weight rows
         // 32 qd + t/4 + {0, 8, 16, 24} and activation rows 32 cq + 8 r + 2 (t % 4) + {0, 1},
-        // r = 0..3, of the tile -- the 16x256b TMEM load layout over two 16-lane halves
+        // r = 0..3, of the tile -- the 16x256b TMEM load layout over two 16-lane halves.
+        // A scale group's four blocks are unrolled, so every shared-memory and TMEM
+        // address below is a per-thread base plus a constant; the waits are taken by
+        // all lanes together and the arrivals predicated on lane 0, without branches.
         const int qd = warp & 3;
         const int cq = (warp - kEpi0) >> 2;
         const int m = lane & 3;
         const int rr = lane >> 2;
-        const uint32_t t_q = tmem_base + (static_cast<uint32_t>(qd * 32) << 16);
+        const uint32_t t_q = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + static_cast<uint32_t>(cq * 32);
+        // weight scale of row 32 qd + rr + 8 k, block bb of a scale slot: [row][4] or [4][row]
+        const uint32_t w_base = static_cast<uint32_t>(WSR ? (qd * 32 + rr) * GROUP * 4 : (qd * 32 + rr) * 4);
+        constexpr uint32_t kWk = WSR ? 8 * GROUP * 4 : 8 * 4;
+        constexpr uint32_t kWb = WSR ? 4 : TW * 4;
+        // activation scales ordered [bb][cq][c][m][4]: one 16-byte load per chunk, the four
+        // threads m of a chunk reading 64 contiguous bytes
+        const uint32_t a_base = static_cast<uint32_t>(kWsc + (cq * 32 + m * 4) * 4);
+        const uint32_t abort_a = tc::smem_u32(const_cast<int*>(abort_flag));
         uint64_t acc[4][4];  // [row k][r]: f32 pair of activation rows (2m, 2m + 1) + 8r + 32cq
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
             for (int r = 0; r < 4; ++r) acc[k][r] = 0ull;
-        int gi = 0, si = 0;
+        uint32_t gi = 0;  // scale groups over all units of this CTA; stage 2 gi + h uses buffer h
         for (int u = u_first; u < prm.units; u += u_step) {
-            const Unit un = unit(u);
-            for (int kg = 0; kg < un.ng; ++kg, ++gi) {
-                const int sr = gi % SR;
-                const bool oks = warp_wait(&sfull[sr], (gi / SR) & 1, abort_flag, limit, lane);
-                const uint32_t wsc = sbase + kOffSc + sr * kSc;
-                const uint32_t asc = wsc + kWsc;
+            const int ng = unit(u).ng;
+            for (int kg = 0; kg < ng; ++kg, ++gi) {
+                const uint32_t sr = gi % SR;
+                const bool oks = epi_wait(&sfull[sr], (gi / SR) & 1, abort_a, limit);
+                const uint32_t wsc = sbase + kOffSc + sr * kSc + w_base;
+                const uint32_t asc = sbase + kOffSc + sr * kSc + a_base;
 #pragma unroll 1
-                for (int h = 0; h < 2; ++h, ++si) {
-                    const int buf = si % kNbufD;
-                    const bool ok = oks && warp_wait(&tfull[buf], (si / kNbufD) & 1, abort_flag, limit, lane, 32);
+                for (int h = 0; h < kNbufD; ++h) {
+                    const bool ok = oks && epi_wait(&tfull[h], gi & 1, abort_a, limit);
                     if (ok) {
                         tc::tc_fence_after_sync();
 #pragma unroll 1
                         for (int bl = 0; bl < 2; ++bl) {
                             const int bb = h * 2 + bl;  // block within the group
-                            // weight scales of the thread's four rows for block bb, as f32 pairs
-                            uint64_t w2[4];
+                            uint64_t w2[4];             // weight scales of the thread's rows, as f32 pairs
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                const int row = qd * 32 + rr + 8 * k;
-                                const float w =
-                                    tc::lds32f(wsc + (prm.ws_rowmajor ? row * GROUP + bb : bb * TW + row) * 4);
-                                w2[k] = f2_pack(__float_as_uint(w), __float_as_uint(w));
+                                const uint32_t w = tc::lds32(wsc + k * kWk + bb * kWb);
+                                w2[k] = f2_pack(w, w);
                             }
-                            // activation scales of the thread's rows of 16-column chunk c:
-                            // [bb][cq][c][m][4] order, one 16-byte load per chunk, the four
-                            // threads m of a chunk reading 64 contiguous bytes
-                            const uint32_t as0 = asc + ((bb * 4 + cq) * 32 + m * 4) * 4;
-                            const uint32_t col0 = t_q + static_cast<uint32_t>(buf * 2 * TA + bl * TA + cq * 32);
-#pragma unroll
-                            for (int c = 0; c < 2; ++c) {
-                                uint32_t h0[8], h1[8];  // lanes + 0..15 and + 16..31 of the quadrant
-                                tc::TmemLd16x256bX2::load(col0 + c * 16, h0);
-                                tc::TmemLd16x256bX2::load(col0 + (16u << 16) + c * 16, h1);
-                                const float4 av = tc::lds128f(as0 + c * 64);
-                                tc::tmem_wait_ld2x8(h0, h1);
-                                if (bl == 1 && c == 1) {
-                                    // every load of this buffer has landed: hand it back
-                                    tc::tc_fence_before_sync();
-                                    __syncwarp();
-                                    if (lane == 0) tc::mbar_arrive(&tempty[buf]);
-                                }
+                            const uint32_t col0 = t_q + static_cast<uint32_t>(h * 2 * TA + bl * TA);
+                            // sub-chunk s = 2 c + half: 16 columns of one 16-lane half; the load
+                            // of sub-chunk s + 1 is issued before the arithmetic of sub-chunk s
+                            float4 av = tc::lds128f(asc + bb * 512);
+                            auto apply = [&](int sc, const uint32_t(&hv)[8]) {
+                                const int c = sc >> 1, half = sc & 1;
 #pragma unroll
                                 for (int rl = 0; rl < 2; ++rl) {
                                     const int r = 2 * c + rl;
                                     const uint64_t a2 = rl ? f2_pack(__float_as_uint(av.z), __float_as_uint(av.w))
                                                            : f2_pack(__float_as_uint(av.x), __float_as_uint(av.y));
-                                    acc[0][r] = f2_fma(w2[0], f2_mul(a2, f2_pack(h0[4 * rl], h0[4 * rl + 1])), acc[0][r]);
-                                    acc[1][r] = f2_fma(w2[1], f2_mul(a2, f2_pack(h0[4 * rl + 2], h0[4 * rl + 3])), acc[1][r]);
-                                    acc[2][r] = f2_fma(w2[2], f2_mul(a2, f2_pack(h1[4 * rl], h1[4 * rl + 1])), acc[2][r]);
-                                    acc[3][r] = f2_fma(w2[3], f2_mul(a2, f2_pack(h1[4 * rl + 2], h1[4 * rl + 3])), acc[3][r]);
+#pragma unroll
+                                    for (int kk = 0; kk < 2; ++kk) {
+                                        const int k = 2 * half + kk;
+                                        acc[k][r] = f2_fma(w2[k], f2_mul(a2, f2_pack(hv[4 * rl + 2 * kk], hv[4 * rl + 2 * kk + 1])),
+                                                           acc[k][r]);
+                                    }
                                 }
+                            };
+                            uint32_t hA[8], hB[8];
+                            tc::TmemLd16x256bX2::load(col0, hA);
+                            tmem_wait_ld8(hA);
+                            tc::TmemLd16x256bX2::load(col0 + (16u << 16), hB);
+                            apply(0, hA);
+                            tmem_wait_ld8(hB);
+                            tc::TmemLd16x256bX2::load(col0 + 16, hA);
+                            apply(1, hB);
+                            tmem_wait_ld8(hA);
+                            av = tc::lds128f(asc + bb * 512 + 64);
+                            tc::TmemLd16x256bX2::load(col0 + (16u << 16) + 16, hB);
+                            apply(2, hA);
+                            tmem_wait_ld8(hB);
+                            if (bl == 1) {
+                                // every load of this buffer has landed: hand it back
+                                tc::tc_fence_before_sync();
+                                __syncwarp();
+                                arrive_lane0(&tempty[h], lane);
                             }
+                            apply(3, hB);
                         }
                     } else {
                         tc::tc_fence_before_sync();
                         __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&tempty[buf]);
+                        arrive_lane0(&tempty[h], lane);
                     }
                 }
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&sempty[sr]);
+                arrive_lane0(&sempty[sr], lane);
             }
             // the unit's tile (or K split of it) goes to C
-            if (*abort_flag == 0) {
+            if (abort_get(abort_a) == 0) {
+                const Unit un = unit(u);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int64_t j = un.j0 + qd * 32 + rr + 8 * k;
@@ -571,29 +633,31 @@ EncodeTiledFn encode_fn() {
 
 using TcwKernel = void (*)(CUtensorMap, CUtensorMap, TcwParams);
 
-// The build of qdot_tcw_kernel with the most registers a thread whose 704
-// threads the device admits in one block (the per-block register file is the
-// limit; the device, not the arithmetic, decides which one fits), with its
-// shared-memory size set; null if none.  Chosen once per device.
-TcwKernel pick_kernel(int dev) {
+// The build of qdot_tcw_kernel for the weight-scale layout with the most
+// registers a thread that the device admits for 704 threads in one block (the
+// register file of an SM sub-partition holds six of the 22 warps), with its
+// shared-memory size set; null if none.  Chosen once per device and layout.
+TcwKernel pick_kernel(int dev, bool rowmajor) {
     static std::mutex mu;
-    static TcwKernel chosen[64] = {};
-    static bool have[64] = {};
+    static TcwKernel chosen[64][2] = {};
+    static bool have[64][2] = {};
     if (dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lk(mu);
-    if (!have[dev]) {
-        have[dev] = true;
-        const TcwKernel cands[3] = {qdot_tcw_kernel<88>, qdot_tcw_kernel<80>, qdot_tcw_kernel<72>};
-        for (TcwKernel k : cands) {
+    const int l = rowmajor ? 1 : 0;
+    if (!have[dev][l]) {
+        have[dev][l] = true;
+        const TcwKernel cands[2][2] = {{qdot_tcw_kernel<80, false>, qdot_tcw_kernel<72, false>},
+                                       {qdot_tcw_kernel<80, true>, qdot_tcw_kernel<72, true>}};
+        for (TcwKernel k : cands[l]) {
             cudaFuncAttributes fa{};
             if (cudaFuncGetAttributes(&fa, k) != cudaSuccess || fa.maxThreadsPerBlock < kThreads) continue;
             if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) continue;
-            chosen[dev] = k;
+            chosen[dev][l] = k;
             break;
         }
         cudaGetLastError();  // a declined candidate leaves no sticky error behind
     }
-    return chosen[dev];
+    return chosen[dev][l];
 }
 
 int g_skip = -1;
@@ -700,7 +764,7 @@ cudaError_t launch_qdot_tcw(const QdotArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     const int64_t grid = std::min<int64_t>(prm.units, sms);
-    auto kern = pick_kernel(dev);
+    auto kern = pick_kernel(dev, rowmajor);
     if (!kern) return cudaErrorNotSupported;
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), static_cast<size_t>(kSmem), stream,
                       maps[0], maps[1], prm);
@@ -716,7 +780,7 @@ cudaError_t read_and_clear_status_w(unsigned* status) {
 int tcw_kernel_regs() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const TcwKernel k = pick_kernel(dev);
+    const TcwKernel k = pick_kernel(dev, true);
     if (!k) return 0;
     cudaFuncAttributes fa{};
     return cudaFuncGetAttributes(&fa, k) == cudaSuccess ? fa.numRegs : 0;

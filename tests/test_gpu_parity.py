@@ -297,6 +297,9 @@ def test_qdot_tc_small(pq, M, N, K, layout):
     assert_within_bound(C, out, bound, f"tc M={M} N={N} K={K} layout={layout}")
 
 
+DEFAULT_PROMPT_KERNEL = 1  # scales in registers (include/pq_debug.h)
+
+
 def _set_prompt_kernel(pq, which):
     import ctypes
     lib = pq.load()
@@ -315,7 +318,7 @@ PROMPT_SHAPES = [(65, 64, 256), (130, 200, 128), (256, 384, 1024), (300, 129, 25
 @pytest.mark.parametrize("layout", [0, 1])
 def test_prompt_kernels(pq, which, M, N, K, layout):
     """Both tensor-core kernels of the prompt shapes (M > 64) against the oracle: the one
-    with the scale-product MMA (the default) and the one applying the scales in registers;
+    with the scale-product MMA and the one applying the scales in registers (the default);
     ragged M and N, both scale layouts, split K."""
     a, a_s, w, w_s = rand_operands(M * 7 + N * 3 + K + layout + 1000 * which, M, N, K)
     out, bound = oracle.qdot(a, a_s, w, w_s, omp=True)
@@ -326,24 +329,24 @@ def test_prompt_kernels(pq, which, M, N, K, layout):
         C = pq.qdot_q8_0_ex(dev(a), dev(a_s), dev(w), dev(ws), ws_layout=layout, path=path)
         pq.check_device()
     finally:
-        _set_prompt_kernel(pq, 0)
+        _set_prompt_kernel(pq, DEFAULT_PROMPT_KERNEL)
     assert_within_bound(C, out, bound, f"kernel {which} M={M} N={N} K={K} layout={layout}")
 
 
-def test_second_prompt_kernel_at_full_size(pq):
-    """The second prompt kernel (scales in registers) at the benchmark's full size (M = 512,
-    K = 4096, N = 14336) on one complete row per 128-row band and one column per 128-column
-    band."""
+@pytest.mark.parametrize("which", [0, 1], ids=["scale_product_mma", "scales_in_registers"])
+def test_prompt_kernels_at_full_size(pq, which):
+    """Both prompt kernels at the benchmark's full size (M = 512, K = 4096, N = 14336) on one
+    complete row per 128-row band and one column per 128-column band."""
     name = "prompt_m512_k4096_n14336"
     x, w, qa, sa, qw, sw = quantized_workload(name)
     A, AS = pq.quantize_q8_0(dev(x))
     W, WS = pq.quantize_q8_0(dev(w))
     try:
-        _set_prompt_kernel(pq, 1)
+        _set_prompt_kernel(pq, which)
         C = host(pq.qdot_q8_0(A, AS, W, WS))
         pq.check_device()
     finally:
-        _set_prompt_kernel(pq, 0)
+        _set_prompt_kernel(pq, DEFAULT_PROMPT_KERNEL)
     M, N = qa.shape[0], qw.shape[0]
     rng = np.random.default_rng(3)
     rows = np.array([b + rng.integers(0, min(128, M - b)) for b in range(0, M, 128)])

@@ -67,6 +67,6 @@ def test_tc_bounded_wait_gives_up_and_recovers(pq, M, kernel, path, K):
         C = pq.qdot_q8_0_ex(A, AS, W, WS, path=path)
         pq.check_device()
     finally:
-        _prompt_kernel(lib, 0)
+        _prompt_kernel(lib, 1)  # the default (include/pq_debug.h)
     out, bound = oracle.qdot(a, a_s, w, w_s)
     assert np.all(np.abs(C.cpu().numpy().astype(np.float64) - out) <= bound)
