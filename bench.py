@@ -497,9 +497,9 @@ def roofline_for(prob: Problem, qdot_ms: float, peaks, peak_src: str, one_kernel
                 "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes": nbytes}
     achieved = wl.ops / (qdot_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
-    # prompt shapes: Q8_0 weights run the kernel that applies the scales in
-    # registers (qdot_tcw.cu), Q5_0 weights the one with the scale-product MMA
-    kernel = "qdot_tc" if prob.q50 else "qdot_tcw"
+    # prompt shapes (Q8_0 and Q5_0 weights) run the kernel that applies the
+    # scales in registers (qdot_tcw.cu)
+    kernel = "qdot_tcw"
     traffic = recorded_traffic(kernel, wl.name)
     return {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,

@@ -91,11 +91,12 @@ cudaError_t launch_qdot_tc_q50(const QdotArgs& a, cudaStream_t stream);
 
 // tcgen05 tensor-core kernels.  cudaErrorNotSupported if the device is not
 // sm_103.  The prompt shapes that the kernel of qdot_tcw.cu takes (M > 64,
-// scaled output, K % 128 == 0, a call that may allocate) run it (scales applied
-// in registers, two blocks per hand-off) unless set_prompt_kernel(0) asks for
-// the kernel of qdot_tc.cu, which runs every other shape.
+// scaled output, K % 128 == 0, a call that may allocate; Q8_0 or Q5_0 weights)
+// run it (scales applied in registers, two blocks per hand-off) unless
+// set_prompt_kernel(0) asks for the kernel of qdot_tc.cu, which runs every
+// other shape.
 cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream);
-cudaError_t launch_qdot_tcw(const QdotArgs& a, cudaStream_t stream);
+cudaError_t launch_qdot_tcw(const QdotArgs& a, cudaStream_t stream, bool q5 = false);
 void set_prompt_kernel(int which);
 
 // Warp-level MMA kernel (mma.sync m16n8k16, f16 operands, exact block sums) for

@@ -1109,6 +1109,10 @@ cudaError_t launch_qdot_tc(const QdotArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_qdot_tc_q50(const QdotArgs& a, cudaStream_t stream) {
     if (a.S != nullptr) return cudaErrorNotSupported;
+    if (a.M > 64 && g_prompt_kernel == 1) {
+        const cudaError_t e = launch_qdot_tcw(a, stream, true);
+        if (e != cudaErrorNotSupported) return e;
+    }
     return launch_tc<false, true>(a, stream);
 }
 

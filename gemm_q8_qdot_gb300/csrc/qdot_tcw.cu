@@ -1,11 +1,13 @@
 // qdot_t for prompt-sized M on the sm_103a tensor cores, with the scales
 // applied in f32 registers (no scale-product MMA) and two Q8_0 blocks per
-// hand-off between the roles.
+// hand-off between the roles; also q50_qdot_t, with Q5_0 weight blocks.
 //
 // What it computes ("Quantized built-ins and formats", section "Q8_0"; the
 // integer-tensor-core variant qmma_t in "Phobos Language Spec" section 10):
 //   out[i, j] = sum_b a_scales[i, b] * w_scales[j, b] * S[i, j, b],
-//   S[i, j, b] = sum_{k in block b} a[i, k] * w[j, k]   (an integer).
+//   S[i, j, b] = sum_{k in block b} a[i, k] * w[j, k]   (an integer),
+// with w[j, k] = q - 16 for Q5_0 weights ("Phobos Language Spec" section 10,
+// Q5_0 row).
 //
 // Engine.  As in the other tensor-core kernel: int8 values are exact in f16,
 // and every partial sum of one 32-element block (|S| <= 2^19 < 2^24) is exact
@@ -18,9 +20,10 @@
 // scale is one value per TMEM lane (per epilogue thread row) and an
 // activation scale one value per column, and the activation scales can be laid
 // out in the order the epilogue threads read them.  The weights are widened
-// int8 -> f16 by four converter warps from the TMA-loaded int8 tile into the
-// f16 stage; the activations were converted once per call into f16 MMA tiles
-// by a small kernel (tile_act_kernel) and arrive by bulk copy.
+// int8 -> f16 (or Q5_0 blocks decoded to q - 16 in f16) by four converter warps
+// from the TMA-loaded tile into the f16 stage; the activations were converted
+// once per call into f16 MMA tiles by a small kernel (tile_act_kernel) and
+// arrive by bulk copy.
 //
 // Hand-offs.  One f16 stage holds 64 K (two Q8_0 blocks) of both operands,
 // and one accumulator buffer of 256 TMEM columns holds the block sums of those
@@ -31,7 +34,7 @@
 // Warps (704 threads, one persistent CTA per SM over (activation tile, weight
 // tile, K split) units, the activation tile fastest, so the CTAs running at
 // the same time share weight tiles in L2):
-//   warp 0      producer: per scale group (128 K) the int8 weight tile and
+//   warp 0      producer: per scale group (128 K) the weight tile and
 //               the weight-scale box (TMA), the group's activation scales,
 //               and the activation tiles of two f16 stages (bulk copies);
 //   warp 1      MMA issuer (one thread), TMEM allocation;
@@ -72,6 +75,7 @@ constexpr int kWt = TW * 64 * 2;         // f16 weight tile of one stage: 128 ro
 constexpr int kStage = kAct + kWt;       // one f16 stage: two Q8_0 blocks of both operands
 constexpr int kAsc = GROUP * TA * 4;     // activation scales of one group (2 KB)
 constexpr int kW8 = TW * 128;            // int8 weight tile of one group (16 KB)
+constexpr int kQ5Row = GROUP * 20;       // Q5_0 blocks of one row and group: 4 x (qh word + 16 nibble bytes)
 constexpr int kWsc = TW * GROUP * 4;     // weight scales of one group (2 KB)
 constexpr int S16 = 4;                   // f16 stages
 constexpr int S8 = 3;                    // int8 weight stages (groups)
@@ -164,6 +168,43 @@ __device__ __forceinline__ void tmem_wait_ld8(uint32_t (&r)[8]) {
                  : "memory");
 }
 
+// Q5_0 ("Phobos Language Spec" section 10, Q5_0 row): a block is the qh word,
+// then 16 bytes whose byte e holds element e in its low nibble and element
+// e + 16 in its high nibble, each element q - 16 with the fifth bit of q in
+// bit e of qh.  q5_spread4 puts the four bits of x at bit 0 of the four bytes
+// (x * 0x00204081 places bit i at bit 8i, no carries); q5_to_f16x4 turns four
+// biased elements q in [0, 31] (one a byte) into two f16x2 of q - 16, exactly
+// (each byte placed under the f16 exponent of 1024, then 1040 = 1024 + 16
+// subtracted).
+__device__ __forceinline__ uint32_t q5_spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
+
+__device__ __forceinline__ void q5_to_f16x4(uint32_t q, uint32_t& lo, uint32_t& hi) {
+    const uint32_t a = __byte_perm(q, 0x64646464u, 0x4140u);
+    const uint32_t b = __byte_perm(q, 0x64646464u, 0x4342u);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6410u), __ushort_as_half(0x6410u));
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&ha);
+    hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+// The 16-byte f16 chunk c (elements 8c .. 8c + 7) of a Q5_0 block given as
+// its qh word and four data words.
+__device__ __forceinline__ uint4 q5_chunk(uint32_t qh, const uint32_t (&d)[4], int c) {
+    uint32_t u[2];
+#pragma unroll
+    for (int hw = 0; hw < 2; ++hw) {
+        const int e0 = 8 * c + 4 * hw;  // first element of the word
+        const uint32_t dw = d[(e0 & 15) >> 2];
+        const uint32_t nib = e0 < 16 ? (dw & 0x0f0f0f0fu) : ((dw >> 4) & 0x0f0f0f0fu);
+        u[hw] = nib | (q5_spread4((qh >> e0) & 0xfu) << 4);
+    }
+    uint4 o;
+    q5_to_f16x4(u[0], o.x, o.y);
+    q5_to_f16x4(u[1], o.z, o.w);
+    return o;
+}
+
 // The epilogue's wait: every lane tests the barrier (no branch to lane 0 and no
 // broadcast); the result is made warp-uniform before the warp-collective TMEM
 // loads it guards.  The abort flag is read from shared memory by its address.
@@ -202,8 +243,9 @@ __device__ __forceinline__ void arrive_lane0(uint64_t* bar, int lane) {
 }
 
 // NREG registers a thread (the launcher takes the largest build the device
-// admits with 704 threads); WSR: weight scales [N, K/32] (else [K/32, N])
-template <int NREG, bool WSR>
+// admits with 704 threads); WSR: weight scales [N, K/32] (else [K/32, N]); Q5:
+// the weights are Q5_0 blocks [N, K/32 * 20] bytes (q50_qdot_t) instead of int8
+template <int NREG, bool WSR, bool Q5>
 __global__ void __maxnreg__(NREG)
 qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWS,
                 const TcwParams prm) {
@@ -292,12 +334,13 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
                 for (int k = 0; k < un.ng; ++k, ++gi) {
                     const int g = un.g_begin + k;
                     if (gi == prm.inject_skip_stage) continue;  // test hook: this group never arrives
-                    // int8 weight tile of the group: 128 rows x 128 K, 128-byte swizzle
+                    // weight tile of the group: 128 rows x 128 K, int8 with 128-byte swizzle
+                    // or Q5_0 blocks (80 bytes a row, no swizzle)
                     const int s8 = gi % S8;
                     if (bounded_wait(&empty8[s8], ((gi / S8) & 1) ^ 1, abort_flag, limit, kBackoff)) {
                         issued8 = gi + 1;
-                        tc::mbar_arrive_expect_tx(&full8[s8], kW8);
-                        tc::tma_load_2d(smem + kOffW8 + s8 * kW8, &tmW, &full8[s8], g * 128,
+                        tc::mbar_arrive_expect_tx(&full8[s8], Q5 ? TW * kQ5Row : kW8);
+                        tc::tma_load_2d(smem + kOffW8 + s8 * kW8, &tmW, &full8[s8], g * (Q5 ? kQ5Row : 128),
                                         static_cast<int>(un.j0));
                     }
                     // weight scales (TMA box) and activation scales (bulk copy) of the group
@@ -378,7 +421,7 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         }
     } else if (warp >= kConv0 && warp < kEpi0) {
         // ------------------------------------------------------------ converters
-        // warp cw widens weight rows 32 cw .. 32 cw + 31 of the group's int8 tile, one row
+        // warp cw widens weight rows 32 cw .. 32 cw + 31 of the group's weight tile, one row
         // per lane, into the f16 weight tiles of the group's two stages (UMMA K-major
         // 128-byte swizzle: row r at r * 128 bytes, 16-byte chunk c at (c ^ (r & 7)) << 4)
         const int row = (warp - kConv0) * 32 + lane;
@@ -388,33 +431,70 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
             for (int k = 0; k < ng; ++k, ++gi) {
                 const int s8 = gi % S8;
                 const bool ok8 = warp_wait(&full8[s8], (gi / S8) & 1, abort_flag, limit, lane, kBackoff);
-                const uint32_t w8 = sbase + kOffW8 + s8 * kW8 + row * 128;
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    const int si = 2 * gi + h;
-                    const int s16 = si % S16;
-                    const bool ok = ok8 && warp_wait(&empty16[s16], ((si / S16) & 1) ^ 1, abort_flag, limit, lane,
-                                                     kBackoff);
-                    if (ok) {
-                        const uint32_t w16 = sbase + kOffSt + s16 * kStage + kAct + row * 128;
-                        uint4 v[4];
+                if constexpr (Q5) {
+                    // the row's four Q5_0 blocks: 80 bytes (rows 80 bytes apart: the 16-byte
+                    // loads of eight consecutive rows fall in distinct banks)
+                    const uint32_t w5 = sbase + kOffW8 + s8 * kW8 + row * kQ5Row;
+                    uint32_t q[GROUP * 5];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) v[c] = tc::lds128(w8 + (((h * 4 + c) ^ (row & 7)) << 4));
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint4 o0, o1;
-                            i8x4_to_f16x4(v[c].x, o0.x, o0.y);
-                            i8x4_to_f16x4(v[c].y, o0.z, o0.w);
-                            i8x4_to_f16x4(v[c].z, o1.x, o1.y);
-                            i8x4_to_f16x4(v[c].w, o1.z, o1.w);
-                            tc::sts128(w16 + (((2 * c) ^ (row & 7)) << 4), o0);
-                            tc::sts128(w16 + (((2 * c + 1) ^ (row & 7)) << 4), o1);
-                        }
-                        tc::fence_proxy_async_smem();
+                    for (int t = 0; t < 5; ++t) {
+                        const uint4 v = ok8 ? tc::lds128(w5 + 16 * t) : make_uint4(0u, 0u, 0u, 0u);
+                        q[4 * t] = v.x;
+                        q[4 * t + 1] = v.y;
+                        q[4 * t + 2] = v.z;
+                        q[4 * t + 3] = v.w;
                     }
-                    __syncwarp();
-                    // arrive also after an abort: every barrier keeps a consistent phase
-                    if (lane == 0) tc::mbar_arrive(&full16[s16]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int si = 2 * gi + h;
+                        const int s16 = si % S16;
+                        const bool ok = ok8 && warp_wait(&empty16[s16], ((si / S16) & 1) ^ 1, abort_flag, limit,
+                                                         lane, kBackoff);
+                        if (ok) {
+                            const uint32_t w16 = sbase + kOffSt + s16 * kStage + kAct + row * 128;
+#pragma unroll
+                            for (int bb = 0; bb < 2; ++bb) {
+                                const int b = 2 * h + bb;  // block within the group
+                                const uint32_t d[4] = {q[5 * b + 1], q[5 * b + 2], q[5 * b + 3], q[5 * b + 4]};
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    tc::sts128(w16 + (((4 * bb + c) ^ (row & 7)) << 4), q5_chunk(q[5 * b], d, c));
+                            }
+                            tc::fence_proxy_async_smem();
+                        }
+                        __syncwarp();
+                        // arrive also after an abort: every barrier keeps a consistent phase
+                        if (lane == 0) tc::mbar_arrive(&full16[s16]);
+                    }
+                } else {
+                    const uint32_t w8 = sbase + kOffW8 + s8 * kW8 + row * 128;
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        const int si = 2 * gi + h;
+                        const int s16 = si % S16;
+                        const bool ok = ok8 && warp_wait(&empty16[s16], ((si / S16) & 1) ^ 1, abort_flag, limit,
+                                                         lane, kBackoff);
+                        if (ok) {
+                            const uint32_t w16 = sbase + kOffSt + s16 * kStage + kAct + row * 128;
+                            uint4 v[4];
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) v[c] = tc::lds128(w8 + (((h * 4 + c) ^ (row & 7)) << 4));
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                uint4 o0, o1;
+                                i8x4_to_f16x4(v[c].x, o0.x, o0.y);
+                                i8x4_to_f16x4(v[c].y, o0.z, o0.w);
+                                i8x4_to_f16x4(v[c].z, o1.x, o1.y);
+                                i8x4_to_f16x4(v[c].w, o1.z, o1.w);
+                                tc::sts128(w16 + (((2 * c) ^ (row & 7)) << 4), o0);
+                                tc::sts128(w16 + (((2 * c + 1) ^ (row & 7)) << 4), o1);
+                            }
+                            tc::fence_proxy_async_smem();
+                        }
+                        __syncwarp();
+                        // arrive also after an abort: every barrier keeps a consistent phase
+                        if (lane == 0) tc::mbar_arrive(&full16[s16]);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&empty8[s8]);
@@ -633,10 +713,12 @@ EncodeTiledFn encode_fn() {
 
 using TcwKernel = void (*)(CUtensorMap, CUtensorMap, TcwParams);
 
-// The build of qdot_tcw_kernel for the weight-scale layout with the most
-// registers a thread that the device admits for 704 threads in one block (the
-// register file of an SM sub-partition holds six of the 22 warps), with its
-// shared-memory size set; null if none.  Chosen once per device and layout.
+// The build of qdot_tcw_kernel for the weight format and the weight-scale
+// layout with the most registers a thread that the device admits for 704
+// threads in one block (the register file of an SM sub-partition holds six of
+// the 22 warps), with its shared-memory size set; null if none.  Chosen once
+// per device, format and layout.
+template <bool Q5>
 TcwKernel pick_kernel(int dev, bool rowmajor) {
     static std::mutex mu;
     static TcwKernel chosen[64][2] = {};
@@ -646,8 +728,8 @@ TcwKernel pick_kernel(int dev, bool rowmajor) {
     const int l = rowmajor ? 1 : 0;
     if (!have[dev][l]) {
         have[dev][l] = true;
-        const TcwKernel cands[2][2] = {{qdot_tcw_kernel<80, false>, qdot_tcw_kernel<72, false>},
-                                       {qdot_tcw_kernel<80, true>, qdot_tcw_kernel<72, true>}};
+        const TcwKernel cands[2][2] = {{qdot_tcw_kernel<80, false, Q5>, qdot_tcw_kernel<72, false, Q5>},
+                                       {qdot_tcw_kernel<80, true, Q5>, qdot_tcw_kernel<72, true, Q5>}};
         for (TcwKernel k : cands[l]) {
             cudaFuncAttributes fa{};
             if (cudaFuncGetAttributes(&fa, k) != cudaSuccess || fa.maxThreadsPerBlock < kThreads) continue;
@@ -665,13 +747,14 @@ unsigned long long g_timeout = 4000000000ull;  // ~2 s at 2 GHz
 
 }  // namespace
 
-// Prompt shapes (M > 64) of qdot_t, block-scaled output only (the launch
-// order: tile_act_kernel, the zeroing of C for split K, qdot_tcw_kernel).
+// Prompt shapes (M > 64) of qdot_t (q5: of q50_qdot_t, a.W holding Q5_0 blocks
+// [N, K/32 * 20] bytes), block-scaled output only (the launch order:
+// tile_act_kernel, the zeroing of C for split K, qdot_tcw_kernel).
 // cudaErrorNotSupported when the shape or the operands do not suit this kernel
-// (K % 128 != 0, scale planes that TMA cannot load, not sm_103) or when the
-// call may not allocate its activation workspace; the caller then takes the
-// other tensor-core kernel.
-cudaError_t launch_qdot_tcw(const QdotArgs& a, cudaStream_t stream) {
+// (K % 128 != 0, weights or scale planes that TMA cannot load, not sm_103) or
+// when the call may not allocate its activation workspace; the caller then
+// takes the other tensor-core kernel.
+cudaError_t launch_qdot_tcw(const QdotArgs& a, cudaStream_t stream, bool q5) {
     if (a.S != nullptr || a.no_alloc || a.M <= 64 || a.K % 128 != 0) return cudaErrorNotSupported;
     if (a.K > 0x7fffffffLL || a.M > 0x7fffffffLL || a.N > 0x7fffffffLL) return cudaErrorNotSupported;
     int dev = 0, major = 0, minor = 0, sms = 0;
@@ -723,14 +806,16 @@ cudaError_t launch_qdot_tcw(const QdotArgs& a, cudaStream_t stream) {
 
     CUtensorMap maps[2];
     {
-        // int8 W [N, K]: box {128 bytes of K, 128 rows}, 128-byte swizzle, zero fill past N
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.N)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K)};
-        const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(TW)};
+        // int8 W [N, K]: box {128 bytes of K, 128 rows}, 128-byte swizzle; Q5_0 W [N, K/32 * 20]
+        // bytes: box {80 bytes (one scale group), 128 rows}, no swizzle; zero fill past N
+        const int64_t row_bytes = q5 ? KB * 20 : a.K;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(a.N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+        const cuuint32_t box[2] = {q5 ? static_cast<cuuint32_t>(kQ5Row) : 128u, static_cast<cuuint32_t>(TW)};
         const cuuint32_t estr[2] = {1, 1};
         if (fn(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(a.W), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+               CU_TENSOR_MAP_INTERLEAVE_NONE, q5 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorNotSupported;
     }
     {
@@ -764,7 +849,7 @@ cudaError_t launch_qdot_tcw(const QdotArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     const int64_t grid = std::min<int64_t>(prm.units, sms);
-    auto kern = pick_kernel(dev, rowmajor);
+    auto kern = q5 ? pick_kernel<true>(dev, rowmajor) : pick_kernel<false>(dev, rowmajor);
     if (!kern) return cudaErrorNotSupported;
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), static_cast<size_t>(kSmem), stream,
                       maps[0], maps[1], prm);
@@ -780,7 +865,7 @@ cudaError_t read_and_clear_status_w(unsigned* status) {
 int tcw_kernel_regs() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const TcwKernel k = pick_kernel(dev, true);
+    const TcwKernel k = pick_kernel<false>(dev, true);
     if (!k) return 0;
     cudaFuncAttributes fa{};
     return cudaFuncGetAttributes(&fa, k) == cudaSuccess ? fa.numRegs : 0;

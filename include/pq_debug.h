@@ -32,15 +32,15 @@ extern "C" {
 int pq_debug_set_tc_fault(int skip_stage, unsigned long long timeout_cycles);
 
 /*
- * Chooses the tensor-core kernel of the prompt shapes (M > 64): 1 (the
- * default) the kernel that applies the scales in registers and hands two Q8_0
- * blocks at a time between its roles, wherever it takes the call (scaled
- * output, K a multiple of 128, a call that may allocate its activation
- * workspace); 0 the kernel with the scale-product MMA, which also serves small
- * batches, block sums, Q5_0 weights and the allocation-free entry.  Both
- * compute the same qdot_t within its tolerance; the hook lets the tests and
- * measurements run either.  Host state, process-wide, not thread-safe;
- * PQ_ERR_INVALID_ARG for any other value.
+ * Chooses the tensor-core kernel of the prompt shapes (M > 64, Q8_0 or Q5_0
+ * weights): 1 (the default) the kernel that applies the scales in registers
+ * and hands two blocks at a time between its roles, wherever it takes the
+ * call (scaled output, K a multiple of 128, a call that may allocate its
+ * activation workspace); 0 the kernel with the scale-product MMA, which also
+ * serves small batches, block sums and the allocation-free entry.  Both
+ * compute the same qdot_t (q50_qdot_t) within its tolerance; the hook lets the
+ * tests and measurements run either.  Host state, process-wide, not
+ * thread-safe; PQ_ERR_INVALID_ARG for any other value.
  */
 int pq_debug_set_prompt_kernel(int which);
 

@@ -103,20 +103,36 @@ def test_q50_workload_full(pq):
 
 # ------------------------------------------------------------ tensor-core route (M > 64)
 
-TC_SHAPES = [(65, 64, 128), (130, 300, 512), (256, 129, 1024), (512, 256, 4096)]
+TC_SHAPES = [(65, 64, 128), (130, 300, 512), (256, 129, 1024), (512, 256, 4096), (384, 2048, 1024)]
+DEFAULT_PROMPT_KERNEL = 1  # scales in registers (include/pq_debug.h)
 
 
+def _set_prompt_kernel(pq, which):
+    import ctypes
+    lib = pq.load()
+    lib.pq_debug_set_prompt_kernel.argtypes = [ctypes.c_int]
+    lib.pq_debug_set_prompt_kernel.restype = ctypes.c_int
+    assert lib.pq_debug_set_prompt_kernel(which) == 0
+
+
+@pytest.mark.parametrize("which", [0, 1], ids=["scale_product_mma", "scales_in_registers"])
 @pytest.mark.parametrize("M,N,K", TC_SHAPES)
 @pytest.mark.parametrize("layout", [0, 1])
-def test_q50_qdot_tensor_cores(pq, M, N, K, layout):
-    """Prompt shapes take the tensor-core kernel, which decodes the Q5_0 blocks to f16 in
-    shared memory (ragged N, both scale layouts, split K at the small shapes)."""
+def test_q50_qdot_tensor_cores(pq, M, N, K, layout, which):
+    """Prompt shapes take a tensor-core kernel, which decodes the Q5_0 blocks to f16 in
+    shared memory: the one applying the scales in registers (the default) or the one with
+    the scale-product MMA (ragged N, both scale layouts, split K at the small shapes, many
+    tiles per CTA at the last)."""
     a, a_s, w5, w_s = operands(M * 11 + N + K + layout, M, N, K)
     ws = w_s if layout == 0 else np.ascontiguousarray(w_s.T)
     out, bound = oracle.qdot_q5_0(a, a_s, w5, ws, ws_layout=layout)
-    C = pq.q50_qdot(dev(a), dev(a_s), dev(w5), dev(ws), ws_layout=layout)
-    pq.check_device()
-    within(C, out, bound, f"q50 tc M={M} N={N} K={K} layout={layout}")
+    try:
+        _set_prompt_kernel(pq, which)
+        C = pq.q50_qdot(dev(a), dev(a_s), dev(w5), dev(ws), ws_layout=layout)
+        pq.check_device()
+    finally:
+        _set_prompt_kernel(pq, DEFAULT_PROMPT_KERNEL)
+    within(C, out, bound, f"q50 tc kernel {which} M={M} N={N} K={K} layout={layout}")
 
 
 def test_q50_tensor_cores_under_capture(pq):
@@ -152,20 +168,28 @@ def test_q50_prompt_unaligned_weights_fall_back(pq):
     within(C, out, bound, "q50 offset W5, prompt shape")
 
 
-def test_q50_prompt_workload_full(pq):
-    """The Q5_0 prompt workload at full size through the tensor cores: sampled rows and columns."""
+@pytest.mark.parametrize("which", [0, 1], ids=["scale_product_mma", "scales_in_registers"])
+def test_q50_prompt_workload_full(pq, which):
+    """The Q5_0 prompt workload at full size through both tensor-core kernels: one complete
+    row per 128-row band and one complete column per 128-column band, so that every
+    128 x 128 output tile (every unit of the persistent CTAs) is checked."""
     wl = workloads.WORKLOADS["q50_prompt_m512_k4096_n14336"]
     x = workloads.activations(wl)
     qa, sa = oracle.quantize_q8_0(x)
     w5, ws = workloads.q50_weights(wl)
-    C = pq.q50_qdot(dev(qa), dev(sa), dev(w5), dev(ws))
-    pq.check_device()
+    try:
+        _set_prompt_kernel(pq, which)
+        C = pq.q50_qdot(dev(qa), dev(sa), dev(w5), dev(ws))
+        pq.check_device()
+    finally:
+        _set_prompt_kernel(pq, DEFAULT_PROMPT_KERNEL)
     rng = np.random.default_rng(4)
-    rows = np.sort(rng.choice(wl.M, 96, replace=False))
-    cols = np.sort(rng.choice(wl.N, 256, replace=False))
-    out, bound = oracle.qdot_q5_0(qa[rows], sa[rows], w5[cols], ws[cols])
-    sub = C[torch.from_numpy(rows).to(DEV)][:, torch.from_numpy(cols).to(DEV)]
-    within(sub, out, bound, "q50 prompt full size")
+    rows = np.array([b + rng.integers(0, min(128, wl.M - b)) for b in range(0, wl.M, 128)])
+    cols = np.array([b + rng.integers(0, min(128, wl.N - b)) for b in range(0, wl.N, 128)])
+    out, bound = oracle.qdot_q5_0(qa[rows], sa[rows], w5, ws, omp=True)
+    within(C[torch.from_numpy(rows).to(DEV)], out, bound, "q50 prompt full size, rows")
+    out, bound = oracle.qdot_q5_0(qa, sa, w5[cols], ws[cols], omp=True)
+    within(C[:, torch.from_numpy(cols).to(DEV)], out, bound, "q50 prompt full size, columns")
     assert torch.isfinite(C).all()
 
 
