@@ -4,9 +4,9 @@ The producer of a pipelined kernel is told (test hook, include/pq_debug.h) to
 skip one pipeline stage, so the consumers' waits on that stage never complete.
 Every wait is bounded: the kernel must give up within its limit, record the
 timeout in the library's status word, drain its work in flight, free its
-tensor memory and return.  Covered: the tcgen05 kernel (narrow tiles and both
-prompt-shape kernels) and the TMA-fed warp-level MMA kernel, whose CTAs also
-wait on one another across their cluster.  The test checks the reported status and that the
+tensor memory and return.  Covered: the tcgen05 kernels (narrow tiles, and both
+prompt-shape kernels with Q8_0 and with Q5_0 weights) and the TMA-fed
+warp-level MMA kernel, whose CTAs also wait on one another across their cluster.  The test checks the reported status and that the
 context stays usable (a normal launch afterwards gives correct results).
 """
 import ctypes
@@ -69,4 +69,37 @@ def test_tc_bounded_wait_gives_up_and_recovers(pq, M, kernel, path, K):
     finally:
         _prompt_kernel(lib, 1)  # the default (include/pq_debug.h)
     out, bound = oracle.qdot(a, a_s, w, w_s)
+    assert np.all(np.abs(C.cpu().numpy().astype(np.float64) - out) <= bound)
+
+
+@pytest.mark.parametrize("kernel", [0, 1], ids=["scale_product_mma", "scales_in_registers"])
+def test_q50_prompt_bounded_wait_gives_up_and_recovers(pq, kernel):
+    """The same for Q5_0 weights at a prompt shape, on both tensor-core kernels: the producer
+    skips one stage, the consumers' bounded waits give up, the status reports the timeout
+    and the next call on the same operands is correct."""
+    lib = pq.load()
+    _prompt_kernel(lib, kernel)
+    rng = np.random.default_rng(7)
+    M, N, K = 256, 256, 2048
+    a = workloads.random_int8(rng, (M, K))
+    w5 = rng.integers(0, 256, size=(N, K // 32 * 20), dtype=np.uint8)
+    a_s = workloads.random_scales(rng, (M, K // 32))
+    w_s = workloads.random_scales(rng, (N, K // 32))
+    A, AS, W5, WS = (torch.from_numpy(v).cuda() for v in (a, a_s, w5, w_s))
+    pq.check_device()  # clean status before
+    try:
+        _hook(lib, 1, 20_000_000)  # ~10 ms at 2 GHz
+        C = torch.full((M, N), 123.0, device="cuda")
+        pq.q50_qdot(A, AS, W5, WS, C)
+        with pytest.raises(pq.PQError) as ei:
+            pq.check_device()
+        assert ei.value.code == pq.PQ_ERR_TIMEOUT
+    finally:
+        _hook(lib, -1, 0)
+    try:
+        C = pq.q50_qdot(A, AS, W5, WS)
+        pq.check_device()
+    finally:
+        _prompt_kernel(lib, 1)  # the default (include/pq_debug.h)
+    out, bound = oracle.qdot_q5_0(a, a_s, w5, w_s)
     assert np.all(np.abs(C.cpu().numpy().astype(np.float64) - out) <= bound)
