@@ -74,11 +74,11 @@ constexpr int kAct = TA * 64 * 2;        // f16 activation tile of one stage: 12
 constexpr int kWt = TW * 64 * 2;         // f16 weight tile of one stage: 128 rows x 64 K (16 KB)
 constexpr int kStage = kAct + kWt;       // one f16 stage: two Q8_0 blocks of both operands
 constexpr int kAsc = GROUP * TA * 4;     // activation scales of one group (2 KB)
-constexpr int kW8 = TW * 128;            // int8 weight tile of one group (16 KB)
+constexpr int kW8 = TW * 128;            // weight tile slot of one group: int8 (16 KB) or Q5_0 (10 KB)
 constexpr int kQ5Row = GROUP * 20;       // Q5_0 blocks of one row and group: 4 x (qh word + 16 nibble bytes)
 constexpr int kWsc = TW * GROUP * 4;     // weight scales of one group (2 KB)
 constexpr int S16 = 4;                   // f16 stages
-constexpr int S8 = 3;                    // int8 weight stages (groups)
+constexpr int S8 = 3;                    // weight tile stages (groups)
 constexpr int SR = 4;                    // scale slots (groups)
 constexpr int kOffSt = 0;
 constexpr int kOffW8 = kOffSt + S16 * kStage;
@@ -254,7 +254,7 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
     uint64_t* full16 = bars;                  // f16 stage ready: activations landed (tx) + 4 converter warps
     uint64_t* empty16 = full16 + S16;         // its MMAs completed (commit)
-    uint64_t* full8 = empty16 + S16;          // int8 weight tile landed (producer, tx)
+    uint64_t* full8 = empty16 + S16;          // weight tile landed (producer, tx)
     uint64_t* empty8 = full8 + S8;            // converted (4 converter warps)
     uint64_t* sfull = empty8 + S8;            // scales of a group landed (producer, tx)
     uint64_t* sempty = sfull + SR;            // read (16 epilogue warps)

@@ -249,10 +249,12 @@ int pq_qdot_q8_0_blocksums(const int8_t* A, const int8_t* W, int32_t* S,
  * the reading taken).  WS is f32 [N, K/32] (PQ_WS_N_KB) or [K/32, N]
  * (PQ_WS_KB_N, q50_qmma_t's layout); A and AS as for pq_qdot_q8_0.  C is
  * overwritten.  Alignment: A 16 bytes; W5, AS, WS, C 4 bytes.  M <= 64 runs
- * the dp4a kernel; M > 64 runs the tensor-core kernel, which decodes the
- * blocks to f16 in shared memory (it needs K a multiple of 128 and W5, AS, WS
- * 16-byte aligned, and uses the per-stream workspace of pq_qdot_q8_0; shapes
- * it declines run the dp4a kernel).
+ * the dp4a kernel; M > 64 runs a tensor-core kernel, which decodes the blocks
+ * to f16 in shared memory (it needs K a multiple of 128 and W5 and WS 16-byte
+ * aligned, and uses the per-stream workspace of pq_qdot_q8_0; inside a stream
+ * capture before that workspace exists, the other tensor-core kernel, which
+ * also needs AS 16-byte aligned; shapes and operands both decline run the
+ * dp4a kernel).
  */
 int pq_q50_qdot(const int8_t* A, const float* AS, const uint8_t* W5, const float* WS, float* C,
                 int64_t M, int64_t N, int64_t K, int ws_layout, cudaStream_t stream);
