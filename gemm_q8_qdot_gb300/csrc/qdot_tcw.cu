@@ -161,6 +161,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Waits for every tcgen05.ld this thread has issued; the 8 registers named are
+// those of the load it is meant for, so no use of them is scheduled before it.
 __device__ __forceinline__ void tmem_wait_ld8(uint32_t (&r)[8]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
@@ -505,9 +507,9 @@ qdot_tcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         // thread (quadrant qd, column quarter cq, lane t): weight rows
         // 32 qd + t/4 + {0, 8, 16, 24} and activation rows 32 cq + 8 r + 2 (t % 4) + {0, 1},
         // r = 0..3, of the tile -- the 16x256b TMEM load layout over two 16-lane halves.
-        // A scale group's four blocks are unrolled, so every shared-memory and TMEM
-        // address below is a per-thread base plus a constant; the waits are taken by
-        // all lanes together and the arrivals predicated on lane 0, without branches.
+        // Every shared-memory and TMEM address below is a per-thread base plus a block
+        // offset and a constant; the waits are taken by all lanes together and the
+        // arrivals predicated on lane 0, without branches.
         const int qd = warp & 3;
         const int cq = (warp - kEpi0) >> 2;
         const int m = lane & 3;
