@@ -38,7 +38,9 @@ cudaError_t stream_workspace(cudaStream_t stream, size_t bytes, void** out, int 
     static std::mutex mu;
     static Slot slots[64];
     static int nslots = 0;
-    static void* retired[64 * 48] = {};  // replaced workspaces, kept until exit
+    // replaced workspaces are never freed (work already enqueued or captured may
+    // still use them); they stay listed here, reachable, until the process exits
+    [[maybe_unused]] static void* retired[64 * 48] = {};
     static int nretired = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
